@@ -1,0 +1,390 @@
+#!/usr/bin/env python3
+"""Benchmark of the fp16 GEMM C = A . B^T on GB300.
+
+One step = one GEMM of the workload (default: the 8192^3, fp16-output
+workload with uniform[-1, 1] operands from seed 2) through the C ABI, with the
+operands resident in device memory.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                  [--variant V] [--depth D] [--block-n BN] [--impl ours|reference]
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
+and a device synchronise on both sides, timed with CUDA events on the launch
+stream; max over ranks.  The operands (A + B = 256 MiB at 8192^3) and the
+output (128 MiB) are larger than the 126 MiB L2, so no flush is inserted.
+
+``--impl reference`` times the CPU oracle (the only other implementation of
+this computation) on a bounded sample of the same workload on the host cores.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["csrc/ptx.cuh", "csrc/gemm_common.h", "csrc/device_common.cuh",
+                  "csrc/kernel_ws.cu", "csrc/kernels_ladder.cu", "csrc/api.cu"]
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "tma_pipelined_tensor_fp16_gb300", rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return FALLBACK_PEAKS, "fallback"
+
+
+def load_traffic(workload, kernel_key):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel
+    sources are unchanged since it was taken; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(workload, {}).get(kernel_key)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def find_config(name):
+    from tma_pipelined_tensor_fp16_gb300 import inputs
+    for c in inputs.CONFIGS:
+        if c["name"] == name or name in c["name"]:
+            return c
+    raise SystemExit("unknown config %r; known: %s" % (name, [c["name"] for c in inputs.CONFIGS]))
+
+
+def algorithmic(cfg):
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    out_bytes = 2 if cfg["out"] == "f16" else 4
+    flops = 2.0 * M * N * K
+    nbytes = 2.0 * M * K + 2.0 * N * K + out_bytes * M * N
+    return flops, nbytes
+
+
+# --------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                        rows.append(parts)
+        finally:
+            try:
+                os.unlink(self.path)
+            except OSError:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        sm = [float(r[1]) for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for i, n in enumerate(names):
+                if r[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())
+                if any(r[3].replace(".", "").isdigit() for r in rows) else None,
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------- oracle timing
+
+def time_oracle(cfg, target_s, rows_cap=None):
+    """Time the CPU oracle on whole rows of C for this workload; returns
+    (flops_per_s, threads, rows, seconds)."""
+    import oracle
+    from tma_pipelined_tensor_fp16_gb300 import inputs
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    threads = oracle.default_threads()
+    A, B = inputs.make_operands(M, N, K, cfg["dist"], cfg["seed"])
+    probe = max(1, min(M, threads))
+    t0 = time.perf_counter()
+    oracle.gemm_rows(A, B, 0, probe, threads)
+    dt = time.perf_counter() - t0
+    rows = int(max(probe, min(M, probe * target_s / max(dt, 1e-6))))
+    if rows_cap:
+        rows = min(rows, rows_cap)
+    t0 = time.perf_counter()
+    oracle.gemm_rows(A, B, 0, rows, threads)
+    dt = time.perf_counter() - t0
+    return 2.0 * rows * N * K / dt, threads, rows, dt, (A, B)
+
+
+def run_reference(args, cfg, rank):
+    if rank != 0:
+        return
+    import oracle
+    from tma_pipelined_tensor_fp16_gb300 import inputs
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    A, B = inputs.make_operands(M, N, K, cfg["dist"], cfg["seed"])
+    threads = oracle.default_threads()
+    # size one step (a block of whole rows of C) to about 3 s of host work
+    probe = max(1, min(M, threads))
+    t0 = time.perf_counter()
+    oracle.gemm_rows(A, B, 0, probe, threads)
+    per_row = (time.perf_counter() - t0) / probe
+    rows = int(max(1, min(M, 3.0 / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        oracle.gemm_rows(A, B, 0, max(1, rows // 4), threads)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        r0 = (i * rows) % max(1, M - rows + 1)
+        oracle.gemm_rows(A, B, r0, r0 + rows, threads)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * N * K * args.steps
+    value = flops / dt / 1e12
+    sample = "%d of %d rows of C (all %d columns, K=%d) per step, fp64 accumulate" % (rows, M, N, K)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg["name"], "M": M, "N": N, "K": K, "out": cfg["out"],
+                   "operands": "%s seed %d" % (cfg["dist"], cfg["seed"])},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+METRIC = "fp16 GEMM TFLOP/s at 8192^3 (1 GB300) and % of dense fp16 tensor peak"
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="gemm_8192x8192x8192_f16out")
+    ap.add_argument("--variant", default="auto")
+    ap.add_argument("--depth", type=int, default=0)
+    ap.add_argument("--block-n", type=int, default=0)
+    ap.add_argument("--group-m", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = find_config(args.config)
+
+    if args.impl == "reference":
+        run_reference(args, cfg, rank)
+        return
+
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    import tma_pipelined_tensor_fp16_gb300 as pkg
+    from tma_pipelined_tensor_fp16_gb300 import inputs
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    __graft_entry__.build()
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    A, B = inputs.make_operands(M, N, K, cfg["dist"], cfg["seed"])
+    dA = torch.from_numpy(A.view(np.float16)).cuda()
+    dB = torch.from_numpy(B.view(np.float16)).cuda()
+    out_dt = torch.float16 if cfg["out"] == "f16" else torch.float32
+    dC = torch.empty((M, N), dtype=out_dt, device="cuda")
+    plan = pkg.Plan(M, N, K, out=cfg["out"], variant=args.variant, pipe_depth=args.depth,
+                    block_n=args.block_n, group_m=args.group_m)
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+
+    for _ in range(args.warmup):
+        plan.run(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), sh)
+    torch.cuda.synchronize()
+    if plan.device_status() != 0:
+        raise SystemExit("warm-up failed: " + pkg.gemm_last_error())
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            plan.run(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), sh)
+            ev[i][1].record(stream)
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    if plan.device_status() != 0:
+        raise SystemExit("timed run failed: " + pkg.gemm_last_error())
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if dist is not None:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    flops, nbytes = algorithmic(cfg)
+    ms_per_step = total_ms / args.steps
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    avg_launch_s = statistics.mean(launch_ms) * 1e-3
+
+    # --------------------------------------------------- end to end, host buffers
+    e2e = None
+    if not args.no_e2e:
+        hA = torch.from_numpy(A.view(np.float16)).pin_memory()
+        hB = torch.from_numpy(B.view(np.float16)).pin_memory()
+        hC = torch.empty((M, N), dtype=out_dt).pin_memory()
+        e2e_steps = max(3, min(args.steps, 10))
+        for _ in range(2):
+            plan.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), sh)
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            plan.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), sh)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(A.nbytes + B.nbytes),
+               "d2h_bytes_per_step": int(hC.numel() * hC.element_size()),
+               "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
+               "api": "gemm_run_host (pinned host buffers; copies, kernel and sync inside)"}
+    plan_desc = plan.describe()
+    pcfg = plan.config()
+    plan.close()
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_kind = load_peaks()
+    memory_bound = cfg["name"].startswith("gemm_skinny")
+    kernel_key = "k_ws<%d,%s,%s>" % (pcfg["block_n"], "f16" if cfg["out"] == "f16" else "f32",
+                                      "persistent" if pcfg["variant"] == 5 else "v%d" % pcfg["variant"])
+    traffic = load_traffic(cfg["name"], kernel_key)
+    if memory_bound:
+        achieved = nbytes / avg_launch_s / 1e9
+        peak = float(peaks["hbm_gbs"])
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": "%s hbm_gbs (copy)" % peak_kind}
+    else:
+        achieved = flops / avg_launch_s / 1e12
+        peak = float(peaks["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": "%s bf16_tflops burst (fp16 dense rate = bf16 rate)" % peak_kind}
+    roof["algorithmic_per_launch"] = flops if not memory_bound else nbytes
+    roof["avg_launch_ms"] = avg_launch_s * 1e3
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        fps, threads, rows, secs, _ = time_oracle(cfg, args.cpu_seconds)
+        cpu = {"value": fps / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": "%d of %d rows of C (all %d columns, K=%d), fp64 accumulate, %.1f s"
+                         % (rows, M, N, K, secs)}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": cfg["name"], "M": M, "N": N, "K": K, "out": cfg["out"],
+                   "operands": "%s seed %d" % (cfg["dist"], cfg["seed"]),
+                   "l2": "no flush: A+B+C exceed the L2" if M * K * 2 + N * K * 2 > 130e6
+                   else "operands fit in L2 (warm)",
+                   "plan": plan_desc},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "tflops_per_launch_median": flops / (statistics.median(launch_ms) * 1e-3) / 1e12,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,169 @@
+/*
+ * tmagemm.h -- C ABI of the GB300 (sm_103a) TMA-pipelined fp16 GEMM.
+ *
+ * Operation ("GEMM II -- pipelining with TMA", Step 4: the A tile is loaded at
+ * {m, k} and the B tile at {n, k}, each BLK x BLK_K, fp16; the baseline
+ * paragraph: fp32 accumulate; the TMA-store epilogue: the accumulator is
+ * narrowed to the output dtype):
+ *
+ *     C[m][n] = sum_{k < K} A[m][k] * B[n][k]
+ *
+ *   A : M x K fp16, row-major (element (m,k) at A[m*K + k])
+ *   B : N x K fp16, row-major, i.e. B^T is K-major (element (n,k) at B[n*K + k])
+ *   C : M x N, row-major (ldc = N), fp32 or fp16 (round to nearest even)
+ *   accumulation in fp32 on the tensor cores.
+ *
+ * Everything runs on one GPU, in the library's own CUDA kernels; there is no
+ * CPU fallback: calls fail with an error code when no device is present.
+ *
+ * Threading: plans are independent; one plan must not be used by two host
+ * threads at once.  Errors: every function that can fail returns a gemm_status
+ * (or NULL) and leaves a message for gemm_last_error() (thread-local).
+ */
+#ifndef TMAGEMM_H
+#define TMAGEMM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TMAGEMM_API __attribute__((visibility("default")))
+#else
+#define TMAGEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gemm_plan gemm_plan; /* opaque; owned by the library */
+
+typedef enum { GEMM_OUT_F32 = 0, GEMM_OUT_F16 = 1 } gemm_dtype;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1, /* NULL pointer, non-positive size, bad option value */
+    GEMM_ERR_UNSUPPORTED = 2, /* shape/alignment the TMA path cannot take, or a
+                                 stage count that does not fit shared memory */
+    GEMM_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+    GEMM_ERR_TIMEOUT = 4,     /* a kernel wait exceeded its bound (see
+                                 gemm_get_device_status) */
+    GEMM_ERR_NO_DEVICE = 5    /* no usable CUDA device / wrong architecture */
+} gemm_status;
+
+/* Kernel variants: the ablation ladder of "GEMM II -- pipelining with TMA"
+ * (Steps 3-6) plus the warp-specialised forms. */
+typedef enum {
+    GEMM_VAR_AUTO = 0,              /* = GEMM_VAR_PERSISTENT */
+    GEMM_VAR_SYNC_TILED = 1,        /* Step 3: thread copies, one MMA at a time */
+    GEMM_VAR_TMA_SERIAL = 2,        /* Step 4: TMA load + expect_tx, serial loop */
+    GEMM_VAR_PIPELINED = 3,         /* Step 5: PIPE_DEPTH ring, lock-step prefetch */
+    GEMM_VAR_WS_PIPELINED = 4,      /* producer warp / MMA warp / epilogue warps,
+                                       full+empty ring, one tile per CTA */
+    GEMM_VAR_PERSISTENT = 5,        /* warp-specialised, grid = SM count, grouped
+                                       raster, two TMEM accumulators */
+    GEMM_VAR_PERSISTENT_LOCKSTEP = 6 /* Step 6 as printed: persistent CTAs running
+                                       the lock-step Step-5 loop */
+} gemm_variant;
+
+/* Plan options; a zero field means "choose automatically". */
+typedef struct {
+    int variant;        /* gemm_variant */
+    int pipe_depth;     /* shared-memory stages, 1..8 (ring variants) */
+    int block_n;        /* output tile width: 64, 128 or 256 (tile height is 128) */
+    int group_m;        /* raster group height in M tiles (default 8) */
+    int grid;           /* persistent variants: CTAs to launch (default: SM count) */
+    int wait_budget_ms; /* bound on any single in-kernel wait (default 2000) */
+    int debug_stall;    /* 1: the producer first waits on a barrier that nothing
+                           completes, so the run ends in GEMM_ERR_TIMEOUT (for
+                           testing the watchdog; warp-specialised variants) */
+} gemm_options;
+
+/* Resolved configuration of a plan (also returned by gemm_select_config). */
+typedef struct {
+    int variant;
+    int block_m, block_n, block_k;
+    int pipe_depth;
+    int group_m;
+    int grid;           /* CTAs launched */
+    int threads;        /* threads per CTA */
+    int tiles_m, tiles_n, num_tiles, k_blocks;
+    int smem_bytes;     /* dynamic shared memory per CTA */
+    int tmem_cols;      /* TMEM columns allocated per CTA */
+    int tx_bytes;       /* bytes one stage's barrier expects (A + B tile) */
+} gemm_config;
+
+/* Create a plan for C[M x N] = A[M x K] . B[N x K]^T on the current CUDA
+ * device.  dtype_out is a gemm_dtype.  Preconditions: M, N, K >= 1 and
+ * < 2^31; K % 8 == 0 and N * sizeof(out) % 16 == 0 (TMA global strides are
+ * multiples of 16 bytes, "05 Async Data Movement - TMA", the tensor-map
+ * descriptor; a TMA copy must start on a 16-byte boundary).  Returns NULL on
+ * error (gemm_last_status() / gemm_last_error() say why).  The plan owns host
+ * state and a 32-byte device status record; nothing else is allocated. */
+TMAGEMM_API gemm_plan* gemm_create_plan(int64_t M, int64_t N, int64_t K, int dtype_out);
+
+/* Same with options (NULL = all automatic).  An explicit pipe_depth whose ring
+ * does not fit in shared memory fails with GEMM_ERR_UNSUPPORTED. */
+TMAGEMM_API gemm_plan* gemm_create_plan_ex(int64_t M, int64_t N, int64_t K, int dtype_out,
+                               const gemm_options* opts);
+
+/* Enqueue C = A . B^T on `cuda_stream` (a cudaStream_t; NULL = legacy default
+ * stream).  A, B, C are DEVICE pointers owned by the caller, 16-byte aligned,
+ * laid out as above; C's rows and columns beyond M x N are never written.
+ * Asynchronous: returns after the launch.  Argument and launch errors are
+ * returned at once; an in-kernel timeout is reported by
+ * gemm_get_device_status after the caller has synchronised the stream.  The
+ * plan must be used on the device it was created on. */
+TMAGEMM_API int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_stream);
+
+/* End-to-end variant of gemm_run for HOST buffers: copies A and B to device
+ * buffers owned by the plan (allocated on first use, reused after), runs the
+ * GEMM on `cuda_stream`, copies C back and synchronises the stream.  A, B, C
+ * are host pointers (page-locked memory gives full copy bandwidth).  Returns
+ * GEMM_ERR_TIMEOUT if the kernel's watchdog fired. */
+TMAGEMM_API int gemm_run_host(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_stream);
+
+/* Read (and clear) the plan's device status record.  Call after
+ * synchronising the stream(s) the plan ran on.  Returns GEMM_OK or
+ * GEMM_ERR_TIMEOUT (a wait ran past wait_budget_ms; the kernel then skipped
+ * its remaining work, freed TMEM and exited, so C is incomplete), or
+ * GEMM_ERR_CUDA if the read itself failed. */
+TMAGEMM_API int gemm_get_device_status(gemm_plan* plan);
+
+/* Free the plan (NULL is allowed). */
+TMAGEMM_API void gemm_destroy(gemm_plan* plan);
+
+/* Message / code of the last failing call on this host thread. */
+TMAGEMM_API const char* gemm_last_error(void);
+TMAGEMM_API int gemm_last_status(void);
+
+/* Human-readable one-line description of the plan (variant, tile, depth,
+ * shared memory, grid).  The string is owned by the plan. */
+TMAGEMM_API const char* gemm_plan_describe(const gemm_plan* plan);
+
+/* The plan's resolved configuration. */
+TMAGEMM_API int gemm_plan_config(const gemm_plan* plan, gemm_config* out);
+
+/* ---- host-only helpers (no GPU needed; used by tests and tools) ---- */
+
+/* Resolve options into a configuration for a device with `sm_count` SMs and
+ * `smem_optin` bytes of opt-in shared memory per block, exactly as
+ * gemm_create_plan_ex does.  Returns a gemm_status. */
+TMAGEMM_API int gemm_select_config(int64_t M, int64_t N, int64_t K, int dtype_out, const gemm_options* opts,
+                       int sm_count, int smem_optin, gemm_config* out);
+
+/* Output tile (m_tile, n_tile) of linear tile index `tile` in the grouped
+ * raster order the kernels use ("GEMM II -- pipelining with TMA", Step 6,
+ * l2_group_size).  Returns GEMM_ERR_INVALID_ARG if tile is out of range. */
+TMAGEMM_API int gemm_schedule_tile(const gemm_config* cfg, int64_t tile, int* m_tile, int* n_tile);
+
+/* Byte offset of logical byte `byte_in_row` of row `row` inside a
+ * 1024-byte-aligned tile of 128-byte rows stored with the 128-byte swizzle
+ * ("05 Async Data Movement - TMA", "How TMA Writes a Swizzled Layout"), as
+ * the thread-copy variant writes it and the TMA engine lays it out. */
+TMAGEMM_API int64_t gemm_sw128_offset(int64_t row, int64_t byte_in_row);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TMAGEMM_H */

@@ -1,0 +1,170 @@
+"""CPU-side checks of the C ABI and the host logic the kernels share: the
+library builds and exports every entry point declared in include/*.h, the
+configuration choice and its argument checks, the grouped raster scheduler,
+the 128-byte swizzle map, and the stage byte count -- each against values the
+pages print (tests/golden/) or against properties that must hold.
+"""
+import glob
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def b():
+    from tma_pipelined_tensor_fp16_gb300 import build, binding
+    build.build()
+    return binding
+
+
+def _declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names += re.findall(r"^TMAGEMM_API\s+[\w\s\*]+?\b(\w+)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+def _golden(name):
+    vals = {}
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.split("#", 1)[0].strip()
+        if line:
+            k, v = line.split("=", 1)
+            vals[k.strip()] = v.strip()
+    return vals
+
+
+def test_library_exports_every_declared_symbol(b):
+    declared = _declared_functions()
+    assert len(declared) >= 13
+    out = subprocess.run(["nm", "-D", "--defined-only", b.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (\w+)$", out, re.M))
+    missing = [n for n in declared if n not in exported]
+    assert not missing, missing
+    lib = b.lib()
+    for n in declared:
+        assert getattr(lib, n) is not None
+
+
+def test_create_plan_without_device_reports_no_device(b):
+    assert not b.gemm_create_plan(256, 256, 256, b.GEMM_OUT_F32)
+    assert b.gemm_last_status() == b.GEMM_ERR_NO_DEVICE
+    assert "device" in b.last_error()
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, 8, 8, 0), 1), ((8, -1, 8, 0), 1), ((8, 8, 8, 7), 1),
+    ((8, 8, 12, 0), 2),        # K not a multiple of 8 (16-byte TMA stride)
+    ((8, 6, 8, 0), 2),         # N*4 bytes not a multiple of 16
+    ((8, 12, 8, 1), 2),        # N*2 bytes not a multiple of 16
+    ((8, 12, 8, 0), 0),        # N*4 = 48 bytes: fine for fp32 output
+])
+def test_argument_checks(b, args, status):
+    st, _ = b.gemm_select_config(*args)
+    assert st == status, b.last_error()
+    # plan creation reports shape errors before looking for a device
+    if status:
+        assert not b.gemm_create_plan(*args)
+        assert b.gemm_last_status() == status
+
+
+def test_depth_that_does_not_fit_is_rejected(b):
+    st, _ = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(pipe_depth=5, block_n=256))
+    assert st == b.GEMM_ERR_UNSUPPORTED and "does not fit" in b.last_error()
+    st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(pipe_depth=4, block_n=256))
+    assert st == 0 and c.smem_bytes <= 232448
+
+
+def test_headline_configuration(b):
+    st, c = b.gemm_select_config(8192, 8192, 8192, 1)
+    assert st == 0
+    assert c.variant == b.GEMM_VAR_PERSISTENT
+    assert (c.block_m, c.block_n, c.block_k) == (128, 256, 64)
+    assert c.pipe_depth == 4 and c.grid == 152 and c.threads == 192
+    assert c.num_tiles == 2048 and c.k_blocks == 128 and c.tmem_cols == 512
+
+
+def test_stage_byte_count_matches_page_formula(b):
+    # byte_count = (BLK_M*BLK_K + BLK_N*BLK_K) * 2 for fp16 tiles
+    g = _golden("p1_step4_byte_count.txt")
+    for bn in (64, 128, 256):
+        st, c = b.gemm_select_config(1024, 1024, 1024, 1, b.make_options(block_n=bn))
+        assert st == 0
+        assert c.tx_bytes == (c.block_m * c.block_k + c.block_n * c.block_k) * int(g["F16_SIZE"])
+    # the 2048 + 2048 = 4096 worked example: two 2048-byte tiles on one barrier
+    assert int(g["example_tile_bytes"]) * 2 == int(g["example_expect_tx"])
+
+
+def test_tile_arithmetic_of_the_persistent_step(b):
+    g = _golden("p1_step6_tile_arithmetic.txt")
+    n = int(g["matrix"])
+    st, c = b.gemm_select_config(n, n, n, 1, b.make_options(block_n=int(g["tile"]), grid=int(
+        g["sm_count"]), variant="persistent"), sm_count=int(g["sm_count"]))
+    assert st == 0
+    assert c.num_tiles == int(g["tiles"])
+    assert round(c.num_tiles / c.grid) == int(g["tiles_per_cta"])
+
+
+@pytest.mark.parametrize("M,N,group", [(4096, 4096, 8), (4000, 3000, 8), (64, 16384, 8),
+                                       (1000, 72, 3), (128 * 13, 256 * 5, 4)])
+def test_raster_covers_every_tile_once_in_group_order(b, M, N, group):
+    st, c = b.gemm_select_config(M, N, 64, 1, b.make_options(group_m=group, block_n=256))
+    assert st == 0
+    seen = np.zeros((c.tiles_m, c.tiles_n), dtype=np.int64)
+    prev = None
+    for t in range(c.num_tiles):
+        st, m, n = b.gemm_schedule_tile(c, t)
+        assert st == 0
+        seen[m, n] += 1
+        # consecutive tiles stay inside one group of `group` M-tiles
+        g0 = (m // group)
+        if prev is not None:
+            assert g0 >= prev[0]
+            if g0 == prev[0]:
+                assert n >= prev[2]
+        prev = (g0, m, n)
+    assert (seen == 1).all()
+    st, _, _ = b.gemm_schedule_tile(c, c.num_tiles)
+    assert st == b.GEMM_ERR_INVALID_ARG
+
+
+def test_persistent_ctas_partition_the_tiles(b):
+    st, c = b.gemm_select_config(4000, 3000, 5000, 0)
+    assert st == 0
+    owner = {}
+    for cta in range(c.grid):
+        for t in range(cta, c.num_tiles, c.grid):
+            assert t not in owner
+            owner[t] = cta
+    assert len(owner) == c.num_tiles
+
+
+def test_swizzle_map_matches_page_rule_and_bank_analysis(b):
+    g = _golden("p2_swizzle_128b.txt")
+    # physical 16-byte sector = logical sector XOR (row mod 8), inside an
+    # 8-row x 128-byte atom; bytes inside a sector keep their order
+    for row in range(16):
+        for byte in range(128):
+            off = b.gemm_sw128_offset(row, byte)
+            assert off // 128 == row
+            assert (off % 128) // 16 == (byte // 16) ^ (row % 8)
+            assert off % 16 == byte % 16
+    # eight consecutive rows reading one logical sector column hit eight
+    # distinct 4-bank sectors (no conflict) in the 128-byte-grouped layout
+    for col in range(8):
+        sectors = {(b.gemm_sw128_offset(r, col * 16) // 16) % 8 for r in range(8)}
+        assert len(sectors) == int(g["grouped_distinct_bank_sectors"])
+    # the page's ungrouped 256-byte-row comparison: XOR term advances by two
+    # per row, leaving only four distinct sectors (a 2-way conflict)
+    for col in range(16):
+        sectors = {((col % 8) ^ ((2 * r + col // 8) % 8)) for r in range(8)}
+        assert len(sectors) == int(g["ungrouped_distinct_bank_sectors"])
+    assert b.gemm_sw128_offset(0, 128) == -1

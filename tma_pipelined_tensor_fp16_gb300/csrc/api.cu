@@ -1,0 +1,490 @@
+// api.cu -- host runtime behind the C ABI (include/tmagemm.h): argument
+// checks, configuration choice, TMA tensor-map encoding, the device status
+// record and the kernel launch.  Control crosses to the device only at the
+// launch inside gemm_run.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/tmagemm.h"
+#include "gemm_common.h"
+#include "launch.h"
+
+using namespace tg;
+
+namespace {
+
+thread_local std::string g_err;
+thread_local int g_status = GEMM_OK;
+
+int fail(int status, const std::string& msg)
+{
+    g_status = status;
+    g_err = msg;
+    return status;
+}
+
+int ok()
+{
+    g_status = GEMM_OK;
+    g_err.clear();
+    return GEMM_OK;
+}
+
+int cuda_fail(const char* what, cudaError_t e)
+{
+    return fail(GEMM_ERR_CUDA, std::string(what) + ": " + cudaGetErrorName(e) + " (" +
+                                   cudaGetErrorString(e) + ")");
+}
+
+const char* variant_name(int v)
+{
+    switch (v) {
+    case VAR_SYNC_TILED: return "sync_tiled";
+    case VAR_TMA_SERIAL: return "tma_serial";
+    case VAR_PIPELINED: return "pipelined";
+    case VAR_WS_PIPELINED: return "ws_pipelined";
+    case VAR_PERSISTENT: return "persistent";
+    case VAR_PERSISTENT_LOCKSTEP: return "persistent_lockstep";
+    default: return "?";
+    }
+}
+
+bool is_ws(int v) { return v == VAR_WS_PIPELINED || v == VAR_PERSISTENT; }
+bool is_persistent(int v) { return v == VAR_PERSISTENT || v == VAR_PERSISTENT_LOCKSTEP; }
+bool has_ring(int v) { return v != VAR_SYNC_TILED && v != VAR_TMA_SERIAL; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Fraction of launched tile slots that do work when `tiles` tiles run in
+// waves over `sms` SMs.
+double wave_efficiency(int64_t tiles, int sms)
+{
+    const int64_t waves = ceil_div(tiles, sms);
+    return static_cast<double>(tiles) / static_cast<double>(waves * sms);
+}
+
+int choose_block_n(int variant, int64_t M, int64_t N, int sms)
+{
+    if (!is_persistent(variant) && variant != VAR_WS_PIPELINED) return 128;
+    const int64_t tm = ceil_div(M, BLK_M);
+    if (tm * ceil_div(N, 256) >= sms) return 256;
+    // Few tiles: trade tile width (operand reuse per tile) against filling
+    // the SMs.  Relative per-tile efficiency of narrower tiles is an estimate.
+    const int cand[3] = {256, 128, 64};
+    const double tile_eff[3] = {1.0, 0.95, 0.85};
+    int best = 256;
+    double best_score = -1.0;
+    for (int i = 0; i < 3; ++i) {
+        const double s = wave_efficiency(tm * ceil_div(N, cand[i]), sms) * tile_eff[i];
+        if (s > best_score + 1e-9) {
+            best_score = s;
+            best = cand[i];
+        }
+    }
+    return best;
+}
+
+int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_options* o,
+                       int sms, int smem_optin, gemm_config* c)
+{
+    gemm_options opts;
+    std::memset(&opts, 0, sizeof(opts));
+    if (o) opts = *o;
+    if (!c) return fail(GEMM_ERR_INVALID_ARG, "config output pointer is NULL");
+    const int64_t LIM = (int64_t(1) << 31) - 1;
+    if (M < 1 || N < 1 || K < 1 || M > LIM || N > LIM || K > LIM)
+        return fail(GEMM_ERR_INVALID_ARG, "M, N, K must be in [1, 2^31-1]");
+    if (dtype != GEMM_OUT_F32 && dtype != GEMM_OUT_F16)
+        return fail(GEMM_ERR_INVALID_ARG, "dtype_out must be GEMM_OUT_F32 (0) or GEMM_OUT_F16 (1)");
+    if (K % 8 != 0)
+        return fail(GEMM_ERR_UNSUPPORTED,
+                    "K must be a multiple of 8: the TMA row stride of A and B (K*2 bytes) must be a multiple of 16 bytes");
+    const int elt = dtype == GEMM_OUT_F16 ? 2 : 4;
+    if ((N * elt) % 16 != 0)
+        return fail(GEMM_ERR_UNSUPPORTED,
+                    "N * sizeof(output) must be a multiple of 16 bytes (TMA row stride of C)");
+    if (opts.variant < 0 || opts.variant > VAR_PERSISTENT_LOCKSTEP)
+        return fail(GEMM_ERR_INVALID_ARG, "unknown variant");
+    if (opts.pipe_depth < 0 || opts.pipe_depth > MAX_STAGES)
+        return fail(GEMM_ERR_INVALID_ARG, "pipe_depth must be 0 (auto) or 1..8");
+    if (opts.block_n != 0 && opts.block_n != 64 && opts.block_n != 128 && opts.block_n != 256)
+        return fail(GEMM_ERR_INVALID_ARG, "block_n must be 0 (auto), 64, 128 or 256");
+    if (opts.group_m < 0 || opts.grid < 0 || opts.wait_budget_ms < 0)
+        return fail(GEMM_ERR_INVALID_ARG, "group_m, grid and wait_budget_ms must be >= 0");
+    if (sms < 1 || smem_optin < 1) return fail(GEMM_ERR_INVALID_ARG, "bad device limits");
+
+    const int variant = opts.variant == VAR_AUTO ? VAR_PERSISTENT : opts.variant;
+    if (opts.debug_stall && !is_ws(variant))
+        return fail(GEMM_ERR_INVALID_ARG, "debug_stall needs a warp-specialised variant");
+    const int bn = opts.block_n ? opts.block_n : choose_block_n(variant, M, N, sms);
+    const int staging = variant == VAR_SYNC_TILED ? 0 : NUM_STAGING;
+
+    int depth;
+    if (!has_ring(variant)) {
+        if (opts.pipe_depth > 1)
+            return fail(GEMM_ERR_INVALID_ARG, "this variant has a single stage (pipe_depth 0 or 1)");
+        depth = 1;
+    } else if (opts.pipe_depth) {
+        depth = opts.pipe_depth;
+        const uint32_t need = smem_layout(depth, bn, staging).total;
+        if (need > static_cast<uint32_t>(smem_optin)) {
+            char buf[200];
+            std::snprintf(buf, sizeof(buf),
+                          "pipe_depth %d with a 128x%d tile does not fit: %u bytes of shared memory > %d available",
+                          depth, bn, need, smem_optin);
+            return fail(GEMM_ERR_UNSUPPORTED, buf);
+        }
+    } else {
+        depth = 0;
+        for (int d = MAX_STAGES; d >= 1; --d)
+            if (smem_layout(d, bn, staging).total <= static_cast<uint32_t>(smem_optin)) {
+                depth = d;
+                break;
+            }
+        if (depth == 0) return fail(GEMM_ERR_UNSUPPORTED, "no stage count fits shared memory");
+    }
+
+    const int64_t tm = ceil_div(M, BLK_M), tn = ceil_div(N, bn);
+    const int64_t tiles = tm * tn;
+    if (tiles > LIM) return fail(GEMM_ERR_UNSUPPORTED, "too many output tiles");
+    uint32_t smem = smem_layout(depth, bn, staging).total;
+    if (is_persistent(variant)) {
+        // One resident CTA per SM: ask for more than half of the SM's shared
+        // memory so that a second CTA can never be co-scheduled.
+        const uint32_t half = static_cast<uint32_t>(smem_optin) / 2u + 1024u;
+        if (smem < half) smem = half;
+        if (smem > static_cast<uint32_t>(smem_optin)) smem = static_cast<uint32_t>(smem_optin);
+    }
+
+    std::memset(c, 0, sizeof(*c));
+    c->variant = variant;
+    c->block_m = BLK_M;
+    c->block_n = bn;
+    c->block_k = BLK_K;
+    c->pipe_depth = depth;
+    c->group_m = opts.group_m ? opts.group_m : 8;
+    c->tiles_m = static_cast<int>(tm);
+    c->tiles_n = static_cast<int>(tn);
+    c->num_tiles = static_cast<int>(tiles);
+    c->k_blocks = static_cast<int>(ceil_div(K, BLK_K));
+    if (is_persistent(variant)) {
+        int64_t g = opts.grid ? opts.grid : sms;
+        if (g > tiles) g = tiles;
+        c->grid = static_cast<int>(g);
+    } else {
+        c->grid = static_cast<int>(tiles);
+    }
+    c->threads = is_ws(variant) ? 192 : 128;
+    c->smem_bytes = static_cast<int>(smem);
+    c->tmem_cols = (variant == VAR_PERSISTENT) ? 2 * bn : bn;
+    c->tx_bytes = static_cast<int>(stage_tx_bytes(bn));
+    return ok();
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D tensor map over a row-major matrix with `rows` rows of `cols` elements
+// (row pitch `pitch_bytes`), box = box_cols x box_rows, 128-byte swizzle,
+// out-of-bounds elements read as zero.
+int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t cols,
+              uint64_t rows, uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows,
+              const char* what)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+    if (!enc) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {pitch_bytes};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char buf[160];
+        std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what,
+                      static_cast<int>(r));
+        return fail(GEMM_ERR_CUDA, buf);
+    }
+    return GEMM_OK;
+}
+
+}  // namespace
+
+struct gemm_plan {
+    int64_t M, N, K;
+    int dtype;
+    gemm_config cfg;
+    int device;
+    unsigned long long budget_ns;
+    int debug_stall;
+    DevStatus* d_status;
+    int epoch;
+    // tensor maps for the last (A, B, C) triple
+    const void* mapA_ptr;
+    const void* mapB_ptr;
+    const void* mapC_ptr;
+    CUtensorMap tmA, tmB, tmC;
+    // device buffers of gemm_run_host
+    void* hA;
+    void* hB;
+    void* hC;
+    std::string desc;
+};
+
+extern "C" {
+
+int gemm_select_config(int64_t M, int64_t N, int64_t K, int dtype_out, const gemm_options* opts,
+                       int sm_count, int smem_optin, gemm_config* out)
+{
+    return select_config_impl(M, N, K, dtype_out, opts, sm_count, smem_optin, out);
+}
+
+gemm_plan* gemm_create_plan_ex(int64_t M, int64_t N, int64_t K, int dtype_out,
+                               const gemm_options* opts)
+{
+    // Shape/option errors are reported before touching the device.
+    gemm_config probe;
+    if (select_config_impl(M, N, K, dtype_out, opts, 148, 232448, &probe) != GEMM_OK)
+        return nullptr;
+
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        fail(GEMM_ERR_NO_DEVICE, std::string("no CUDA device: ") + cudaGetErrorString(e));
+        return nullptr;
+    }
+    int major = 0, minor = 0, sms = 0, smem_optin = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    e = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) {
+        cuda_fail("cudaDeviceGetAttribute", e);
+        return nullptr;
+    }
+    if (major != 10 || minor != 3) {
+        char buf[160];
+        std::snprintf(buf, sizeof(buf),
+                      "device %d is sm_%d%d; this library is built for sm_103a (GB300) only", dev,
+                      major, minor);
+        fail(GEMM_ERR_NO_DEVICE, buf);
+        return nullptr;
+    }
+    gemm_plan* p = new gemm_plan();
+    p->M = M;
+    p->N = N;
+    p->K = K;
+    p->dtype = dtype_out;
+    p->device = dev;
+    if (select_config_impl(M, N, K, dtype_out, opts, sms, smem_optin, &p->cfg) != GEMM_OK) {
+        delete p;
+        return nullptr;
+    }
+    const int budget_ms = (opts && opts->wait_budget_ms) ? opts->wait_budget_ms : 2000;
+    p->budget_ns = static_cast<unsigned long long>(budget_ms) * 1000000ull;
+    p->debug_stall = opts ? opts->debug_stall : 0;
+    e = cudaMalloc(&p->d_status, sizeof(DevStatus));
+    if (e == cudaSuccess) e = cudaMemset(p->d_status, 0, sizeof(DevStatus));
+    if (e != cudaSuccess) {
+        cuda_fail("allocating the device status record", e);
+        if (p->d_status) cudaFree(p->d_status);
+        delete p;
+        return nullptr;
+    }
+    char buf[320];
+    const gemm_config& c = p->cfg;
+    std::snprintf(buf, sizeof(buf),
+                  "variant=%s tile=%dx%dx%d pipe_depth=%d smem=%d grid=%d threads=%d tiles=%d (%dx%d) "
+                  "k_blocks=%d tmem_cols=%d group_m=%d out=%s",
+                  variant_name(c.variant), c.block_m, c.block_n, c.block_k, c.pipe_depth,
+                  c.smem_bytes, c.grid, c.threads, c.num_tiles, c.tiles_m, c.tiles_n, c.k_blocks,
+                  c.tmem_cols, c.group_m, dtype_out == GEMM_OUT_F16 ? "f16" : "f32");
+    p->desc = buf;
+    ok();
+    return p;
+}
+
+gemm_plan* gemm_create_plan(int64_t M, int64_t N, int64_t K, int dtype_out)
+{
+    return gemm_create_plan_ex(M, N, K, dtype_out, nullptr);
+}
+
+int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_stream)
+{
+    if (!plan) return fail(GEMM_ERR_INVALID_ARG, "plan is NULL");
+    if (!A || !B || !C) return fail(GEMM_ERR_INVALID_ARG, "A, B and C must be non-NULL");
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+         reinterpret_cast<uintptr_t>(C)) & 15u)
+        return fail(GEMM_ERR_UNSUPPORTED, "A, B and C must be 16-byte aligned (TMA)");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+    if (dev != plan->device)
+        return fail(GEMM_ERR_INVALID_ARG, "plan was created on another device");
+
+    const gemm_config& c = plan->cfg;
+    if (A != plan->mapA_ptr || B != plan->mapB_ptr || C != plan->mapC_ptr) {
+        int r = encode_2d(&plan->tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, plan->K, plan->M,
+                          plan->K * 2, BLK_K, BLK_M, "A");
+        if (r == GEMM_OK)
+            r = encode_2d(&plan->tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, plan->K, plan->N,
+                          plan->K * 2, BLK_K, c.block_n, "B");
+        if (r == GEMM_OK) {
+            if (plan->dtype == GEMM_OUT_F16)
+                r = encode_2d(&plan->tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, plan->N, plan->M,
+                              plan->N * 2, 64, BLK_M, "C");
+            else
+                r = encode_2d(&plan->tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, plan->N, plan->M,
+                              plan->N * 4, 32, BLK_M, "C");
+        }
+        if (r != GEMM_OK) {
+            plan->mapA_ptr = plan->mapB_ptr = plan->mapC_ptr = nullptr;
+            return r;
+        }
+        plan->mapA_ptr = A;
+        plan->mapB_ptr = B;
+        plan->mapC_ptr = C;
+    }
+
+    LaunchSpec s;
+    s.variant = c.variant;
+    s.block_n = c.block_n;
+    s.f16out = plan->dtype == GEMM_OUT_F16;
+    s.grid = c.grid;
+    s.threads = c.threads;
+    s.smem_bytes = static_cast<unsigned>(c.smem_bytes);
+    s.tmA = &plan->tmA;
+    s.tmB = &plan->tmB;
+    s.tmC = &plan->tmC;
+    Params& p = s.p;
+    p.M = static_cast<int>(plan->M);
+    p.N = static_cast<int>(plan->N);
+    p.K = static_cast<int>(plan->K);
+    p.tiles_m = c.tiles_m;
+    p.tiles_n = c.tiles_n;
+    p.num_tiles = c.num_tiles;
+    p.k_blocks = c.k_blocks;
+    p.group_m = c.group_m;
+    p.pipe_depth = c.pipe_depth;
+    p.A = A;
+    p.B = B;
+    p.C = C;
+    p.status = plan->d_status;
+    if (++plan->epoch <= 0) plan->epoch = 1;
+    p.epoch = plan->epoch;
+    p.budget_ns = plan->budget_ns;
+    p.debug_stall = plan->debug_stall;
+
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    e = is_ws(c.variant) ? launch_ws(s, stream) : launch_ladder(s, stream);
+    if (e != cudaSuccess) return cuda_fail("kernel launch", e);
+    return ok();
+}
+
+int gemm_get_device_status(gemm_plan* plan)
+{
+    if (!plan) return fail(GEMM_ERR_INVALID_ARG, "plan is NULL");
+    DevStatus st;
+    cudaError_t e = cudaMemcpy(&st, plan->d_status, sizeof(st), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail("reading the device status record", e);
+    if (st.code == DEV_OK) return ok();
+    DevStatus zero;
+    std::memset(&zero, 0, sizeof(zero));
+    zero.abort_epoch = st.abort_epoch;  // keep: a stale epoch never matches a new run
+    cudaMemcpy(plan->d_status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    char buf[200];
+    std::snprintf(buf, sizeof(buf),
+                  "kernel wait timed out (where=%d block=%d tile=%d k_block=%d); the run was abandoned",
+                  st.where, st.block, st.tile, st.kblock);
+    return fail(st.code == DEV_TIMEOUT ? GEMM_ERR_TIMEOUT : GEMM_ERR_CUDA, buf);
+}
+
+int gemm_run_host(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_stream)
+{
+    if (!plan) return fail(GEMM_ERR_INVALID_ARG, "plan is NULL");
+    if (!A || !B || !C) return fail(GEMM_ERR_INVALID_ARG, "A, B and C must be non-NULL");
+    const size_t bytesA = static_cast<size_t>(plan->M) * plan->K * 2;
+    const size_t bytesB = static_cast<size_t>(plan->N) * plan->K * 2;
+    const size_t bytesC =
+        static_cast<size_t>(plan->M) * plan->N * (plan->dtype == GEMM_OUT_F16 ? 2 : 4);
+    cudaError_t e = cudaSuccess;
+    if (!plan->hA) e = cudaMalloc(&plan->hA, bytesA);
+    if (e == cudaSuccess && !plan->hB) e = cudaMalloc(&plan->hB, bytesB);
+    if (e == cudaSuccess && !plan->hC) e = cudaMalloc(&plan->hC, bytesC);
+    if (e != cudaSuccess) return cuda_fail("allocating device buffers for gemm_run_host", e);
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    e = cudaMemcpyAsync(plan->hA, A, bytesA, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(plan->hB, B, bytesB, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail("host-to-device copy", e);
+    int r = gemm_run(plan, plan->hA, plan->hB, plan->hC, cuda_stream);
+    if (r != GEMM_OK) return r;
+    e = cudaMemcpyAsync(C, plan->hC, bytesC, cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return cuda_fail("device-to-host copy", e);
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
+    return gemm_get_device_status(plan);
+}
+
+void gemm_destroy(gemm_plan* plan)
+{
+    if (!plan) return;
+    if (plan->d_status) cudaFree(plan->d_status);
+    if (plan->hA) cudaFree(plan->hA);
+    if (plan->hB) cudaFree(plan->hB);
+    if (plan->hC) cudaFree(plan->hC);
+    delete plan;
+}
+
+const char* gemm_last_error(void) { return g_err.c_str(); }
+
+int gemm_last_status(void) { return g_status; }
+
+const char* gemm_plan_describe(const gemm_plan* plan)
+{
+    return plan ? plan->desc.c_str() : "(null plan)";
+}
+
+int gemm_plan_config(const gemm_plan* plan, gemm_config* out)
+{
+    if (!plan || !out) return fail(GEMM_ERR_INVALID_ARG, "plan or out is NULL");
+    *out = plan->cfg;
+    return ok();
+}
+
+int gemm_schedule_tile(const gemm_config* cfg, int64_t tile, int* m_tile, int* n_tile)
+{
+    if (!cfg || !m_tile || !n_tile) return fail(GEMM_ERR_INVALID_ARG, "NULL argument");
+    if (tile < 0 || tile >= cfg->num_tiles || cfg->group_m < 1)
+        return fail(GEMM_ERR_INVALID_ARG, "tile index out of range");
+    raster_tile(static_cast<int>(tile), cfg->tiles_m, cfg->tiles_n, cfg->group_m, *m_tile,
+                *n_tile);
+    return ok();
+}
+
+int64_t gemm_sw128_offset(int64_t row, int64_t byte_in_row)
+{
+    if (row < 0 || byte_in_row < 0 || byte_in_row >= 128) return -1;
+    return static_cast<int64_t>(sw128_offset(static_cast<uint32_t>(row),
+                                             static_cast<uint32_t>(byte_in_row)));
+}
+
+}  // extern "C"

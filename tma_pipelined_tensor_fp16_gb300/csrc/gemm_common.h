@@ -1,0 +1,142 @@
+// gemm_common.h -- definitions shared by the host runtime and the kernels:
+// tile constants, the launch parameter block, the device status record, the
+// persistent tile scheduler's raster and the 128-byte swizzle map.
+#pragma once
+
+#include <cstdint>
+
+#ifdef __CUDACC__
+#define TG_HD __host__ __device__ __forceinline__
+#else
+#define TG_HD inline
+#endif
+
+namespace tg {
+
+// Output tile rows per CTA (one tcgen05.mma covers BLK_M x BLK_N x 16) and the
+// K extent of one pipeline stage: 64 fp16 = one 128-byte swizzle row, the
+// widest swizzle atom ("05 Async Data Movement - TMA", the 3-D TMA section:
+// a 128-byte swizzle holds exactly 64 fp16 along the contiguous dimension).
+constexpr int BLK_M = 128;
+constexpr int BLK_K = 64;
+constexpr int MMA_K = 16;
+constexpr int MAX_STAGES = 8;
+constexpr int STAGING_BYTES = 128 * 128;  // one 128-row x 128-byte output sub-tile
+constexpr int NUM_STAGING = 2;            // double-buffered output staging
+
+// Bytes one pipeline stage receives: the A tile plus the B tile, in fp16
+// ("GEMM II -- pipelining with TMA", Step 4, the byte_count formula).  The TMA
+// engine delivers the whole box even where it hangs past the tensor's edge
+// (the out-of-bounds part arrives zero-filled), so the count never shrinks
+// for ragged tiles.
+TG_HD uint32_t stage_tx_bytes(int block_n)
+{
+    return static_cast<uint32_t>((BLK_M * BLK_K + block_n * BLK_K) * 2);
+}
+
+// Error codes written by a kernel to its status record (same values as the
+// public gemm_status codes).
+enum : int { DEV_OK = 0, DEV_TIMEOUT = 4 };
+
+// Where a bounded wait gave up (recorded for diagnosis).
+enum : int {
+    WAIT_FULL = 1,        // consumer waiting for a stage's TMA bytes
+    WAIT_EMPTY = 2,       // producer waiting for the MMA to free a stage
+    WAIT_MMA = 3,         // waiting for an MMA batch to complete
+    WAIT_TMEM_FULL = 4,   // epilogue waiting for an accumulator
+    WAIT_TMEM_EMPTY = 5,  // MMA issuer waiting for the epilogue to drain TMEM
+    WAIT_DRAIN = 6,       // teardown waiting for in-flight copies / MMAs
+    WAIT_STALL = 7        // the stall-test barrier that nothing completes
+};
+
+// Device-side status record, one per plan (device memory, 32 bytes).
+struct DevStatus {
+    int code;         // first error code recorded (0 = none)
+    int where;        // WAIT_* of the first timeout
+    int block;        // blockIdx.x of the first timeout
+    int tile;         // tile index being processed
+    int kblock;       // k-block index being processed
+    int abort_epoch;  // epoch of the most recent run that hit a timeout
+    int pad[2];
+};
+
+struct Params {
+    int M, N, K;
+    int tiles_m, tiles_n, num_tiles, k_blocks;
+    int group_m;     // raster group height (in M tiles)
+    int pipe_depth;  // stages in the shared-memory ring (1..MAX_STAGES)
+    const void* A;   // M x K fp16, row-major (used by the thread-copy variant)
+    const void* B;   // N x K fp16, row-major (used by the thread-copy variant)
+    void* C;         // M x N, row-major, fp16 or fp32 (used by plain-store epilogues)
+    DevStatus* status;
+    int epoch;                  // run counter, > 0
+    unsigned long long budget_ns;  // bound on any single wait
+    int debug_stall;            // 1: producer first waits on a barrier nothing completes
+};
+
+// Grouped raster order of the output tiles ("GEMM II -- pipelining with TMA",
+// Step 6, l2_group_size): walking the linear tile index t, `group_m`
+// consecutive M-tiles are visited for one N-tile before moving to the next
+// N-tile, so tiles handed out together share A row-bands and B column-bands
+// in L2.  The last group may be shorter.  Defined for 0 <= t < tiles_m*tiles_n.
+TG_HD void raster_tile(int t, int tiles_m, int tiles_n, int group_m, int& m_tile, int& n_tile)
+{
+    const int per_group = group_m * tiles_n;
+    const int gid = t / per_group;
+    const int m_first = gid * group_m;
+    const int rows = (tiles_m - m_first) < group_m ? (tiles_m - m_first) : group_m;
+    const int r = t - gid * per_group;
+    m_tile = m_first + r % rows;
+    n_tile = r / rows;
+}
+
+// Byte offset, inside a 1024-byte-aligned tile of 128-byte rows, of the byte
+// at (row, byte_in_row) after the 128-byte swizzle: the 16-byte chunk index is
+// XORed with the row's position inside its 8-row atom ("05 Async Data
+// Movement - TMA", "How TMA Writes a Swizzled Layout": physical sector =
+// logical sector XOR (row mod 8)).
+TG_HD uint32_t sw128_offset(uint32_t row, uint32_t byte_in_row)
+{
+    const uint32_t chunk = (byte_in_row >> 4) & 7u;
+    return row * 128u + (((chunk ^ (row & 7u)) << 4) | (byte_in_row & 15u));
+}
+
+// Shared-memory layout of one CTA (byte offsets from a 1024-byte-aligned
+// base): `stages` A tiles (128 x 128 B), `stages` B tiles (block_n x 128 B),
+// `staging` output sub-tile buffers, then the mbarriers and the TMEM address
+// slot.  `total` includes 1024 bytes of slack for aligning the base.
+struct SmemLayout {
+    uint32_t a, b, staging, bars, total;
+};
+
+constexpr uint32_t A_TILE_BYTES = BLK_M * BLK_K * 2;  // 16 KB
+constexpr uint32_t BAR_AREA_BYTES = 256;
+
+TG_HD uint32_t b_tile_bytes(int block_n) { return static_cast<uint32_t>(block_n * BLK_K * 2); }
+
+TG_HD SmemLayout smem_layout(int stages, int block_n, int staging)
+{
+    SmemLayout L;
+    L.a = 0;
+    L.b = L.a + static_cast<uint32_t>(stages) * A_TILE_BYTES;
+    L.staging = L.b + static_cast<uint32_t>(stages) * b_tile_bytes(block_n);
+    L.bars = L.staging + static_cast<uint32_t>(staging) * STAGING_BYTES;
+    L.total = L.bars + BAR_AREA_BYTES + 1024;
+    return L;
+}
+
+// Barrier slots (8-byte mbarriers) inside the barrier area.
+enum : int {
+    BAR_FULL = 0,                     // [MAX_STAGES]  stage filled by TMA
+    BAR_EMPTY = BAR_FULL + MAX_STAGES,  // [MAX_STAGES]  stage released by the MMA
+    BAR_TMEM_FULL = BAR_EMPTY + MAX_STAGES,  // [2] accumulator ready for the epilogue
+    BAR_TMEM_EMPTY = BAR_TMEM_FULL + 2,      // [2] accumulator drained by the epilogue
+    BAR_MMA = BAR_TMEM_EMPTY + 2,            // MMA batch complete (lock-step variants)
+    BAR_DRAIN = BAR_MMA + 1,                 // teardown drain of in-flight MMAs
+    BAR_STALL = BAR_DRAIN + 1,               // stall test: never completed
+    BAR_COUNT = BAR_STALL + 1
+};
+constexpr uint32_t TMEM_SLOT_OFFSET = BAR_COUNT * 8;  // u32 TMEM base address
+static_assert(TMEM_SLOT_OFFSET + 4 <= BAR_AREA_BYTES, "barrier area too small");
+
+}  // namespace tg

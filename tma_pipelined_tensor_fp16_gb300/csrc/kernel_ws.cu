@@ -1,0 +1,266 @@
+// kernel_ws.cu -- the warp-specialised rungs of the ladder: the CTA's threads
+// split into roles that talk only through mbarriers, so the copy engine, the
+// tensor core and the epilogue run at the same time ("GEMM II -- pipelining
+// with TMA", closing section: split the lock-step team into producer and
+// consumer roles; tilus "Multi-Stage Software Pipelining", What's Next: a
+// producer warp and consumers joined by a producer/consumer barrier pair; "B200
+// Tma Pipeline Designer", Case 1: the consumer waits on tma2mma[stage], the
+// producer waits on mma2tma[stage] before overwriting).
+//
+//   warp 0, one lane   TMA producer: wait empty[s], arrive.expect_tx(full[s]),
+//                      two bulk tensor loads into stage s.
+//   warp 1, one lane   MMA issuer: wait full[s], four tcgen05.mma into the
+//                      TMEM accumulator, tcgen05.commit -> empty[s]; after the
+//                      last K block, commit -> tmem_full[acc].
+//   warps 2..5         epilogue: wait tmem_full[acc], TMEM -> regs -> swizzled
+//                      staging -> TMA store, arrive tmem_empty[acc].
+//
+// PERSIST = false: one output tile per CTA, one accumulator (grid = tiles).
+// PERSIST = true : grid = SM count; each CTA walks the grouped raster
+// (t = blockIdx.x, + gridDim.x, ...), TMEM is allocated once for two
+// accumulators so the epilogue of tile i overlaps the main loop of tile i+1,
+// and the ring position {stage, phase} runs on continuously across tiles (the
+// tilus tutorial's single per-role phase that flips on wrap-around), so no
+// phase is ever reset.
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace tg {
+
+namespace {
+
+struct CtaSmem {
+    uint8_t* gen;
+    uint32_t base;
+};
+
+__device__ __forceinline__ CtaSmem cta_smem()
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = align1024(raw);
+    return CtaSmem{smem_raw + (base - raw), base};
+}
+
+__device__ __forceinline__ uint32_t bar_addr(uint32_t bars, int slot)
+{
+    return bars + static_cast<uint32_t>(slot) * 8u;
+}
+
+}  // namespace
+
+constexpr int WS_THREADS = 192;
+constexpr int EPI_FIRST_WARP = 2;
+constexpr uint32_t EPI_BAR_ID = 1;
+
+template <int BN, bool F16OUT, bool PERSIST>
+__global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CUtensorMap tmA,
+                                                      const __grid_constant__ CUtensorMap tmB,
+                                                      const __grid_constant__ CUtensorMap tmC,
+                                                      const Params p)
+{
+    constexpr int ACC = PERSIST ? 2 : 1;
+    constexpr uint32_t TMEM_COLS = ACC * BN;  // 64..512, a power of two
+    const int D = p.pipe_depth;
+    const CtaSmem sm = cta_smem();
+    const SmemLayout L = smem_layout(D, BN, NUM_STAGING);
+    const uint32_t sA = sm.base + L.a;
+    const uint32_t sB = sm.base + L.b;
+    const uint32_t staging = sm.base + L.staging;
+    const uint32_t bars = sm.base + L.bars;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm.gen + L.bars + TMEM_SLOT_OFFSET);
+    const int tid = static_cast<int>(threadIdx.x);
+    const int warp = tid >> 5;
+    const uint32_t lane = lane_id();
+    Watchdog wd = make_watchdog(p);
+    const int tile_step = PERSIST ? static_cast<int>(gridDim.x) : p.num_tiles;
+    const int KB = p.k_blocks;
+
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmC);
+        for (int s = 0; s < D; ++s) {
+            mbar_init(bar_addr(bars, BAR_FULL + s), 1);   // producer's expect_tx arrival
+            mbar_init(bar_addr(bars, BAR_EMPTY + s), 1);  // MMA issuer's commit
+        }
+        for (int a = 0; a < ACC; ++a) {
+            mbar_init(bar_addr(bars, BAR_TMEM_FULL + a), 1);     // MMA issuer's commit
+            mbar_init(bar_addr(bars, BAR_TMEM_EMPTY + a), 128);  // every epilogue thread
+        }
+        mbar_init(bar_addr(bars, BAR_DRAIN), 1);
+        mbar_init(bar_addr(bars, BAR_STALL), 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish_alloc_permit();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            const uint32_t tx = stage_tx_bytes(BN);
+            if (p.debug_stall) wd.wait(bar_addr(bars, BAR_STALL), 0, WAIT_STALL, -1, -1);
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            for (int t = static_cast<int>(blockIdx.x); t < p.num_tiles; t += tile_step) {
+                int mt, nt;
+                raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
+                const int m0 = mt * BLK_M, n0 = nt * BN;
+                for (int kb = 0; kb < KB; ++kb) {
+                    // a fresh barrier passes a wait on parity 1 at once: the
+                    // first trip around the ring does not wait
+                    wd.wait(bar_addr(bars, BAR_EMPTY + stage), phase ^ 1u, WAIT_EMPTY, t, kb);
+                    if (!wd.aborted) {
+                        const uint32_t fb = bar_addr(bars, BAR_FULL + stage);
+                        mbar_arrive_expect_tx(fb, tx);
+                        tma_load_2d(sA + stage * A_TILE_BYTES, &tmA, fb, kb * BLK_K, m0);
+                        tma_load_2d(sB + stage * b_tile_bytes(BN), &tmB, fb, kb * BLK_K, n0);
+                        ++issued;
+                    }
+                    if (++stage == D) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // drain: the last min(D, issued) loads have landed before exit
+            if (wd.aborted) {
+                int st = stage;
+                uint32_t ph = phase;
+                for (int i = 0; i < D && i < issued; ++i) {
+                    if (st == 0) {
+                        st = D - 1;
+                        ph ^= 1u;
+                    } else {
+                        --st;
+                    }
+                    wd.drain(bar_addr(bars, BAR_FULL + st), ph);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------- MMA issuer
+            constexpr uint32_t idesc = idesc_f16_f32(BLK_M, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            for (int t = static_cast<int>(blockIdx.x); t < p.num_tiles; t += tile_step) {
+                // the epilogue has drained this accumulator (fresh: passes)
+                wd.wait(bar_addr(bars, BAR_TMEM_EMPTY + acc), acc_phase ^ 1u, WAIT_TMEM_EMPTY,
+                        t, -1);
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < KB; ++kb) {
+                    wd.wait(bar_addr(bars, BAR_FULL + stage), phase, WAIT_FULL, t, kb);
+                    if (!wd.aborted) {
+                        tc_fence_after_sync();
+                        const uint64_t adesc = sw128_kmajor_desc(sA + stage * A_TILE_BYTES);
+                        const uint64_t bdesc = sw128_kmajor_desc(sB + stage * b_tile_bytes(BN));
+#pragma unroll
+                        for (int kk = 0; kk < BLK_K / MMA_K; ++kk)
+                            mma_f16_ss(d_tmem, adesc + static_cast<uint64_t>(kk * 2),
+                                       bdesc + static_cast<uint64_t>(kk * 2), idesc,
+                                       (kb == 0 && kk == 0) ? 0u : 1u);
+                        // frees the stage once these MMAs have read it
+                        mma_commit(bar_addr(bars, BAR_EMPTY + stage));
+                    }
+                    if (++stage == D) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!wd.aborted) mma_commit(bar_addr(bars, BAR_TMEM_FULL + acc));
+                if (ACC == 2) {
+                    acc ^= 1;
+                    if (acc == 0) acc_phase ^= 1u;
+                } else {
+                    acc_phase ^= 1u;
+                }
+            }
+            // every MMA has completed before TMEM is released
+            mma_commit(bar_addr(bars, BAR_DRAIN));
+            wd.drain(bar_addr(bars, BAR_DRAIN), 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const bool issuer = (tid == EPI_FIRST_WARP * 32);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        uint32_t sub_count = 0;
+        for (int t = static_cast<int>(blockIdx.x); t < p.num_tiles; t += tile_step) {
+            int mt, nt;
+            raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
+            wd.wait(bar_addr(bars, BAR_TMEM_FULL + acc), acc_phase, WAIT_TMEM_FULL, t, -1);
+            tc_fence_after_sync();
+            epilogue_tma_store<BN, F16OUT>(tmem_base + static_cast<uint32_t>(acc * BN), q, lane,
+                                           issuer, staging, &tmC, mt * BLK_M, nt * BN, p.N,
+                                           sub_count, EPI_BAR_ID, !wd.aborted);
+            tc_fence_before_sync();
+            mbar_arrive(bar_addr(bars, BAR_TMEM_EMPTY + acc));
+            if (ACC == 2) {
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            } else {
+                acc_phase ^= 1u;
+            }
+        }
+        if (issuer) bulk_wait_group<0>();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+namespace {
+
+template <typename KernelT>
+cudaError_t launch_kernel(KernelT kernel, const LaunchSpec& s, cudaStream_t stream)
+{
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(s.smem_bytes));
+    if (e != cudaSuccess) return e;
+    kernel<<<s.grid, WS_THREADS, s.smem_bytes, stream>>>(*s.tmA, *s.tmB, *s.tmC, s.p);
+    return cudaGetLastError();
+}
+
+template <int BN, bool F16OUT>
+cudaError_t launch_bn(const LaunchSpec& s, cudaStream_t stream)
+{
+    if (s.variant == VAR_PERSISTENT) return launch_kernel(k_ws<BN, F16OUT, true>, s, stream);
+    if (s.variant == VAR_WS_PIPELINED) return launch_kernel(k_ws<BN, F16OUT, false>, s, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_ws(const LaunchSpec& s, cudaStream_t stream)
+{
+    switch (s.block_n) {
+    case 64:
+        return s.f16out ? launch_bn<64, true>(s, stream) : launch_bn<64, false>(s, stream);
+    case 128:
+        return s.f16out ? launch_bn<128, true>(s, stream) : launch_bn<128, false>(s, stream);
+    case 256:
+        return s.f16out ? launch_bn<256, true>(s, stream) : launch_bn<256, false>(s, stream);
+    default:
+        return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace tg
