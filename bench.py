@@ -101,7 +101,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "25"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -151,11 +151,17 @@ def time_oracle(cfg, target_s, rows_cap=None):
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
     threads = oracle.default_threads()
     A, B = inputs.make_operands(M, N, K, cfg["dist"], cfg["seed"])
-    probe = max(1, min(M, threads))
+    # two probes separate the per-call decode of B from the per-row cost
+    p1 = max(1, min(M, threads))
+    p2 = max(p1 + 1, min(M, 4 * threads))
     t0 = time.perf_counter()
-    oracle.gemm_rows(A, B, 0, probe, threads)
-    dt = time.perf_counter() - t0
-    rows = int(max(probe, min(M, probe * target_s / max(dt, 1e-6))))
+    oracle.gemm_rows(A, B, 0, p1, threads)
+    t1 = time.perf_counter()
+    oracle.gemm_rows(A, B, 0, p2, threads)
+    t2 = time.perf_counter()
+    per_row = max((t2 - t1) - (t1 - t0), 1e-9) / (p2 - p1)
+    fixed = max((t1 - t0) - per_row * p1, 0.0)
+    rows = int(max(p2, min(M, (target_s - fixed) / per_row)))
     if rows_cap:
         rows = min(rows, rows_cap)
     t0 = time.perf_counter()
@@ -209,8 +215,8 @@ METRIC = "fp16 GEMM TFLOP/s at 8192^3 (1 GB300) and % of dense fp16 tensor peak"
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="gemm_8192x8192x8192_f16out")
     ap.add_argument("--variant", default="auto")

@@ -1,0 +1,102 @@
+"""Sweep the kernel variants, tile widths and pipeline depths on one workload.
+
+    python -m tma_pipelined_tensor_fp16_gb300.sweep --config gemm_8192 \
+        [--variants persistent,ws_pipelined] [--depths 2,3,4] [--block-n 64,128,256] \
+        [--iters 20] [--out results.jsonl]
+
+Prints one JSON line per configuration: the plan, the shared memory it needs
+(or why it does not fit), and the median / mean TFLOP/s and GB/s of `iters`
+launches timed with CUDA events on the launch stream after 3 warm-up
+launches.  This is the PIPE_DEPTH-versus-shared-memory trade-off measured on
+the device ("GEMM II -- pipelining with TMA", Step 5: deeper rings hide more
+latency; tilus "Multi-Stage Software Pipelining": deeper pipelines force
+smaller tiles).
+"""
+import argparse
+import json
+import os
+import statistics
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--config", default="gemm_8192x8192x8192_f16out")
+    ap.add_argument("--variants", default="sync_tiled,tma_serial,pipelined,persistent_lockstep,"
+                                          "ws_pipelined,persistent")
+    ap.add_argument("--depths", default="1,2,3,4,5,6,7,8")
+    ap.add_argument("--block-n", default="64,128,256")
+    ap.add_argument("--iters", type=int, default=20)
+    ap.add_argument("--out", default="")
+    a = ap.parse_args(argv)
+
+    import numpy as np
+    import torch
+
+    from . import binding, build, inputs
+    build.build()
+    cfg = next(c for c in inputs.CONFIGS if a.config in c["name"])
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    A, B = inputs.make_operands(M, N, K, cfg["dist"], cfg["seed"])
+    dA = torch.from_numpy(A.view(np.float16)).cuda()
+    dB = torch.from_numpy(B.view(np.float16)).cuda()
+    dC = torch.empty((M, N), dtype=torch.float16 if cfg["out"] == "f16" else torch.float32,
+                     device="cuda")
+    flops = 2.0 * M * N * K
+    nbytes = 2.0 * (M * K + N * K) + dC.element_size() * M * N
+    stream = torch.cuda.Stream()
+    sink = open(a.out, "a") if a.out else None
+    for variant in a.variants.split(","):
+        for bn in [int(x) for x in a.block_n.split(",")]:
+            depths = [int(x) for x in a.depths.split(",")]
+            if variant in ("sync_tiled", "tma_serial"):
+                depths = [1]
+            for d in depths:
+                rec = {"workload": cfg["name"], "variant": variant, "block_n": bn, "depth": d}
+                try:
+                    plan = binding.Plan(M, N, K, out=cfg["out"], variant=variant, block_n=bn,
+                                        pipe_depth=d)
+                except binding.GemmError as e:
+                    rec["error"] = str(e)
+                    _emit(rec, sink)
+                    continue
+                rec["plan"] = plan.describe()
+                args = (dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), stream.cuda_stream)
+                for _ in range(3):
+                    plan.run(*args)
+                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                      for _ in range(a.iters)]
+                torch.cuda.synchronize()
+                for e0, e1 in ev:
+                    e0.record(stream)
+                    plan.run(*args)
+                    e1.record(stream)
+                torch.cuda.synchronize()
+                st = plan.device_status()
+                plan.close()
+                ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+                rec.update({
+                    "status": st,
+                    "ms_median": statistics.median(ms), "ms_min": min(ms),
+                    "tflops_median": flops / (statistics.median(ms) * 1e-3) / 1e12,
+                    "tflops_mean": flops / (statistics.mean(ms) * 1e-3) / 1e12,
+                    "gbs_median": nbytes / (statistics.median(ms) * 1e-3) / 1e9,
+                })
+                _emit(rec, sink)
+    if sink:
+        sink.close()
+
+
+def _emit(rec, sink):
+    line = json.dumps(rec)
+    print(line, flush=True)
+    if sink:
+        sink.write(line + "\n")
+
+
+if __name__ == "__main__":
+    main()
