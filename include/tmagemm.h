@@ -162,6 +162,34 @@ TMAGEMM_API int gemm_schedule_tile(const gemm_config* cfg, int64_t tile, int* m_
  * the thread-copy variant writes it and the TMA engine lays it out. */
 TMAGEMM_API int64_t gemm_sw128_offset(int64_t row, int64_t byte_in_row);
 
+/* Allocation-free variant of gemm_create_plan + gemm_run + gemm_destroy for
+ * callers that cannot call cudaMalloc: processes whose device memory is
+ * owned by a framework's caching allocator or a pre-reserved arena (a foreign
+ * cudaMalloc fails or is forbidden there), and latency-critical loops that
+ * cannot pay the device synchronisation that cudaMalloc/cudaFree imply.  The
+ * pages have no counterpart of this entry point.
+ *
+ * Runs the default (persistent, warp-specialised) kernel for C = A . B^T with
+ * the same operands, layouts, preconditions and arithmetic as gemm_run, on
+ * `cuda_stream`.  It allocates nothing: its only scratch memory, the kernel's
+ * 32-byte watchdog status record, lives in a file-scope device array of 256
+ * bytes (the stated maximum; a build whose record outgrew it would be rejected
+ * with GEMM_ERR_UNSUPPORTED) that every GPU loading this library holds until
+ * the process exits.  It calls no cudaMalloc, cudaFree or allocating library
+ * routine.
+ *
+ * The first call on each device looks up that array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture begins.  Every call on a device shares the one
+ * array and clears it at the start (an asynchronous memset on `cuda_stream`),
+ * so calls that overlap on the GPU race on the status record: serialise them.
+ *
+ * device_status: NULL makes the call asynchronous (like gemm_run, with no
+ * watchdog report).  Non-NULL makes it synchronise `cuda_stream` and store
+ * GEMM_OK or GEMM_ERR_TIMEOUT there, which is also returned. */
+TMAGEMM_API int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, const void* A,
+                                 const void* B, void* C, void* cuda_stream, int* device_status);
+
 #ifdef __cplusplus
 }
 #endif

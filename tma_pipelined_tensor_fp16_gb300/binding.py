@@ -69,6 +69,8 @@ _SIGS = {
                                           ctypes.POINTER(ctypes.c_int),
                                           ctypes.POINTER(ctypes.c_int)]),
     "gemm_sw128_offset": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int64]),
+    "gemm_run_noalloc": (ctypes.c_int, [ctypes.c_int64] * 3 + [ctypes.c_int] + [ctypes.c_void_p] * 4
+                         + [ctypes.POINTER(ctypes.c_int)]),
 }
 
 _lib = None
@@ -124,6 +126,19 @@ def gemm_run(plan, A_ptr, B_ptr, C_ptr, stream_handle):
 
 def gemm_run_host(plan, A_ptr, B_ptr, C_ptr, stream_handle):
     return lib().gemm_run_host(plan, A_ptr, B_ptr, C_ptr, stream_handle)
+
+
+def gemm_run_noalloc(M, N, K, dtype_out, A_ptr, B_ptr, C_ptr, stream_handle, want_status=True):
+    """Allocation-free run of the default kernel (see include/tmagemm.h).
+    Returns (status, device_status); device_status is None when the call is
+    asynchronous (want_status=False)."""
+    if want_status:
+        ds = ctypes.c_int(-1)
+        st = lib().gemm_run_noalloc(M, N, K, dtype_out, A_ptr, B_ptr, C_ptr, stream_handle,
+                                    ctypes.byref(ds))
+        return st, ds.value
+    st = lib().gemm_run_noalloc(M, N, K, dtype_out, A_ptr, B_ptr, C_ptr, stream_handle, None)
+    return st, None
 
 
 def gemm_get_device_status(plan):

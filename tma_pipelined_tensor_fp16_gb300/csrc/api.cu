@@ -488,3 +488,160 @@ int64_t gemm_sw128_offset(int64_t row, int64_t byte_in_row)
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// Some callers cannot call cudaMalloc: applications whose device memory is
+// owned entirely by a framework's caching allocator or a pre-reserved arena
+// (a foreign cudaMalloc either fails for lack of memory or is forbidden by
+// policy), and latency-critical serving loops that cannot afford the device
+// synchronisation cudaMalloc/cudaFree imply.  gemm_create_plan allocates the
+// plan's device status record, so those callers use gemm_run_noalloc instead:
+// the persistent kernel's only scratch memory, that status record, lives in
+// the file-scope array below, which every GPU that loads this library holds
+// until the process exits.
+
+namespace {
+
+constexpr size_t NOALLOC_SCRATCH_BYTES = 256;  // stated maximum scratch size
+static_assert(sizeof(DevStatus) <= NOALLOC_SCRATCH_BYTES, "status record must fit");
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
+int g_noalloc_epoch[NOALLOC_MAX_DEVICES] = {};
+
+}  // namespace
+
+// Shared by every gemm_run_noalloc call on a device; keeps the last call's
+// contents.  Host code must not pass this name to a kernel: on the host it is
+// a stand-in symbol, not a device address (see noalloc_scratch_ptr).
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of g_noalloc_scratch on device `dev` (which is current),
+// looked up once per device with cudaGetSymbolAddress.
+int noalloc_scratch_ptr(int dev, void** out)
+{
+    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES)
+        return fail(GEMM_ERR_UNSUPPORTED, "device index too large for gemm_run_noalloc");
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return cuda_fail("cudaGetSymbolAddress(g_noalloc_scratch)", e);
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, const void* A,
+                                const void* B, void* C, void* cuda_stream, int* device_status)
+{
+    if (device_status) *device_status = GEMM_OK;
+    if (!A || !B || !C) return fail(GEMM_ERR_INVALID_ARG, "A, B and C must be non-NULL");
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+         reinterpret_cast<uintptr_t>(C)) & 15u)
+        return fail(GEMM_ERR_UNSUPPORTED, "A, B and C must be 16-byte aligned (TMA)");
+    const size_t scratch_needed = sizeof(DevStatus);
+    if (scratch_needed > NOALLOC_SCRATCH_BYTES) {
+        char buf[160];
+        std::snprintf(buf, sizeof(buf),
+                      "gemm_run_noalloc needs %zu bytes of scratch; its static array holds %zu",
+                      scratch_needed, NOALLOC_SCRATCH_BYTES);
+        return fail(GEMM_ERR_UNSUPPORTED, buf);
+    }
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(GEMM_ERR_NO_DEVICE, std::string("no CUDA device: ") +
+                                                              cudaGetErrorString(e));
+    int major = 0, minor = 0, sms = 0, smem_optin = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    e = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return cuda_fail("cudaDeviceGetAttribute", e);
+    if (major != 10 || minor != 3)
+        return fail(GEMM_ERR_NO_DEVICE, "this library is built for sm_103a (GB300) only");
+
+    gemm_options opts;
+    std::memset(&opts, 0, sizeof(opts));
+    opts.variant = VAR_PERSISTENT;
+    gemm_config c;
+    int r = select_config_impl(M, N, K, dtype_out, &opts, sms, smem_optin, &c);
+    if (r != GEMM_OK) return r;
+
+    void* scratch = nullptr;
+    r = noalloc_scratch_ptr(dev, &scratch);
+    if (r != GEMM_OK) return r;
+
+    CUtensorMap tmA, tmB, tmC;
+    r = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, K * 2, BLK_K, BLK_M, "A");
+    if (r == GEMM_OK)
+        r = encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, K * 2, BLK_K, c.block_n,
+                      "B");
+    if (r == GEMM_OK) {
+        if (dtype_out == GEMM_OUT_F16)
+            r = encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, N, M, N * 2, 64, BLK_M, "C");
+        else
+            r = encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, N * 4, 32, BLK_M, "C");
+    }
+    if (r != GEMM_OK) return r;
+
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    // The status record must start at zero for this call.
+    e = cudaMemsetAsync(scratch, 0, sizeof(DevStatus), stream);
+    if (e != cudaSuccess) return cuda_fail("clearing the scratch status record", e);
+
+    LaunchSpec s;
+    s.variant = c.variant;
+    s.block_n = c.block_n;
+    s.f16out = dtype_out == GEMM_OUT_F16;
+    s.grid = c.grid;
+    s.threads = c.threads;
+    s.smem_bytes = static_cast<unsigned>(c.smem_bytes);
+    s.tmA = &tmA;
+    s.tmB = &tmB;
+    s.tmC = &tmC;
+    Params& p = s.p;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.tiles_m = c.tiles_m;
+    p.tiles_n = c.tiles_n;
+    p.num_tiles = c.num_tiles;
+    p.k_blocks = c.k_blocks;
+    p.group_m = c.group_m;
+    p.pipe_depth = c.pipe_depth;
+    p.A = A;
+    p.B = B;
+    p.C = C;
+    p.status = static_cast<DevStatus*>(scratch);
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        if (++g_noalloc_epoch[dev] <= 0) g_noalloc_epoch[dev] = 1;
+        p.epoch = g_noalloc_epoch[dev];
+    }
+    p.budget_ns = 2000ull * 1000000ull;
+    p.debug_stall = 0;
+    e = launch_ws(s, stream);
+    if (e != cudaSuccess) return cuda_fail("kernel launch", e);
+
+    if (device_status) {
+        e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
+        DevStatus st;
+        e = cudaMemcpy(&st, scratch, sizeof(st), cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail("reading the scratch status record", e);
+        *device_status = st.code == DEV_OK ? GEMM_OK : GEMM_ERR_TIMEOUT;
+        if (st.code != DEV_OK)
+            return fail(GEMM_ERR_TIMEOUT, "kernel wait timed out; the run was abandoned");
+    }
+    return ok();
+}
