@@ -31,7 +31,8 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["csrc/ptx.cuh", "csrc/gemm_common.h", "csrc/device_common.cuh",
-                  "csrc/kernel_ws.cu", "csrc/kernels_ladder.cu", "csrc/api.cu"]
+                  "csrc/kernel_ws.cu", "csrc/kernel_ws2.cu", "csrc/kernels_ladder.cu",
+                  "csrc/api.cu"]
 
 
 def kernel_source_hash():
@@ -86,7 +87,9 @@ def algorithmic(cfg):
 # --------------------------------------------------------------- clocks
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi polling in the background; only samples whose timestamps fall
+    inside the timed region (mark_start .. mark_end) are reported."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -94,6 +97,7 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def start(self):
         fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
@@ -101,13 +105,21 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "25"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
-        time.sleep(0.3)
+        time.sleep(0.5)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+        time.sleep(0.05)
 
     def stop(self):
+        import datetime
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -119,26 +131,34 @@ class ClockSampler:
             with open(self.path) as f:
                 for line in f:
                     parts = [p.strip() for p in line.split(",")]
-                    if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
-                        rows.append(parts)
+                    if len(parts) < 10 or not parts[2].replace(".", "").isdigit():
+                        continue
+                    try:
+                        ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    except ValueError:
+                        continue
+                    rows.append((ts, parts[1:]))
         finally:
             try:
                 os.unlink(self.path)
             except OSError:
                 pass
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
-        sm = [float(r[1]) for r in rows]
+        inside = [r for ts, r in rows if self.t0 is not None and self.t0 <= ts <= self.t1]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0,
+                    "reasons": ["no nvidia-smi sample inside the timed region"]}
+        sm = [float(r[1]) for r in inside]
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
+        for r in inside:
             for i, n in enumerate(names):
                 if r[5 + i].lower().startswith("active"):
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
-                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())
-                if any(r[3].replace(".", "").isdigit() for r in rows) else None,
-                "samples": len(rows), "reasons": sorted(reasons)}
+        power = [float(r[3]) for r in inside if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm),
+                "sm_max_mhz": float(inside[0][2]),
+                "power_w_max": max(power) if power else None,
+                "samples": len(inside), "reasons": sorted(reasons)}
 
 
 # --------------------------------------------------------------- oracle timing
@@ -215,7 +235,7 @@ METRIC = "fp16 GEMM TFLOP/s at 8192^3 (1 GB300) and % of dense fp16 tensor peak"
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="gemm_8192x8192x8192_f16out")
@@ -282,6 +302,7 @@ def main():
     t_end = torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
+    sampler.mark_start()
     with torch.cuda.stream(stream):
         t_start.record(stream)
         for i in range(args.steps):
@@ -290,6 +311,7 @@ def main():
             ev[i][1].record(stream)
         t_end.record(stream)
     torch.cuda.synchronize()
+    sampler.mark_end()
     barrier()
     clocks = sampler.stop()
     if plan.device_status() != 0:
@@ -345,8 +367,13 @@ def main():
 
     peaks, peak_kind = load_peaks()
     memory_bound = cfg["name"].startswith("gemm_skinny")
-    kernel_key = "k_ws<%d,%s,%s>" % (pcfg["block_n"], "f16" if cfg["out"] == "f16" else "f32",
-                                      "persistent" if pcfg["variant"] == 5 else "v%d" % pcfg["variant"])
+    out_tag = "f16" if cfg["out"] == "f16" else "f32"
+    if pcfg["variant"] == 7:
+        kernel_key = "k_ws2<%s>" % out_tag
+    else:
+        kernel_key = "k_ws<%d,%s,%s>" % (pcfg["block_n"], out_tag,
+                                          "persistent" if pcfg["variant"] == 5 else
+                                          "v%d" % pcfg["variant"])
     traffic = load_traffic(cfg["name"], kernel_key)
     if memory_bound:
         achieved = nbytes / avg_launch_s / 1e9

@@ -53,7 +53,9 @@ typedef enum {
 /* Kernel variants: the ablation ladder of "GEMM II -- pipelining with TMA"
  * (Steps 3-6) plus the warp-specialised forms. */
 typedef enum {
-    GEMM_VAR_AUTO = 0,              /* = GEMM_VAR_PERSISTENT */
+    GEMM_VAR_AUTO = 0,              /* GEMM_VAR_PERSISTENT_2CTA when M > 128 and there
+                                       are at least (SM count / 2) 256x256 tiles,
+                                       else GEMM_VAR_PERSISTENT */
     GEMM_VAR_SYNC_TILED = 1,        /* Step 3: thread copies, one MMA at a time */
     GEMM_VAR_TMA_SERIAL = 2,        /* Step 4: TMA load + expect_tx, serial loop */
     GEMM_VAR_PIPELINED = 3,         /* Step 5: PIPE_DEPTH ring, lock-step prefetch */
@@ -61,15 +63,20 @@ typedef enum {
                                        full+empty ring, one tile per CTA */
     GEMM_VAR_PERSISTENT = 5,        /* warp-specialised, grid = SM count, grouped
                                        raster, two TMEM accumulators */
-    GEMM_VAR_PERSISTENT_LOCKSTEP = 6 /* Step 6 as printed: persistent CTAs running
+    GEMM_VAR_PERSISTENT_LOCKSTEP = 6, /* Step 6 as printed: persistent CTAs running
                                        the lock-step Step-5 loop */
+    GEMM_VAR_PERSISTENT_2CTA = 7    /* warp-specialised, persistent, on CTA pairs
+                                       (clusters of 2): 256x256 tiles with
+                                       tcgen05.mma.cta_group::2, each CTA loading
+                                       its own half of the operands */
 } gemm_variant;
 
 /* Plan options; a zero field means "choose automatically". */
 typedef struct {
     int variant;        /* gemm_variant */
     int pipe_depth;     /* shared-memory stages, 1..8 (ring variants) */
-    int block_n;        /* output tile width: 64, 128 or 256 (tile height is 128) */
+    int block_n;        /* output tile width: 64, 128 or 256 (tile height is 128;
+                           the CTA-pair variant uses 256x256 tiles) */
     int group_m;        /* raster group height in M tiles (default 8) */
     int grid;           /* persistent variants: CTAs to launch (default: SM count) */
     int wait_budget_ms; /* bound on any single in-kernel wait (default 2000) */

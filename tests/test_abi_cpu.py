@@ -77,19 +77,44 @@ def test_argument_checks(b, args, status):
 
 
 def test_depth_that_does_not_fit_is_rejected(b):
-    st, _ = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(pipe_depth=5, block_n=256))
+    st, _ = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(
+        variant="persistent", pipe_depth=5, block_n=256))
     assert st == b.GEMM_ERR_UNSUPPORTED and "does not fit" in b.last_error()
-    st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(pipe_depth=4, block_n=256))
+    st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(
+        variant="persistent", pipe_depth=4, block_n=256))
     assert st == 0 and c.smem_bytes <= 232448
 
 
 def test_headline_configuration(b):
     st, c = b.gemm_select_config(8192, 8192, 8192, 1)
     assert st == 0
-    assert c.variant == b.GEMM_VAR_PERSISTENT
-    assert (c.block_m, c.block_n, c.block_k) == (128, 256, 64)
-    assert c.pipe_depth == 4 and c.grid == 152 and c.threads == 192
-    assert c.num_tiles == 2048 and c.k_blocks == 128 and c.tmem_cols == 512
+    assert c.variant == b.GEMM_VAR_PERSISTENT_2CTA
+    assert (c.block_m, c.block_n, c.block_k) == (256, 256, 64)
+    assert c.pipe_depth == 6 and c.grid == 152 and c.threads == 192
+    assert c.num_tiles == 1024 and c.k_blocks == 128 and c.tmem_cols == 512
+    assert c.tx_bytes == 2 * (128 * 64 + 128 * 64) * 2  # both CTAs' A and half-B tiles
+    st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(variant="persistent"))
+    assert st == 0 and (c.block_m, c.block_n, c.pipe_depth, c.num_tiles) == (128, 256, 4, 2048)
+
+
+@pytest.mark.parametrize("M,N,K,variant", [(256, 256, 256, 5), (4096, 4096, 4096, 7),
+                                           (4000, 3000, 5000, 7), (64, 16384, 16384, 5),
+                                           (128, 65536, 64, 5)])
+def test_auto_variant_choice(b, M, N, K, variant):
+    st, c = b.gemm_select_config(M, N, K, 1)
+    assert st == 0 and c.variant == variant
+
+
+def test_pair_variant_constraints(b):
+    st, _ = b.gemm_select_config(1024, 1024, 64, 1, b.make_options(variant="persistent_2cta",
+                                                                    block_n=128))
+    assert st == b.GEMM_ERR_INVALID_ARG
+    st, c = b.gemm_select_config(1024, 1024, 64, 1, b.make_options(variant="persistent_2cta",
+                                                                    grid=7))
+    assert st == 0 and c.grid == 6  # whole clusters of two
+    st, _ = b.gemm_select_config(1024, 1024, 64, 1, b.make_options(variant="persistent_2cta",
+                                                                    pipe_depth=7))
+    assert st == b.GEMM_ERR_UNSUPPORTED
 
 
 def test_stage_byte_count_matches_page_formula(b):

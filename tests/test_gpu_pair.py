@@ -1,0 +1,102 @@
+"""GPU parity of the CTA-pair variant (persistent_2cta: clusters of two CTAs,
+tcgen05.mma.cta_group::2, 256 x 256 pair tiles) against the CPU oracle.
+
+Covers pair tiles whose second CTA is partly or wholly past the last row,
+ragged N and K, every depth 1..6 against short K loops, many tiles per pair,
+integer inputs bit-exact and the five workload shapes at full size.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from tma_pipelined_tensor_fp16_gb300 import inputs
+
+from gpu_util import assert_close, assert_exact, run
+
+pytestmark = pytest.mark.gpu
+V = "persistent_2cta"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+@pytest.mark.parametrize("out", ["f32", "f16"])
+@pytest.mark.parametrize("shape", [(1, 8, 8), (100, 256, 64), (129, 136, 200), (256, 256, 256),
+                                   (300, 520, 328), (640, 776, 456)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_pair_small_shapes(out, shape):
+    M, N, K = shape
+    A, B = inputs.make_operands(M, N, K, "uniform", 300 + M + N + K)
+    got, guard, desc = run(A, B, out, guard_rows=3, variant=V)
+    assert_close(got, oracle.gemm(A, B), K, out, desc)
+    assert np.isnan(guard.astype(np.float32)).all(), "wrote past the end of C"
+
+
+@pytest.mark.parametrize("depth", [1, 2, 3, 4, 5, 6])
+def test_pair_depths_short_k(depth):
+    for kt in sorted({1, max(depth - 1, 1), depth, depth + 1, 2 * depth + 1}):
+        M, N, K = 384, 512, 64 * kt - 8 * (kt % 2)
+        A, B = inputs.make_operands(M, N, K, "normal", 2000 + depth * 16 + kt)
+        got, _, desc = run(A, B, "f32", variant=V, pipe_depth=depth)
+        assert_close(got, oracle.gemm(A, B), K, "f32", "K tiles=%d %s" % (kt, desc))
+
+
+@pytest.mark.parametrize("grid", [2, 6, 0])
+def test_pair_many_tiles_per_cluster(grid):
+    M, N, K = 1280, 1024, 320
+    A, B = inputs.make_operands(M, N, K, "uniform", 77)
+    got, _, desc = run(A, B, "f16", variant=V, grid=grid, group_m=3)
+    assert_close(got, oracle.gemm(A, B), K, "f16", desc)
+
+
+@pytest.mark.parametrize("out", ["f32", "f16"])
+def test_pair_integer_bit_exact(out):
+    M, N, K = 520, 392, 1000
+    A, B = inputs.make_operands(M, N, K, "int", 8)
+    got, _, desc = run(A, B, out, variant=V)
+    assert_exact(got, oracle.gemm(A, B), out, desc)
+
+
+def _sample(M, N, count, seed):
+    rng = np.random.default_rng(seed)
+    rows = np.concatenate([rng.integers(0, M, count), [0, M - 1, min(255, M - 1), min(256, M - 1)]])
+    cols = np.concatenate([rng.integers(0, N, count), [N - 1, 0, min(255, N - 1), N - 1]])
+    return rows.astype(np.int64), cols.astype(np.int64)
+
+
+@pytest.mark.parametrize("cfg", inputs.CONFIGS, ids=[c["name"] for c in inputs.CONFIGS])
+def test_pair_workloads_sampled(cfg):
+    M, N, K, out = cfg["M"], cfg["N"], cfg["K"], cfg["out"]
+    A, B = inputs.make_operands(M, N, K, cfg["dist"], cfg["seed"])
+    got, _, desc = run(A, B, out, variant=V)
+    assert np.isfinite(got.astype(np.float32)).all(), desc
+    rows, cols = _sample(M, N, 3000, cfg["seed"])
+    assert_close(got[rows, cols], oracle.gemm_entries(A, B, rows, cols), K, out, desc)
+    Ai, Bi = inputs.make_operands(M, N, K, "int", 60 + cfg["seed"])
+    goti, _, _ = run(Ai, Bi, out, variant=V)
+    assert_exact(goti[rows, cols], oracle.gemm_entries(Ai, Bi, rows, cols), out, desc)
+
+
+def test_pair_watchdog_timeout():
+    import torch
+
+    import tma_pipelined_tensor_fp16_gb300 as pkg
+    from tma_pipelined_tensor_fp16_gb300 import binding
+    M, N, K = 512, 512, 256
+    A, B = inputs.make_operands(M, N, K, "uniform", 3)
+    dA = torch.from_numpy(A.view(np.float16)).cuda()
+    dB = torch.from_numpy(B.view(np.float16)).cuda()
+    C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    plan = pkg.Plan(M, N, K, out="f32", variant=V, debug_stall=1, wait_budget_ms=100)
+    plan(dA, dB, C)
+    torch.cuda.synchronize()
+    assert plan.device_status() == binding.GEMM_ERR_TIMEOUT
+    plan.close()
+    got, _, desc = run(A, B, "f32", variant=V)
+    assert_close(got, oracle.gemm(A, B), K, "f32", "after timeout: " + desc)

@@ -14,7 +14,8 @@ GEMM_OUT_F32, GEMM_OUT_F16 = 0, 1
 (GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT,
  GEMM_ERR_NO_DEVICE) = range(6)
 (GEMM_VAR_AUTO, GEMM_VAR_SYNC_TILED, GEMM_VAR_TMA_SERIAL, GEMM_VAR_PIPELINED,
- GEMM_VAR_WS_PIPELINED, GEMM_VAR_PERSISTENT, GEMM_VAR_PERSISTENT_LOCKSTEP) = range(7)
+ GEMM_VAR_WS_PIPELINED, GEMM_VAR_PERSISTENT, GEMM_VAR_PERSISTENT_LOCKSTEP,
+ GEMM_VAR_PERSISTENT_2CTA) = range(8)
 
 VARIANTS = {
     "auto": GEMM_VAR_AUTO,
@@ -24,6 +25,7 @@ VARIANTS = {
     "ws_pipelined": GEMM_VAR_WS_PIPELINED,
     "persistent": GEMM_VAR_PERSISTENT,
     "persistent_lockstep": GEMM_VAR_PERSISTENT_LOCKSTEP,
+    "persistent_2cta": GEMM_VAR_PERSISTENT_2CTA,
 }
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 

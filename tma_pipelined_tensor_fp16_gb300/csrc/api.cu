@@ -51,12 +51,20 @@ const char* variant_name(int v)
     case VAR_WS_PIPELINED: return "ws_pipelined";
     case VAR_PERSISTENT: return "persistent";
     case VAR_PERSISTENT_LOCKSTEP: return "persistent_lockstep";
+    case VAR_PERSISTENT_2CTA: return "persistent_2cta";
     default: return "?";
     }
 }
 
-bool is_ws(int v) { return v == VAR_WS_PIPELINED || v == VAR_PERSISTENT; }
-bool is_persistent(int v) { return v == VAR_PERSISTENT || v == VAR_PERSISTENT_LOCKSTEP; }
+bool is_ws(int v)
+{
+    return v == VAR_WS_PIPELINED || v == VAR_PERSISTENT || v == VAR_PERSISTENT_2CTA;
+}
+bool is_persistent(int v)
+{
+    return v == VAR_PERSISTENT || v == VAR_PERSISTENT_LOCKSTEP || v == VAR_PERSISTENT_2CTA;
+}
+bool is_pair(int v) { return v == VAR_PERSISTENT_2CTA; }
 bool has_ring(int v) { return v != VAR_SYNC_TILED && v != VAR_TMA_SERIAL; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -90,6 +98,17 @@ int choose_block_n(int variant, int64_t M, int64_t N, int sms)
     return best;
 }
 
+// Default kernel: CTA pairs (256x256 tiles, cta_group::2) when M spans more
+// than one 128-row tile and there are enough pair tiles to occupy every TPC;
+// otherwise single-CTA persistent tiles, whose narrower widths keep more SMs
+// busy on small or skinny problems.
+int auto_variant(int64_t M, int64_t N, int sms)
+{
+    const int64_t pair_tiles = ceil_div(M, 2 * BLK_M) * ceil_div(N, 256);
+    if (M > BLK_M && pair_tiles >= sms / 2) return VAR_PERSISTENT_2CTA;
+    return VAR_PERSISTENT;
+}
+
 int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_options* o,
                        int sms, int smem_optin, gemm_config* c)
 {
@@ -109,7 +128,7 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     if ((N * elt) % 16 != 0)
         return fail(GEMM_ERR_UNSUPPORTED,
                     "N * sizeof(output) must be a multiple of 16 bytes (TMA row stride of C)");
-    if (opts.variant < 0 || opts.variant > VAR_PERSISTENT_LOCKSTEP)
+    if (opts.variant < 0 || opts.variant > VAR_PERSISTENT_2CTA)
         return fail(GEMM_ERR_INVALID_ARG, "unknown variant");
     if (opts.pipe_depth < 0 || opts.pipe_depth > MAX_STAGES)
         return fail(GEMM_ERR_INVALID_ARG, "pipe_depth must be 0 (auto) or 1..8");
@@ -119,10 +138,18 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
         return fail(GEMM_ERR_INVALID_ARG, "group_m, grid and wait_budget_ms must be >= 0");
     if (sms < 1 || smem_optin < 1) return fail(GEMM_ERR_INVALID_ARG, "bad device limits");
 
-    const int variant = opts.variant == VAR_AUTO ? VAR_PERSISTENT : opts.variant;
+    const int variant = opts.variant == VAR_AUTO ? auto_variant(M, N, sms) : opts.variant;
     if (opts.debug_stall && !is_ws(variant))
         return fail(GEMM_ERR_INVALID_ARG, "debug_stall needs a warp-specialised variant");
-    const int bn = opts.block_n ? opts.block_n : choose_block_n(variant, M, N, sms);
+    if (is_pair(variant) && opts.block_n != 0 && opts.block_n != 256)
+        return fail(GEMM_ERR_INVALID_ARG, "the CTA-pair variant uses 256x256 tiles (block_n 0 or 256)");
+    const int bn = is_pair(variant) ? 256
+                   : opts.block_n   ? opts.block_n
+                                    : choose_block_n(variant, M, N, sms);
+    // Shared memory per CTA holds B tiles of `bn_cta` rows: a CTA of a pair
+    // keeps half of the pair tile's B rows.
+    const int bn_cta = is_pair(variant) ? bn / 2 : bn;
+    const int bm = is_pair(variant) ? 2 * BLK_M : BLK_M;
     const int staging = variant == VAR_SYNC_TILED ? 0 : NUM_STAGING;
 
     int depth;
@@ -132,28 +159,28 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
         depth = 1;
     } else if (opts.pipe_depth) {
         depth = opts.pipe_depth;
-        const uint32_t need = smem_layout(depth, bn, staging).total;
+        const uint32_t need = smem_layout(depth, bn_cta, staging).total;
         if (need > static_cast<uint32_t>(smem_optin)) {
             char buf[200];
             std::snprintf(buf, sizeof(buf),
-                          "pipe_depth %d with a 128x%d tile does not fit: %u bytes of shared memory > %d available",
-                          depth, bn, need, smem_optin);
+                          "pipe_depth %d with a %dx%d tile does not fit: %u bytes of shared memory > %d available",
+                          depth, bm, bn, need, smem_optin);
             return fail(GEMM_ERR_UNSUPPORTED, buf);
         }
     } else {
         depth = 0;
         for (int d = MAX_STAGES; d >= 1; --d)
-            if (smem_layout(d, bn, staging).total <= static_cast<uint32_t>(smem_optin)) {
+            if (smem_layout(d, bn_cta, staging).total <= static_cast<uint32_t>(smem_optin)) {
                 depth = d;
                 break;
             }
         if (depth == 0) return fail(GEMM_ERR_UNSUPPORTED, "no stage count fits shared memory");
     }
 
-    const int64_t tm = ceil_div(M, BLK_M), tn = ceil_div(N, bn);
+    const int64_t tm = ceil_div(M, bm), tn = ceil_div(N, bn);
     const int64_t tiles = tm * tn;
     if (tiles > LIM) return fail(GEMM_ERR_UNSUPPORTED, "too many output tiles");
-    uint32_t smem = smem_layout(depth, bn, staging).total;
+    uint32_t smem = smem_layout(depth, bn_cta, staging).total;
     if (is_persistent(variant)) {
         // One resident CTA per SM: ask for more than half of the SM's shared
         // memory so that a second CTA can never be co-scheduled.
@@ -164,7 +191,7 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
 
     std::memset(c, 0, sizeof(*c));
     c->variant = variant;
-    c->block_m = BLK_M;
+    c->block_m = bm;
     c->block_n = bn;
     c->block_k = BLK_K;
     c->pipe_depth = depth;
@@ -173,7 +200,13 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     c->tiles_n = static_cast<int>(tn);
     c->num_tiles = static_cast<int>(tiles);
     c->k_blocks = static_cast<int>(ceil_div(K, BLK_K));
-    if (is_persistent(variant)) {
+    if (is_pair(variant)) {
+        // clusters of two CTAs, one pair tile per cluster at a time
+        int64_t pairs = (opts.grid ? opts.grid : sms) / 2;
+        if (pairs < 1) pairs = 1;
+        if (pairs > tiles) pairs = tiles;
+        c->grid = static_cast<int>(2 * pairs);
+    } else if (is_persistent(variant)) {
         int64_t g = opts.grid ? opts.grid : sms;
         if (g > tiles) g = tiles;
         c->grid = static_cast<int>(g);
@@ -182,8 +215,9 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     }
     c->threads = is_ws(variant) ? 192 : 128;
     c->smem_bytes = static_cast<int>(smem);
-    c->tmem_cols = (variant == VAR_PERSISTENT) ? 2 * bn : bn;
-    c->tx_bytes = static_cast<int>(stage_tx_bytes(bn));
+    c->tmem_cols = (variant == VAR_PERSISTENT || is_pair(variant)) ? 2 * bn : bn;
+    c->tx_bytes = static_cast<int>(is_pair(variant) ? 2 * stage_tx_bytes(bn_cta)
+                                                    : stage_tx_bytes(bn));
     return ok();
 }
 
@@ -347,7 +381,8 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
                           plan->K * 2, BLK_K, BLK_M, "A");
         if (r == GEMM_OK)
             r = encode_2d(&plan->tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, plan->K, plan->N,
-                          plan->K * 2, BLK_K, c.block_n, "B");
+                          plan->K * 2, BLK_K, is_pair(c.variant) ? c.block_n / 2 : c.block_n,
+                          "B");
         if (r == GEMM_OK) {
             if (plan->dtype == GEMM_OUT_F16)
                 r = encode_2d(&plan->tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, plan->N, plan->M,
@@ -395,7 +430,9 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
     p.debug_stall = plan->debug_stall;
 
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-    e = is_ws(c.variant) ? launch_ws(s, stream) : launch_ladder(s, stream);
+    e = is_pair(c.variant) ? launch_pair(s, stream)
+        : is_ws(c.variant) ? launch_ws(s, stream)
+                           : launch_ladder(s, stream);
     if (e != cudaSuccess) return cuda_fail("kernel launch", e);
     return ok();
 }

@@ -109,6 +109,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
             int stage = 0;
             uint32_t phase = 0;
             int issued = 0;
+            int end_stage = 0;       // ring position just after the last issued load
+            uint32_t end_phase = 0;
             for (int t = static_cast<int>(blockIdx.x); t < p.num_tiles; t += tile_step) {
                 int mt, nt;
                 raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
@@ -128,12 +130,16 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
                         stage = 0;
                         phase ^= 1u;
                     }
+                    if (!wd.aborted) {
+                        end_stage = stage;
+                        end_phase = phase;
+                    }
                 }
             }
             // drain: the last min(D, issued) loads have landed before exit
             if (wd.aborted) {
-                int st = stage;
-                uint32_t ph = phase;
+                int st = end_stage;
+                uint32_t ph = end_phase;
                 for (int i = 0; i < D && i < issued; ++i) {
                     if (st == 0) {
                         st = D - 1;

@@ -16,7 +16,8 @@ enum : int {
     VAR_PIPELINED = 3,
     VAR_WS_PIPELINED = 4,
     VAR_PERSISTENT = 5,
-    VAR_PERSISTENT_LOCKSTEP = 6
+    VAR_PERSISTENT_LOCKSTEP = 6,
+    VAR_PERSISTENT_2CTA = 7
 };
 
 struct LaunchSpec {
@@ -38,5 +39,8 @@ cudaError_t launch_ladder(const LaunchSpec& s, cudaStream_t stream);
 
 // Warp-specialised variants: VAR_WS_PIPELINED, VAR_PERSISTENT.
 cudaError_t launch_ws(const LaunchSpec& s, cudaStream_t stream);
+
+// Warp-specialised persistent GEMM on CTA pairs: VAR_PERSISTENT_2CTA.
+cudaError_t launch_pair(const LaunchSpec& s, cudaStream_t stream);
 
 }  // namespace tg
