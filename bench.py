@@ -243,6 +243,7 @@ def main():
     ap.add_argument("--depth", type=int, default=0)
     ap.add_argument("--block-n", type=int, default=0)
     ap.add_argument("--group-m", type=int, default=0)
+    ap.add_argument("--stream-k", default="auto", choices=["auto", "off", "on"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -284,7 +285,7 @@ def main():
     out_dt = torch.float16 if cfg["out"] == "f16" else torch.float32
     dC = torch.empty((M, N), dtype=out_dt, device="cuda")
     plan = pkg.Plan(M, N, K, out=cfg["out"], variant=args.variant, pipe_depth=args.depth,
-                    block_n=args.block_n, group_m=args.group_m)
+                    block_n=args.block_n, group_m=args.group_m, stream_k=args.stream_k)
     stream = torch.cuda.Stream()
     sh = stream.cuda_stream
 

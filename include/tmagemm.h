@@ -83,6 +83,13 @@ typedef struct {
     int debug_stall;    /* 1: the producer first waits on a barrier that nothing
                            completes, so the run ends in GEMM_ERR_TIMEOUT (for
                            testing the watchdog; warp-specialised variants) */
+    int stream_k;       /* persistent warp-specialised variants: 0 = auto (off),
+                           1 = off, 2 = on whenever the tile count leaves a
+                           partial last wave.  With stream-K the tiles of the
+                           partial last wave are split into K-block ranges
+                           shared evenly by all CTAs (or pairs); partial sums go
+                           through a workspace the plan owns and are added in a
+                           fixed order, so results do not vary from run to run. */
 } gemm_options;
 
 /* Resolved configuration of a plan (also returned by gemm_select_config). */
@@ -97,6 +104,11 @@ typedef struct {
     int smem_bytes;     /* dynamic shared memory per CTA */
     int tmem_cols;      /* TMEM columns allocated per CTA */
     int tx_bytes;       /* bytes one stage's barrier expects (A + B tile) */
+    int dp_tiles;       /* tiles computed whole */
+    int sk_tiles;       /* tiles of the stream-K part (0: none) */
+    int sk_kb_per_worker; /* K blocks of the stream-K part per CTA / pair */
+    int sk_max_contrib; /* most CTAs / pairs that share one stream-K tile */
+    long long workspace_bytes; /* device workspace the plan allocates for stream-K */
 } gemm_config;
 
 /* Create a plan for C[M x N] = A[M x K] . B[N x K]^T on the current CUDA
@@ -105,7 +117,10 @@ typedef struct {
  * multiples of 16 bytes, "05 Async Data Movement - TMA", the tensor-map
  * descriptor; a TMA copy must start on a 16-byte boundary).  Returns NULL on
  * error (gemm_last_status() / gemm_last_error() say why).  The plan owns host
- * state and a 32-byte device status record; nothing else is allocated. */
+ * state, a 32-byte device status record and, when its configuration uses
+ * stream-K, a device workspace of gemm_config.workspace_bytes; because of
+ * that workspace, runs of one plan must not overlap on the GPU (use one plan
+ * per concurrent stream). */
 TMAGEMM_API gemm_plan* gemm_create_plan(int64_t M, int64_t N, int64_t K, int dtype_out);
 
 /* Same with options (NULL = all automatic).  An explicit pipe_depth whose ring
@@ -162,6 +177,15 @@ TMAGEMM_API int gemm_select_config(int64_t M, int64_t N, int64_t K, int dtype_ou
  * raster order the kernels use ("GEMM II -- pipelining with TMA", Step 6,
  * l2_group_size).  Returns GEMM_ERR_INVALID_ARG if tile is out of range. */
 TMAGEMM_API int gemm_schedule_tile(const gemm_config* cfg, int64_t tile, int* m_tile, int* n_tile);
+
+/* Work unit `index` (0, 1, ...) of persistent worker `worker` (a CTA, or a
+ * CTA pair for the pair variant) under `cfg`, in the order the kernels process
+ * them: whole tiles first, then the worker's share of the stream-K part.
+ * Writes the tile (raster index), its K-block range [kb0, kb1) and the
+ * worker's rank among the tile's contributors; returns 1, or 0 when the
+ * worker has no unit `index`, or GEMM_ERR_INVALID_ARG. */
+TMAGEMM_API int gemm_schedule_unit(const gemm_config* cfg, int worker, int index, int* tile,
+                                   int* kb0, int* kb1, int* contrib, int* ncontrib);
 
 /* Byte offset of logical byte `byte_in_row` of row `row` inside a
  * 1024-byte-aligned tile of 128-byte rows stored with the 128-byte swizzle

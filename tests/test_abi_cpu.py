@@ -193,3 +193,54 @@ def test_swizzle_map_matches_page_rule_and_bank_analysis(b):
         sectors = {((col % 8) ^ ((2 * r + col // 8) % 8)) for r in range(8)}
         assert len(sectors) == int(g["ungrouped_distinct_bank_sectors"])
     assert b.gemm_sw128_offset(0, 128) == -1
+
+
+@pytest.mark.parametrize("M,N,K,opts", [
+    (8192, 8192, 8192, {"stream_k": "on"}),                   # pair, 36-tile tail
+    (4096, 4096, 4096, {"stream_k": "on"}),
+    (4000, 3000, 5000, {"stream_k": "on"}),                   # ragged K blocks
+    (64, 16384, 16384, {"stream_k": "on"}),                   # every tile shared
+    (1000, 1000, 520, {"variant": "persistent", "grid": 7, "stream_k": "on"}),
+    (1000, 1000, 520, {"variant": "persistent_2cta", "grid": 10, "stream_k": "on"}),
+    (300, 520, 64, {"variant": "persistent", "stream_k": "on"}),   # one K block per tile
+])
+def test_work_units_cover_every_k_block_once(b, M, N, K, opts):
+    st, c = b.gemm_select_config(M, N, K, 1, b.make_options(**opts))
+    assert st == 0, b.last_error()
+    workers = c.grid // 2 if c.variant == b.GEMM_VAR_PERSISTENT_2CTA else c.grid
+    cover = np.zeros((c.num_tiles, c.k_blocks), dtype=np.int64)
+    contribs = {}
+    work = []
+    for w in range(workers):
+        units = b.gemm_worker_units(c, w)
+        work.append(sum(kb1 - kb0 for _, kb0, kb1, _, _ in units))
+        for tile, kb0, kb1, j, nc in units:
+            assert 0 <= kb0 < kb1 <= c.k_blocks
+            cover[tile, kb0:kb1] += 1
+            if nc > 1:
+                assert tile >= c.dp_tiles and nc <= c.sk_max_contrib
+                contribs.setdefault(tile, []).append((j, kb0, kb1, nc))
+            else:
+                assert (kb0, kb1) == (0, c.k_blocks) or tile >= c.dp_tiles
+    assert (cover == 1).all()
+    for tile, lst in contribs.items():
+        lst.sort()
+        assert [j for j, _, _, _ in lst] == list(range(lst[0][3]))  # ranks 0..n-1, once each
+        assert all(a[2] == b_[1] for a, b_ in zip(lst, lst[1:]))     # ranks follow K order
+    if c.sk_tiles:
+        # equal shares: every worker's K-block count within one range of the others
+        assert max(work) - min(work) <= c.sk_kb_per_worker
+
+
+def test_stream_k_choice(b):
+    on = b.make_options(stream_k="on")
+    st, c = b.gemm_select_config(8192, 8192, 8192, 1, on)
+    assert (c.dp_tiles, c.sk_tiles, c.sk_kb_per_worker) == (988, 36, 61)
+    assert c.dp_tiles % (c.grid // 2) == 0
+    for opts in (None, b.make_options(stream_k="off")):  # auto = off
+        st, c = b.gemm_select_config(8192, 8192, 8192, 1, opts)
+        assert (c.dp_tiles, c.sk_tiles, c.workspace_bytes) == (1024, 0, 0)
+    st, c = b.gemm_select_config(64, 16384, 16384, 1, on)
+    assert c.grid == 152 and c.sk_tiles == c.num_tiles == 128 and c.dp_tiles == 0
+    st, c = b.gemm_select_config(64, 16384, 16384, 1)
+    assert c.grid == 128 and c.sk_tiles == 0

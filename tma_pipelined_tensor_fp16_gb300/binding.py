@@ -33,14 +33,15 @@ VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 class gemm_options(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("variant", "pipe_depth", "block_n", "group_m", "grid", "wait_budget_ms",
-                 "debug_stall")]
+                 "debug_stall", "stream_k")]
 
 
 class gemm_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("variant", "block_m", "block_n", "block_k", "pipe_depth", "group_m", "grid",
                  "threads", "tiles_m", "tiles_n", "num_tiles", "k_blocks", "smem_bytes",
-                 "tmem_cols", "tx_bytes")]
+                 "tmem_cols", "tx_bytes", "dp_tiles", "sk_tiles", "sk_kb_per_worker",
+                 "sk_max_contrib")] + [("workspace_bytes", ctypes.c_longlong)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -71,6 +72,8 @@ _SIGS = {
                                           ctypes.POINTER(ctypes.c_int),
                                           ctypes.POINTER(ctypes.c_int)]),
     "gemm_sw128_offset": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int64]),
+    "gemm_schedule_unit": (ctypes.c_int, [ctypes.POINTER(gemm_config), ctypes.c_int, ctypes.c_int]
+                           + [ctypes.POINTER(ctypes.c_int)] * 5),
     "gemm_run_noalloc": (ctypes.c_int, [ctypes.c_int64] * 3 + [ctypes.c_int] + [ctypes.c_void_p] * 4
                          + [ctypes.POINTER(ctypes.c_int)]),
 }
@@ -105,10 +108,14 @@ def _check(status):
     return status
 
 
+STREAM_K = {"auto": 0, "off": 1, "on": 2}
+
+
 def make_options(variant="auto", pipe_depth=0, block_n=0, group_m=0, grid=0, wait_budget_ms=0,
-                 debug_stall=0):
+                 debug_stall=0, stream_k="auto"):
     v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
-    return gemm_options(v, pipe_depth, block_n, group_m, grid, wait_budget_ms, debug_stall)
+    sk = STREAM_K[stream_k] if isinstance(stream_k, str) else int(stream_k)
+    return gemm_options(v, pipe_depth, block_n, group_m, grid, wait_budget_ms, debug_stall, sk)
 
 
 # ---- the C entry points under their own names ------------------------------
@@ -181,6 +188,27 @@ def gemm_schedule_tile(cfg, tile):
     m, n = ctypes.c_int(), ctypes.c_int()
     st = lib().gemm_schedule_tile(ctypes.byref(cfg), tile, ctypes.byref(m), ctypes.byref(n))
     return st, m.value, n.value
+
+
+def gemm_schedule_unit(cfg, worker, index):
+    """(tile, kb0, kb1, contrib, ncontrib) of a worker's unit, or None past the end."""
+    v = [ctypes.c_int() for _ in range(5)]
+    st = lib().gemm_schedule_unit(ctypes.byref(cfg), worker, index, *[ctypes.byref(x) for x in v])
+    if st == 0:
+        return None
+    if st != 1:
+        raise GemmError(st, last_error())
+    return tuple(x.value for x in v)
+
+
+def gemm_worker_units(cfg, worker):
+    units, i = [], 0
+    while True:
+        u = gemm_schedule_unit(cfg, worker, i)
+        if u is None:
+            return units
+        units.append(u)
+        i += 1
 
 
 def gemm_sw128_offset(row, byte_in_row):

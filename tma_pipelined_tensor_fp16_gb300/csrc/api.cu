@@ -136,6 +136,8 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
         return fail(GEMM_ERR_INVALID_ARG, "block_n must be 0 (auto), 64, 128 or 256");
     if (opts.group_m < 0 || opts.grid < 0 || opts.wait_budget_ms < 0)
         return fail(GEMM_ERR_INVALID_ARG, "group_m, grid and wait_budget_ms must be >= 0");
+    if (opts.stream_k < 0 || opts.stream_k > 2)
+        return fail(GEMM_ERR_INVALID_ARG, "stream_k must be 0 (auto), 1 (off) or 2 (on)");
     if (sms < 1 || smem_optin < 1) return fail(GEMM_ERR_INVALID_ARG, "bad device limits");
 
     const int variant = opts.variant == VAR_AUTO ? auto_variant(M, N, sms) : opts.variant;
@@ -200,15 +202,33 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     c->tiles_n = static_cast<int>(tn);
     c->num_tiles = static_cast<int>(tiles);
     c->k_blocks = static_cast<int>(ceil_div(K, BLK_K));
+    // Stream-K (persistent warp-specialised variants) decides whether a grid
+    // larger than the tile count pays: the extra workers share the K blocks.
+    const int64_t KBLK = ceil_div(K, BLK_K);
+    auto stream_k_worth = [&](int64_t T, int64_t workers) {
+        const int64_t rem = T % workers;
+        if (rem == 0 || opts.stream_k == 1) return false;
+        const int64_t sk = T >= workers ? rem : T;
+        const int64_t L = ceil_div(sk * KBLK, workers);
+        const int64_t maxc = ceil_div(KBLK, L) + 1;
+        if (maxc > 255 || sk * KBLK >= LIM) return false;
+        // Only on request: on this power-capped part the idle SMs of a
+        // partial last wave let the busy ones clock higher, and spreading the
+        // tail over every SM measured slower than leaving it data-parallel for
+        // the 4096^3, 8192^3 and 4000x3000x5000 workloads.
+        (void)L;
+        return opts.stream_k == 2;
+    };
+    const bool sk_capable = variant == VAR_PERSISTENT || is_pair(variant);
     if (is_pair(variant)) {
         // clusters of two CTAs, one pair tile per cluster at a time
         int64_t pairs = (opts.grid ? opts.grid : sms) / 2;
         if (pairs < 1) pairs = 1;
-        if (pairs > tiles) pairs = tiles;
+        if (pairs > tiles && !stream_k_worth(tiles, pairs)) pairs = tiles;
         c->grid = static_cast<int>(2 * pairs);
     } else if (is_persistent(variant)) {
         int64_t g = opts.grid ? opts.grid : sms;
-        if (g > tiles) g = tiles;
+        if (g > tiles && !(sk_capable && stream_k_worth(tiles, g))) g = tiles;
         c->grid = static_cast<int>(g);
     } else {
         c->grid = static_cast<int>(tiles);
@@ -218,6 +238,31 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     c->tmem_cols = (variant == VAR_PERSISTENT || is_pair(variant)) ? 2 * bn : bn;
     c->tx_bytes = static_cast<int>(is_pair(variant) ? 2 * stage_tx_bytes(bn_cta)
                                                     : stage_tx_bytes(bn));
+
+    // Stream-K tail: whole waves stay data-parallel; the tiles of a partial
+    // last wave are cut into equal K-block ranges, one per worker.
+    c->dp_tiles = c->num_tiles;
+    if (sk_capable) {
+        const int64_t workers = is_pair(variant) ? c->grid / 2 : c->grid;
+        const int64_t T = c->num_tiles, KB = c->k_blocks;
+        if (stream_k_worth(T, workers)) {
+            const int64_t sk = T >= workers ? T % workers : T;
+            const int64_t L = ceil_div(sk * KB, workers);
+            const int64_t maxc = ceil_div(KB, L) + 1;
+            {
+                const int halves = is_pair(variant) ? 2 : 1;
+                c->dp_tiles = static_cast<int>(T - sk);
+                c->sk_tiles = static_cast<int>(sk);
+                c->sk_kb_per_worker = static_cast<int>(L);
+                c->sk_max_contrib = static_cast<int>(maxc);
+                // one fp32 slot of BLK_M x (tile columns) per contributor and
+                // CTA, then one ticket word per tile and CTA
+                c->workspace_bytes =
+                    sk * maxc * halves * static_cast<long long>(BLK_M) * bn * 4 +
+                    ((sk * halves * 4 + 255) / 256) * 256;
+            }
+        }
+    }
     return ok();
 }
 
@@ -277,6 +322,8 @@ struct gemm_plan {
     const void* mapB_ptr;
     const void* mapC_ptr;
     CUtensorMap tmA, tmB, tmC;
+    // stream-K workspace: partial tiles, then the ticket words
+    void* d_workspace;
     // device buffers of gemm_run_host
     void* hA;
     void* hB;
@@ -338,9 +385,15 @@ gemm_plan* gemm_create_plan_ex(int64_t M, int64_t N, int64_t K, int dtype_out,
     p->debug_stall = opts ? opts->debug_stall : 0;
     e = cudaMalloc(&p->d_status, sizeof(DevStatus));
     if (e == cudaSuccess) e = cudaMemset(p->d_status, 0, sizeof(DevStatus));
+    if (e == cudaSuccess && p->cfg.workspace_bytes > 0) {
+        e = cudaMalloc(&p->d_workspace, static_cast<size_t>(p->cfg.workspace_bytes));
+        if (e == cudaSuccess)
+            e = cudaMemset(p->d_workspace, 0, static_cast<size_t>(p->cfg.workspace_bytes));
+    }
     if (e != cudaSuccess) {
-        cuda_fail("allocating the device status record", e);
+        cuda_fail("allocating the device status record / stream-K workspace", e);
         if (p->d_status) cudaFree(p->d_status);
+        if (p->d_workspace) cudaFree(p->d_workspace);
         delete p;
         return nullptr;
     }
@@ -348,10 +401,11 @@ gemm_plan* gemm_create_plan_ex(int64_t M, int64_t N, int64_t K, int dtype_out,
     const gemm_config& c = p->cfg;
     std::snprintf(buf, sizeof(buf),
                   "variant=%s tile=%dx%dx%d pipe_depth=%d smem=%d grid=%d threads=%d tiles=%d (%dx%d) "
-                  "k_blocks=%d tmem_cols=%d group_m=%d out=%s",
+                  "k_blocks=%d tmem_cols=%d group_m=%d out=%s stream_k=%d/%d(L=%d)",
                   variant_name(c.variant), c.block_m, c.block_n, c.block_k, c.pipe_depth,
                   c.smem_bytes, c.grid, c.threads, c.num_tiles, c.tiles_m, c.tiles_n, c.k_blocks,
-                  c.tmem_cols, c.group_m, dtype_out == GEMM_OUT_F16 ? "f16" : "f32");
+                  c.tmem_cols, c.group_m, dtype_out == GEMM_OUT_F16 ? "f16" : "f32", c.sk_tiles,
+                  c.num_tiles, c.sk_kb_per_worker);
     p->desc = buf;
     ok();
     return p;
@@ -428,6 +482,21 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
     p.epoch = plan->epoch;
     p.budget_ns = plan->budget_ns;
     p.debug_stall = plan->debug_stall;
+    p.dp_tiles = c.dp_tiles;
+    p.sk_tiles = c.sk_tiles;
+    p.sk_kb_per_worker = c.sk_kb_per_worker;
+    p.sk_max_contrib = c.sk_max_contrib;
+    if (c.sk_tiles > 0) {
+        const int halves = is_pair(c.variant) ? 2 : 1;
+        const size_t partial_bytes = static_cast<size_t>(c.sk_tiles) * c.sk_max_contrib * halves *
+                                     BLK_M * c.block_n * 4;
+        p.sk_partials = static_cast<float*>(plan->d_workspace);
+        p.sk_tickets = reinterpret_cast<unsigned*>(static_cast<char*>(plan->d_workspace) +
+                                                   partial_bytes);
+    } else {
+        p.sk_partials = nullptr;
+        p.sk_tickets = nullptr;
+    }
 
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     e = is_pair(c.variant) ? launch_pair(s, stream)
@@ -485,6 +554,7 @@ void gemm_destroy(gemm_plan* plan)
 {
     if (!plan) return;
     if (plan->d_status) cudaFree(plan->d_status);
+    if (plan->d_workspace) cudaFree(plan->d_workspace);
     if (plan->hA) cudaFree(plan->hA);
     if (plan->hB) cudaFree(plan->hB);
     if (plan->hC) cudaFree(plan->hC);
@@ -515,6 +585,31 @@ int gemm_schedule_tile(const gemm_config* cfg, int64_t tile, int* m_tile, int* n
     raster_tile(static_cast<int>(tile), cfg->tiles_m, cfg->tiles_n, cfg->group_m, *m_tile,
                 *n_tile);
     return ok();
+}
+
+int gemm_schedule_unit(const gemm_config* cfg, int worker, int index, int* tile, int* kb0,
+                       int* kb1, int* contrib, int* ncontrib)
+{
+    if (!cfg || !tile || !kb0 || !kb1 || !contrib || !ncontrib || index < 0)
+        return fail(GEMM_ERR_INVALID_ARG, "NULL argument or negative index");
+    const int workers = is_pair(cfg->variant) ? cfg->grid / 2 : cfg->grid;
+    if (worker < 0 || worker >= workers) return fail(GEMM_ERR_INVALID_ARG, "worker out of range");
+    WorkIter it;
+    it.init(worker, workers, cfg->dp_tiles, cfg->sk_tiles, cfg->k_blocks, cfg->sk_kb_per_worker);
+    WorkUnit u;
+    for (int i = 0; it.next(u); ++i) {
+        if (i == index) {
+            *tile = u.tile;
+            *kb0 = u.kb0;
+            *kb1 = u.kb1;
+            *contrib = u.contrib;
+            *ncontrib = u.ncontrib;
+            ok();
+            return 1;
+        }
+    }
+    ok();
+    return 0;
 }
 
 int64_t gemm_sw128_offset(int64_t row, int64_t byte_in_row)
@@ -610,6 +705,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     gemm_options opts;
     std::memset(&opts, 0, sizeof(opts));
     opts.variant = VAR_PERSISTENT;
+    opts.stream_k = 1;  // no workspace: every tile whole
     gemm_config c;
     int r = select_config_impl(M, N, K, dtype_out, &opts, sms, smem_optin, &c);
     if (r != GEMM_OK) return r;
@@ -667,6 +763,12 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     }
     p.budget_ns = 2000ull * 1000000ull;
     p.debug_stall = 0;
+    p.dp_tiles = c.num_tiles;
+    p.sk_tiles = 0;
+    p.sk_kb_per_worker = 0;
+    p.sk_max_contrib = 0;
+    p.sk_partials = nullptr;
+    p.sk_tickets = nullptr;
     e = launch_ws(s, stream);
     if (e != cudaSuccess) return cuda_fail("kernel launch", e);
 

@@ -128,12 +128,50 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
+// Stage one output sub-tile held in registers (`v`: SUB_COLS fp32 values of
+// output row `row`, as raw bits) and TMA-store it at (col0, m0).
 // `staging`: shared address of NUM_STAGING buffers of STAGING_BYTES, 1024-B
 // aligned.  `sub_count` counts the sub-tiles this group has staged so far (it
 // carries across tiles and selects the staging buffer).  `bar_id` is a named
 // barrier reserved for the 128 threads.  `issuer` is exactly one thread of the
-// group.  Stores are skipped (but every barrier is still executed) when
+// group.  The store is skipped (but every barrier is still executed) when
 // `do_store` is false.
+template <bool F16OUT>
+__device__ __forceinline__ void stage_and_store(const uint32_t* v, uint32_t row, bool issuer,
+                                                uint32_t staging, const CUtensorMap* tmap_c,
+                                                int col0, int m0, uint32_t& sub_count,
+                                                uint32_t bar_id, bool do_store)
+{
+    const uint32_t buf = staging + (sub_count & 1u) * STAGING_BYTES;
+    if (sub_count >= 2) {
+        // the store issued two sub-tiles ago read this buffer
+        if (issuer) bulk_wait_group_read<1>();
+        named_bar_sync(bar_id, 128);
+    }
+    const uint32_t row_base = buf + row * 128u;
+#pragma unroll
+    for (uint32_t c = 0; c < 8; ++c) {
+        const uint32_t dst = row_base + ((c ^ (row & 7u)) << 4);
+        if constexpr (F16OUT) {
+            st_shared_v4(dst, pack_half2(v[8 * c + 0], v[8 * c + 1]),
+                         pack_half2(v[8 * c + 2], v[8 * c + 3]),
+                         pack_half2(v[8 * c + 4], v[8 * c + 5]),
+                         pack_half2(v[8 * c + 6], v[8 * c + 7]));
+        } else {
+            st_shared_v4(dst, v[4 * c + 0], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(bar_id, 128);
+    if (issuer && do_store) {
+        tma_store_2d(tmap_c, buf, col0, m0);
+        bulk_commit_group();
+    }
+    ++sub_count;
+}
+
+// The whole 128 x BLOCK_N accumulator at TMEM column `tmem_acc`, sub-tile by
+// sub-tile: TMEM -> registers -> staging -> TMA store.
 template <int BLOCK_N, bool F16OUT>
 __device__ __forceinline__ void epilogue_tma_store(uint32_t tmem_acc, int q, uint32_t lane,
                                                    bool issuer, uint32_t staging,
@@ -148,7 +186,6 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t tmem_acc, int q, uin
     for (int j = 0; j < S::NUM_SUB; ++j) {
         const int col0 = n0 + j * S::SUB_COLS;
         if (col0 >= N) break;  // uniform across the group: the rest is past the edge
-
         uint32_t v[S::SUB_COLS];
         if constexpr (F16OUT) {
             tmem_load_32cols(taddr + j * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
@@ -156,33 +193,130 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t tmem_acc, int q, uin
         } else {
             tmem_load_32cols(taddr + j * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
         }
+        stage_and_store<F16OUT>(v, row, issuer, staging, tmap_c, col0, m0, sub_count, bar_id,
+                                do_store);
+    }
+}
 
-        const uint32_t buf = staging + (sub_count & 1u) * STAGING_BYTES;
-        if (sub_count >= 2) {
-            // the store issued two sub-tiles ago read this buffer
-            if (issuer) bulk_wait_group_read<1>();
-            named_bar_sync(bar_id, 128);
-        }
-        const uint32_t row_base = buf + row * 128u;
+// ------------------------------------------------------ stream-K fix-up
+//
+// A tile of the stream-K part is accumulated by several workers, each over
+// its own range of K blocks.  Every contributor writes its fp32 partial tile
+// to its own workspace slot, publishes it (fence, then an arrival ticket on
+// the tile's counter), and the contributor that draws the last ticket sums
+// all partials in contributor order (0, 1, ..., in K order) and stores the
+// tile.  The order of the sum never depends on which contributor arrives
+// last, so results are identical run to run.  Slot layout: the value of
+// (row r, column c) sits at float offset ((c / 4) * 128 + r) * 4 + c % 4, so a
+// warp's 16-byte accesses to one column group cover 512 contiguous bytes.
+
+// Fold this run's arrival into the tile's ticket word (epoch << 8 | count)
+// and return the arrival rank; a word left by an earlier run starts over.
+__device__ __forceinline__ uint32_t sk_take_ticket(unsigned* word, int epoch)
+{
+    const uint32_t ep = static_cast<uint32_t>(epoch) & 0xFFFFFFu;
+    uint32_t cur = *reinterpret_cast<volatile unsigned*>(word);
+    while (true) {
+        const bool same = (cur >> 8) == ep;
+        const uint32_t want = same ? cur + 1u : ((ep << 8) | 1u);
+        const uint32_t prev = atomicCAS(word, cur, want);
+        if (prev == cur) return same ? (cur & 0xFFu) : 0u;
+        cur = prev;
+    }
+}
+
+// Write this CTA's 128 x BLOCK_N accumulator to a partial slot (rows past the
+// matrix are skipped).
+template <int BLOCK_N>
+__device__ __forceinline__ void sk_write_partial(uint32_t tmem_acc, int q, uint32_t lane,
+                                                 float* slot, bool row_valid)
+{
+    const uint32_t row = static_cast<uint32_t>(q) * 32u + lane;
+    const uint32_t taddr = tmem_acc + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+    for (int j = 0; j < BLOCK_N / 32; ++j) {
+        uint32_t v[32];
+        tmem_load_32cols(taddr + j * 32, v);
+        if (!row_valid) continue;
 #pragma unroll
-        for (uint32_t c = 0; c < 8; ++c) {
-            const uint32_t dst = row_base + ((c ^ (row & 7u)) << 4);
-            if constexpr (F16OUT) {
-                st_shared_v4(dst, pack_half2(v[8 * c + 0], v[8 * c + 1]),
-                             pack_half2(v[8 * c + 2], v[8 * c + 3]),
-                             pack_half2(v[8 * c + 4], v[8 * c + 5]),
-                             pack_half2(v[8 * c + 6], v[8 * c + 7]));
-            } else {
-                st_shared_v4(dst, v[4 * c + 0], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        for (int c = 0; c < 8; ++c) {
+            float4* dst = reinterpret_cast<float4*>(slot) + (j * 8 + c) * 128 + row;
+            *dst = make_float4(__uint_as_float(v[4 * c + 0]), __uint_as_float(v[4 * c + 1]),
+                               __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+        }
+    }
+}
+
+// Sum the `ncontrib` partial slots (slot0, slot0 + slot_stride, ...) in order
+// and store the tile like epilogue_tma_store.
+template <int BLOCK_N, bool F16OUT>
+__device__ __forceinline__ void sk_reduce_store(const float* slot0, size_t slot_stride,
+                                                int ncontrib, int q, uint32_t lane, bool issuer,
+                                                uint32_t staging, const CUtensorMap* tmap_c,
+                                                int m0, int n0, int N, uint32_t& sub_count,
+                                                uint32_t bar_id, bool do_store, bool row_valid)
+{
+    using S = EpilogueShape<BLOCK_N, F16OUT>;
+    const uint32_t row = static_cast<uint32_t>(q) * 32u + lane;
+#pragma unroll 1
+    for (int j = 0; j < S::NUM_SUB; ++j) {
+        const int col0 = n0 + j * S::SUB_COLS;
+        if (col0 >= N) break;
+        float acc[S::SUB_COLS];
+#pragma unroll
+        for (int i = 0; i < S::SUB_COLS; ++i) acc[i] = 0.0f;
+        if (row_valid) {
+            for (int cj = 0; cj < ncontrib; ++cj) {
+                const float4* src = reinterpret_cast<const float4*>(slot0 + cj * slot_stride);
+#pragma unroll
+                for (int c = 0; c < S::SUB_COLS / 4; ++c) {
+                    const float4 x = __ldcg(src + (j * (S::SUB_COLS / 4) + c) * 128 + row);
+                    acc[4 * c + 0] += x.x;
+                    acc[4 * c + 1] += x.y;
+                    acc[4 * c + 2] += x.z;
+                    acc[4 * c + 3] += x.w;
+                }
             }
         }
-        fence_proxy_async_smem();
-        named_bar_sync(bar_id, 128);
-        if (issuer && do_store) {
-            tma_store_2d(tmap_c, buf, col0, m0);
-            bulk_commit_group();
-        }
-        ++sub_count;
+        stage_and_store<F16OUT>(reinterpret_cast<const uint32_t*>(acc), row, issuer, staging,
+                                tmap_c, col0, m0, sub_count, bar_id, do_store);
+    }
+}
+
+// Epilogue of one stream-K unit for a 128-thread group: write the partial,
+// release the accumulator (the caller's `release` callback, after the TMEM
+// reads), publish, and if this is the last arrival, reduce and store.
+// `ticket_smem` is a u32 in shared memory for broadcasting the ticket.
+template <int BLOCK_N, bool F16OUT, typename Release>
+__device__ __forceinline__ void sk_epilogue(uint32_t tmem_acc, int q, uint32_t lane, bool issuer,
+                                            uint32_t staging, const CUtensorMap* tmap_c, int m0,
+                                            int n0, int M, int N, uint32_t& sub_count,
+                                            uint32_t bar_id, bool aborted, float* slot0,
+                                            size_t slot_stride, int contrib, int ncontrib,
+                                            unsigned* ticket_word, int epoch,
+                                            volatile uint32_t* ticket_smem, Release release)
+{
+    const uint32_t row = static_cast<uint32_t>(q) * 32u + lane;
+    const bool row_valid = m0 + static_cast<int>(row) < M;
+    sk_write_partial<BLOCK_N>(tmem_acc, q, lane, slot0 + contrib * slot_stride,
+                              row_valid && !aborted);
+    release();
+    __threadfence();
+    named_bar_sync(bar_id, 128);
+    if (issuer) {
+        uint32_t t = 0xFFFFFFFFu;  // "not last" when aborted
+        if (!aborted) t = sk_take_ticket(ticket_word, epoch);
+        __threadfence();
+        *ticket_smem = t;
+    }
+    named_bar_sync(bar_id, 128);
+    const uint32_t ticket = *ticket_smem;
+    named_bar_sync(bar_id, 128);  // everyone has read the slot before it is reused
+    if (ticket == static_cast<uint32_t>(ncontrib - 1)) {
+        __threadfence();
+        sk_reduce_store<BLOCK_N, F16OUT>(slot0, slot_stride, ncontrib, q, lane, issuer, staging,
+                                         tmap_c, m0, n0, N, sub_count, bar_id, !aborted,
+                                         row_valid);
     }
 }
 

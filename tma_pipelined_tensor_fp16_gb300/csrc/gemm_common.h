@@ -72,6 +72,83 @@ struct Params {
     int epoch;                  // run counter, > 0
     unsigned long long budget_ns;  // bound on any single wait
     int debug_stall;            // 1: producer first waits on a barrier nothing completes
+    // Stream-K tail (persistent kernels).  The first dp_tiles tiles of the
+    // raster order (a multiple of the worker count) are whole tiles; the last
+    // sk_tiles tiles are cut into K-block ranges of sk_kb_per_worker blocks,
+    // one range per worker.  sk_tiles = 0: every tile is whole.
+    int dp_tiles;
+    int sk_tiles;
+    int sk_kb_per_worker;
+    int sk_max_contrib;         // most workers that can share one tile
+    float* sk_partials;         // [sk_tiles][sk_max_contrib][halves][tile rows x cols] fp32
+    unsigned* sk_tickets;       // [sk_tiles][halves] arrival tickets (epoch << 8 | count)
+};
+
+// One unit of a persistent worker's work: K blocks [kb0, kb1) of one output
+// tile.  sk_index < 0: a whole tile of the data-parallel part; otherwise the
+// tile's index inside the stream-K part, this worker's rank `contrib` among
+// the `ncontrib` workers that share it (ranks follow the K order).
+struct WorkUnit {
+    int tile;
+    int kb0, kb1;
+    int sk_index;
+    int contrib, ncontrib;
+};
+
+// The sequence of work units of worker `w` out of `workers`: first the whole
+// tiles w, w + workers, ... below dp_tiles, then the worker's contiguous range
+// [w*L, (w+1)*L) of the stream-K part's K blocks, taken tile by tile in
+// raster order (each tile's blocks in K order).  Every (tile, K block) pair is
+// covered by exactly one unit of one worker.
+struct WorkIter {
+    int workers, dp_tiles, KB, L;
+    int dp_next;
+    int sk_pos, sk_end;
+
+    TG_HD void init(int w, int nworkers, int dp, int sk, int k_blocks, int kb_per_worker)
+    {
+        workers = nworkers;
+        dp_tiles = dp;
+        KB = k_blocks;
+        L = kb_per_worker;
+        dp_next = w;
+        const long long sk_kb = static_cast<long long>(sk) * k_blocks;
+        const long long b = static_cast<long long>(w) * kb_per_worker;
+        const long long e = b + kb_per_worker;
+        sk_pos = static_cast<int>(sk > 0 && b < sk_kb ? b : 0);
+        sk_end = static_cast<int>(sk > 0 && b < sk_kb ? (e < sk_kb ? e : sk_kb) : 0);
+    }
+
+    TG_HD bool next(WorkUnit& u)
+    {
+        if (dp_next < dp_tiles) {
+            u.tile = dp_next;
+            u.kb0 = 0;
+            u.kb1 = KB;
+            u.sk_index = -1;
+            u.contrib = 0;
+            u.ncontrib = 1;
+            dp_next += workers;
+            return true;
+        }
+        if (sk_pos < sk_end) {
+            const int t = sk_pos / KB;
+            const int kb0 = sk_pos - t * KB;
+            const int left = sk_end - sk_pos;
+            const int kb1 = (KB - kb0) < left ? KB : kb0 + left;
+            const int first = (t * KB) / L;
+            const int last = ((t + 1) * KB - 1) / L;
+            u.tile = dp_tiles + t;
+            u.kb0 = kb0;
+            u.kb1 = kb1;
+            u.sk_index = t;
+            u.contrib = (sk_pos / L) - first;
+            u.ncontrib = last - first + 1;
+            sk_pos += kb1 - kb0;
+            return true;
+        }
+        return false;
+    }
 };
 
 // Grouped raster order of the output tiles ("GEMM II -- pipelining with TMA",
@@ -136,7 +213,8 @@ enum : int {
     BAR_STALL = BAR_DRAIN + 1,               // stall test: never completed
     BAR_COUNT = BAR_STALL + 1
 };
-constexpr uint32_t TMEM_SLOT_OFFSET = BAR_COUNT * 8;  // u32 TMEM base address
-static_assert(TMEM_SLOT_OFFSET + 4 <= BAR_AREA_BYTES, "barrier area too small");
+constexpr uint32_t TMEM_SLOT_OFFSET = BAR_COUNT * 8;     // u32 TMEM base address
+constexpr uint32_t TICKET_SLOT_OFFSET = TMEM_SLOT_OFFSET + 4;  // u32 stream-K ticket broadcast
+static_assert(TICKET_SLOT_OFFSET + 4 <= BAR_AREA_BYTES, "barrier area too small");
 
 }  // namespace tg

@@ -21,7 +21,10 @@
 // accumulators so the epilogue of tile i overlaps the main loop of tile i+1,
 // and the ring position {stage, phase} runs on continuously across tiles (the
 // tilus tutorial's single per-role phase that flips on wrap-around), so no
-// phase is ever reset.
+// phase is ever reset.  A persistent CTA's work is a sequence of WorkUnits:
+// whole tiles, then (when the tile count leaves a partial last wave) its
+// share of the stream-K part, finished through the fix-up in
+// device_common.cuh.
 #include "device_common.cuh"
 #include "launch.h"
 
@@ -73,8 +76,11 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
     const int warp = tid >> 5;
     const uint32_t lane = lane_id();
     Watchdog wd = make_watchdog(p);
-    const int tile_step = PERSIST ? static_cast<int>(gridDim.x) : p.num_tiles;
+    const int workers = PERSIST ? static_cast<int>(gridDim.x) : p.num_tiles;
     const int KB = p.k_blocks;
+    WorkIter units0;
+    units0.init(static_cast<int>(blockIdx.x), workers, PERSIST ? p.dp_tiles : p.num_tiles,
+                PERSIST ? p.sk_tiles : 0, KB, p.sk_kb_per_worker);
 
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
@@ -111,11 +117,14 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
             int issued = 0;
             int end_stage = 0;       // ring position just after the last issued load
             uint32_t end_phase = 0;
-            for (int t = static_cast<int>(blockIdx.x); t < p.num_tiles; t += tile_step) {
+            WorkIter units = units0;
+            WorkUnit u;
+            while (units.next(u)) {
+                const int t = u.tile;
                 int mt, nt;
                 raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
                 const int m0 = mt * BLK_M, n0 = nt * BN;
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     // a fresh barrier passes a wait on parity 1 at once: the
                     // first trip around the ring does not wait
                     wd.wait(bar_addr(bars, BAR_EMPTY + stage), phase ^ 1u, WAIT_EMPTY, t, kb);
@@ -160,13 +169,16 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
-            for (int t = static_cast<int>(blockIdx.x); t < p.num_tiles; t += tile_step) {
+            WorkIter units = units0;
+            WorkUnit u;
+            while (units.next(u)) {
+                const int t = u.tile;
                 // the epilogue has drained this accumulator (fresh: passes)
                 wd.wait(bar_addr(bars, BAR_TMEM_EMPTY + acc), acc_phase ^ 1u, WAIT_TMEM_EMPTY,
                         t, -1);
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     wd.wait(bar_addr(bars, BAR_FULL + stage), phase, WAIT_FULL, t, kb);
                     if (!wd.aborted) {
                         tc_fence_after_sync();
@@ -176,7 +188,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
                         for (int kk = 0; kk < BLK_K / MMA_K; ++kk)
                             mma_f16_ss(d_tmem, adesc + static_cast<uint64_t>(kk * 2),
                                        bdesc + static_cast<uint64_t>(kk * 2), idesc,
-                                       (kb == 0 && kk == 0) ? 0u : 1u);
+                                       (kb == u.kb0 && kk == 0) ? 0u : 1u);
                         // frees the stage once these MMAs have read it
                         mma_commit(bar_addr(bars, BAR_EMPTY + stage));
                     }
@@ -205,16 +217,36 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t sub_count = 0;
-        for (int t = static_cast<int>(blockIdx.x); t < p.num_tiles; t += tile_step) {
+        WorkIter units = units0;
+        WorkUnit u;
+        volatile uint32_t* ticket_smem =
+            reinterpret_cast<volatile uint32_t*>(sm.gen + L.bars + TICKET_SLOT_OFFSET);
+        while (units.next(u)) {
+            const int t = u.tile;
             int mt, nt;
             raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
             wd.wait(bar_addr(bars, BAR_TMEM_FULL + acc), acc_phase, WAIT_TMEM_FULL, t, -1);
             tc_fence_after_sync();
-            epilogue_tma_store<BN, F16OUT>(tmem_base + static_cast<uint32_t>(acc * BN), q, lane,
-                                           issuer, staging, &tmC, mt * BLK_M, nt * BN, p.N,
-                                           sub_count, EPI_BAR_ID, !wd.aborted);
-            tc_fence_before_sync();
-            mbar_arrive(bar_addr(bars, BAR_TMEM_EMPTY + acc));
+            const uint32_t tmem_acc = tmem_base + static_cast<uint32_t>(acc * BN);
+            const uint32_t empty_bar = bar_addr(bars, BAR_TMEM_EMPTY + acc);
+            if (u.ncontrib == 1) {
+                epilogue_tma_store<BN, F16OUT>(tmem_acc, q, lane, issuer, staging, &tmC,
+                                               mt * BLK_M, nt * BN, p.N, sub_count, EPI_BAR_ID,
+                                               !wd.aborted);
+                tc_fence_before_sync();
+                mbar_arrive(empty_bar);
+            } else {
+                const size_t slot_elems = static_cast<size_t>(BLK_M) * BN;
+                float* slot0 = p.sk_partials +
+                               static_cast<size_t>(u.sk_index) * p.sk_max_contrib * slot_elems;
+                sk_epilogue<BN, F16OUT>(tmem_acc, q, lane, issuer, staging, &tmC, mt * BLK_M,
+                                        nt * BN, p.M, p.N, sub_count, EPI_BAR_ID, wd.aborted,
+                                        slot0, slot_elems, u.contrib, u.ncontrib,
+                                        p.sk_tickets + u.sk_index, p.epoch, ticket_smem, [&] {
+                                            tc_fence_before_sync();
+                                            mbar_arrive(empty_bar);
+                                        });
+            }
             if (ACC == 2) {
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;

@@ -79,6 +79,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
     const int pair = static_cast<int>(blockIdx.x >> 1);
     const int npairs = static_cast<int>(gridDim.x >> 1);
     const int KB = p.k_blocks;
+    WorkIter units0;
+    units0.init(pair, npairs, p.dp_tiles, p.sk_tiles, KB, p.sk_kb_per_worker);
 
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
@@ -116,12 +118,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
             int armed = 0;
             int end_stage = 0;       // ring position just after the last armed stage
             uint32_t end_phase = 0;
-            for (int t = pair; t < p.num_tiles; t += npairs) {
+            WorkIter units = units0;
+            WorkUnit u;
+            while (units.next(u)) {
+                const int t = u.tile;
                 int mt, nt;
                 raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
                 const int m0 = mt * PAIR_BM + static_cast<int>(rank) * BLK_M;
                 const int nb = nt * PAIR_BN + static_cast<int>(rank) * HALF_BN;
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     wd.wait(bar_addr(bars, BAR_EMPTY + stage), phase ^ 1u, WAIT_EMPTY, t, kb);
                     if (!wd.aborted) {
                         const uint32_t fb_local = bar_addr(bars, BAR_FULL + stage);
@@ -176,12 +181,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
-            for (int t = pair; t < p.num_tiles; t += npairs) {
+            WorkIter units = units0;
+            WorkUnit u;
+            while (units.next(u)) {
+                const int t = u.tile;
                 wd.wait(bar_addr(bars, BAR_TMEM_EMPTY + acc), acc_phase ^ 1u, WAIT_TMEM_EMPTY,
                         t, -1);
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PAIR_BN);
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     wd.wait(bar_addr(bars, BAR_FULL + stage), phase, WAIT_FULL, t, kb);
                     if (!wd.aborted) {
                         tc_fence_after_sync();
@@ -192,7 +200,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                         for (int kk = 0; kk < BLK_K / MMA_K; ++kk)
                             mma_f16_ss_pair(d_tmem, adesc + static_cast<uint64_t>(kk * 2),
                                             bdesc + static_cast<uint64_t>(kk * 2), idesc,
-                                            (kb == 0 && kk == 0) ? 0u : 1u);
+                                            (kb == u.kb0 && kk == 0) ? 0u : 1u);
                         // frees stage `stage` in both CTAs once these MMAs have read it
                         mma_commit_pair_multicast(bar_addr(bars, BAR_EMPTY + stage), 0x3);
                     }
@@ -217,20 +225,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t sub_count = 0;
-        for (int t = pair; t < p.num_tiles; t += npairs) {
+        WorkIter units = units0;
+        WorkUnit u;
+        volatile uint32_t* ticket_smem =
+            reinterpret_cast<volatile uint32_t*>(sm.gen + L.bars + TICKET_SLOT_OFFSET);
+        while (units.next(u)) {
+            const int t = u.tile;
             int mt, nt;
             raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
             const int m0 = mt * PAIR_BM + static_cast<int>(rank) * BLK_M;
             wd.wait(bar_addr(bars, BAR_TMEM_FULL + acc), acc_phase, WAIT_TMEM_FULL, t, -1);
             tc_fence_after_sync();
-            epilogue_tma_store<PAIR_BN, F16OUT>(tmem_base + static_cast<uint32_t>(acc * PAIR_BN),
-                                                q, lane, issuer, staging, &tmC, m0, nt * PAIR_BN,
-                                                p.N, sub_count, PAIR_EPI_BAR_ID,
-                                                !wd.aborted && m0 < p.M);
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive_cluster(map_shared_rank(bar_addr(bars, BAR_TMEM_EMPTY + acc), 0));
+            const uint32_t tmem_acc = tmem_base + static_cast<uint32_t>(acc * PAIR_BN);
+            const uint32_t empty_leader =
+                map_shared_rank(bar_addr(bars, BAR_TMEM_EMPTY + acc), 0);
+            auto release = [&] {
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(empty_leader);
+            };
+            if (u.ncontrib == 1) {
+                epilogue_tma_store<PAIR_BN, F16OUT>(tmem_acc, q, lane, issuer, staging, &tmC, m0,
+                                                    nt * PAIR_BN, p.N, sub_count,
+                                                    PAIR_EPI_BAR_ID, !wd.aborted && m0 < p.M);
+                release();
+            } else {
+                // each CTA fixes up its own 128 rows of the pair tile
+                const size_t slot_elems = static_cast<size_t>(BLK_M) * PAIR_BN;
+                float* slot0 = p.sk_partials +
+                               (static_cast<size_t>(u.sk_index) * p.sk_max_contrib * 2 + rank) *
+                                   slot_elems;
+                sk_epilogue<PAIR_BN, F16OUT>(tmem_acc, q, lane, issuer, staging, &tmC, m0,
+                                             nt * PAIR_BN, p.M, p.N, sub_count, PAIR_EPI_BAR_ID,
+                                             wd.aborted, slot0, 2 * slot_elems, u.contrib,
+                                             u.ncontrib, p.sk_tickets + u.sk_index * 2 + rank,
+                                             p.epoch, ticket_smem, release);
+            }
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }

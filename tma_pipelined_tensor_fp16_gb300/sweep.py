@@ -2,12 +2,12 @@
 
     python -m tma_pipelined_tensor_fp16_gb300.sweep --config gemm_8192 \
         [--variants persistent,ws_pipelined] [--depths 2,3,4] [--block-n 64,128,256] \
-        [--iters 20] [--out results.jsonl]
+        [--iters 20] [--rounds 1] [--out results.jsonl]
 
 Prints one JSON line per configuration: the plan, the shared memory it needs
-(or why it does not fit), and the median / mean TFLOP/s and GB/s of `iters`
-launches timed with CUDA events on the launch stream after 3 warm-up
-launches.  This is the PIPE_DEPTH-versus-shared-memory trade-off measured on
+(or why it does not fit), and the median / mean TFLOP/s and GB/s of its
+launches, timed with CUDA events on the launch stream: `rounds` passes over
+all configurations, each timing `iters` launches after 3 warm-up launches.  This is the PIPE_DEPTH-versus-shared-memory trade-off measured on
 the device ("GEMM II -- pipelining with TMA", Step 5: deeper rings hide more
 latency; tilus "Multi-Stage Software Pipelining": deeper pipelines force
 smaller tiles).
@@ -30,7 +30,11 @@ def main(argv=None):
                                           "ws_pipelined,persistent")
     ap.add_argument("--depths", default="1,2,3,4,5,6,7,8")
     ap.add_argument("--block-n", default="64,128,256")
+    ap.add_argument("--stream-k", default="auto", help="comma list of auto,off,on")
+    ap.add_argument("--group-m", default="0", help="comma list of raster group heights")
     ap.add_argument("--iters", type=int, default=20)
+    ap.add_argument("--rounds", type=int, default=1,
+                    help="interleaved rounds over all configurations")
     ap.add_argument("--out", default="")
     a = ap.parse_args(argv)
 
@@ -50,43 +54,52 @@ def main(argv=None):
     nbytes = 2.0 * (M * K + N * K) + dC.element_size() * M * N
     stream = torch.cuda.Stream()
     sink = open(a.out, "a") if a.out else None
+    plans = []
     for variant in a.variants.split(","):
         for bn in [int(x) for x in a.block_n.split(",")]:
             depths = [int(x) for x in a.depths.split(",")]
             if variant in ("sync_tiled", "tma_serial"):
                 depths = [1]
-            for d in depths:
-                rec = {"workload": cfg["name"], "variant": variant, "block_n": bn, "depth": d}
+            for d, sk, gm in [(d, sk, gm) for d in depths for sk in a.stream_k.split(",")
+                              for gm in [int(x) for x in a.group_m.split(",")]]:
+                rec = {"workload": cfg["name"], "variant": variant, "block_n": bn, "depth": d,
+                       "stream_k": sk, "group_m": gm}
                 try:
                     plan = binding.Plan(M, N, K, out=cfg["out"], variant=variant, block_n=bn,
-                                        pipe_depth=d)
+                                        pipe_depth=d, stream_k=sk, group_m=gm)
                 except binding.GemmError as e:
                     rec["error"] = str(e)
                     _emit(rec, sink)
                     continue
                 rec["plan"] = plan.describe()
-                args = (dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), stream.cuda_stream)
-                for _ in range(3):
-                    plan.run(*args)
-                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                      for _ in range(a.iters)]
-                torch.cuda.synchronize()
-                for e0, e1 in ev:
-                    e0.record(stream)
-                    plan.run(*args)
-                    e1.record(stream)
-                torch.cuda.synchronize()
-                st = plan.device_status()
-                plan.close()
-                ms = [e0.elapsed_time(e1) for e0, e1 in ev]
-                rec.update({
-                    "status": st,
-                    "ms_median": statistics.median(ms), "ms_min": min(ms),
-                    "tflops_median": flops / (statistics.median(ms) * 1e-3) / 1e12,
-                    "tflops_mean": flops / (statistics.mean(ms) * 1e-3) / 1e12,
-                    "gbs_median": nbytes / (statistics.median(ms) * 1e-3) / 1e9,
-                })
-                _emit(rec, sink)
+                plans.append((rec, plan, []))
+    args = (dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), stream.cuda_stream)
+    # Rounds interleave the configurations so that slow drifts of the clock
+    # (power and temperature) fall on all of them alike.
+    for _ in range(a.rounds):
+        for rec, plan, ms in plans:
+            for _ in range(3):
+                plan.run(*args)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(a.iters)]
+            torch.cuda.synchronize()
+            for e0, e1 in ev:
+                e0.record(stream)
+                plan.run(*args)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            ms.extend(e0.elapsed_time(e1) for e0, e1 in ev)
+    for rec, plan, ms in plans:
+        rec.update({
+            "status": plan.device_status(),
+            "launches": len(ms),
+            "ms_median": statistics.median(ms), "ms_min": min(ms),
+            "tflops_median": flops / (statistics.median(ms) * 1e-3) / 1e12,
+            "tflops_mean": flops / (statistics.mean(ms) * 1e-3) / 1e12,
+            "gbs_median": nbytes / (statistics.median(ms) * 1e-3) / 1e9,
+        })
+        plan.close()
+        _emit(rec, sink)
     if sink:
         sink.close()
 
