@@ -54,7 +54,7 @@ typedef enum {
  * (Steps 3-6) plus the warp-specialised forms. */
 typedef enum {
     GEMM_VAR_AUTO = 0,              /* GEMM_VAR_PERSISTENT_2CTA when M > 128 and there
-                                       are at least (SM count / 2) 256x256 tiles,
+                                       are at least (SM count / 2) 256x128 tiles,
                                        else GEMM_VAR_PERSISTENT */
     GEMM_VAR_SYNC_TILED = 1,        /* Step 3: thread copies, one MMA at a time */
     GEMM_VAR_TMA_SERIAL = 2,        /* Step 4: TMA load + expect_tx, serial loop */
@@ -66,17 +66,19 @@ typedef enum {
     GEMM_VAR_PERSISTENT_LOCKSTEP = 6, /* Step 6 as printed: persistent CTAs running
                                        the lock-step Step-5 loop */
     GEMM_VAR_PERSISTENT_2CTA = 7    /* warp-specialised, persistent, on CTA pairs
-                                       (clusters of 2): 256x256 tiles with
+                                       (clusters of 2): 256 x block_n tiles with
                                        tcgen05.mma.cta_group::2, each CTA loading
-                                       its own half of the operands */
+                                       its own half of the operands; block_n 128,
+                                       192 or 256 (fp16 out), 128, 160, 192, 224 or
+                                       256 (fp32 out), chosen by wave efficiency */
 } gemm_variant;
 
 /* Plan options; a zero field means "choose automatically". */
 typedef struct {
     int variant;        /* gemm_variant */
     int pipe_depth;     /* shared-memory stages, 1..8 (ring variants) */
-    int block_n;        /* output tile width: 64, 128 or 256 (tile height is 128;
-                           the CTA-pair variant uses 256x256 tiles) */
+    int block_n;        /* output tile width: 64, 128 or 256 (tile height 128);
+                           for the CTA-pair variant see GEMM_VAR_PERSISTENT_2CTA */
     int group_m;        /* raster group height in M tiles (default 8) */
     int grid;           /* persistent variants: CTAs to launch (default: SM count) */
     int wait_budget_ms; /* bound on any single in-kernel wait (default 2000) */
@@ -90,6 +92,10 @@ typedef struct {
                            shared evenly by all CTAs (or pairs); partial sums go
                            through a workspace the plan owns and are added in a
                            fixed order, so results do not vary from run to run. */
+    int l2_policy;      /* L2 eviction priority of the operand loads (warp-specialised
+                           variants): 0 = default, 1 = A evict_last and B
+                           evict_first, 2 = A evict_first and B evict_last,
+                           3 = both evict_last */
 } gemm_options;
 
 /* Resolved configuration of a plan (also returned by gemm_select_config). */
@@ -164,6 +170,21 @@ TMAGEMM_API const char* gemm_plan_describe(const gemm_plan* plan);
 
 /* The plan's resolved configuration. */
 TMAGEMM_API int gemm_plan_config(const gemm_plan* plan, gemm_config* out);
+
+/* Record a device timeline of the following runs of `plan` into
+ * `device_buffer` (caller-owned device memory of at least
+ * grid * (units_per_cta + 1) * 10 uint64 words, 8-byte aligned), or stop
+ * recording (NULL).  For each CTA, record 0 is a header {start ns, end ns, SM
+ * id, units processed} and records 1..units_per_cta hold, per work unit, the
+ * globaltimer stamps of its milestones: {tile << 32 | K blocks, first load
+ * issued, last load issued, accumulator free, first MMA issued, last MMA
+ * issued and committed, accumulator complete at the epilogue, last store
+ * issued, ns the MMA issuer waited for loaded stages, ns the producer waited
+ * for free stages}.  These are the prologue / steady-state / drain phases of the stage
+ * ring ("GEMM II -- pipelining with TMA", the pipeline Gantt: TMA and MMA
+ * lanes; "B200 Tma Pipeline Designer", the three-phase timeline).
+ * Warp-specialised variants only; a few stores per unit. */
+TMAGEMM_API int gemm_set_trace(gemm_plan* plan, void* device_buffer, int units_per_cta);
 
 /* ---- host-only helpers (no GPU needed; used by tests and tools) ---- */
 

@@ -97,24 +97,36 @@ def test_headline_configuration(b):
     assert st == 0 and (c.block_m, c.block_n, c.pipe_depth, c.num_tiles) == (128, 256, 4, 2048)
 
 
-@pytest.mark.parametrize("M,N,K,variant", [(256, 256, 256, 5), (4096, 4096, 4096, 7),
-                                           (4000, 3000, 5000, 7), (64, 16384, 16384, 5),
-                                           (128, 65536, 64, 5)])
-def test_auto_variant_choice(b, M, N, K, variant):
-    st, c = b.gemm_select_config(M, N, K, 1)
-    assert st == 0 and c.variant == variant
+@pytest.mark.parametrize("M,N,K,dt,variant,bn", [(256, 256, 256, 0, 5, 64),
+                                                 (4096, 4096, 4096, 1, 7, 256),
+                                                 (8192, 8192, 8192, 1, 7, 256),
+                                                 (4000, 3000, 5000, 0, 7, 224),
+                                                 (64, 16384, 16384, 1, 5, 128),
+                                                 (128, 65536, 64, 1, 5, 256)])
+def test_auto_variant_choice(b, M, N, K, dt, variant, bn):
+    st, c = b.gemm_select_config(M, N, K, dt)
+    assert st == 0 and c.variant == variant and c.block_n == bn
 
 
 def test_pair_variant_constraints(b):
-    st, _ = b.gemm_select_config(1024, 1024, 64, 1, b.make_options(variant="persistent_2cta",
-                                                                    block_n=128))
-    assert st == b.GEMM_ERR_INVALID_ARG
+    for bn, dt, ok in [(128, 1, True), (160, 1, False), (192, 1, True), (224, 1, False),
+                       (160, 0, True), (224, 0, True), (100, 0, False), (64, 0, False)]:
+        st, c = b.gemm_select_config(1024, 1024, 64, dt, b.make_options(variant="persistent_2cta",
+                                                                         block_n=bn))
+        assert (st == 0) == ok, (bn, dt)
+        if ok:
+            assert c.block_n == bn and c.block_m == 256
+            assert c.tx_bytes == 2 * (128 * 64 + (bn // 2) * 64) * 2
+            assert c.tmem_cols >= 2 * bn and c.tmem_cols & (c.tmem_cols - 1) == 0
     st, c = b.gemm_select_config(1024, 1024, 64, 1, b.make_options(variant="persistent_2cta",
                                                                     grid=7))
     assert st == 0 and c.grid == 6  # whole clusters of two
     st, _ = b.gemm_select_config(1024, 1024, 64, 1, b.make_options(variant="persistent_2cta",
-                                                                    pipe_depth=7))
+                                                                    block_n=256, pipe_depth=7))
     assert st == b.GEMM_ERR_UNSUPPORTED
+    st, c = b.gemm_select_config(1024, 1024, 64, 1, b.make_options(variant="persistent_2cta",
+                                                                    block_n=128, pipe_depth=8))
+    assert st == 0  # 24 KB stages: eight fit
 
 
 def test_stage_byte_count_matches_page_formula(b):

@@ -55,6 +55,22 @@ def test_pair_many_tiles_per_cluster(grid):
     assert_close(got, oracle.gemm(A, B), K, "f16", desc)
 
 
+@pytest.mark.parametrize("out,bn", [("f32", 128), ("f32", 160), ("f32", 192), ("f32", 224),
+                                    ("f32", 256), ("f16", 128), ("f16", 192), ("f16", 256)])
+def test_pair_tile_widths(out, bn):
+    # ragged in every dimension, several tiles per pair and a second CTA whose
+    # rows run past M in the last tile row
+    M, N, K = 700, 1000, 456
+    A, B = inputs.make_operands(M, N, K, "normal", 900 + bn)
+    got, guard, desc = run(A, B, out, guard_rows=2, variant=V, block_n=bn, grid=8)
+    assert "x%d" % bn in desc, desc
+    assert_close(got, oracle.gemm(A, B), K, out, desc)
+    assert np.isnan(guard.astype(np.float32)).all()
+    Ai, Bi = inputs.make_operands(M, N, K, "int", 5)
+    goti, _, _ = run(Ai, Bi, out, variant=V, block_n=bn, grid=8)
+    assert_exact(goti, oracle.gemm(Ai, Bi), out, desc)
+
+
 @pytest.mark.parametrize("out", ["f32", "f16"])
 def test_pair_integer_bit_exact(out):
     M, N, K = 520, 392, 1000

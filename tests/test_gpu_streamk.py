@@ -31,9 +31,10 @@ CASES = [
     ("persistent", 390, 776, 456, 5, 128),
     ("persistent", 129, 136, 1000, 4, 64),
     ("persistent", 64, 2048, 4096, 0, 128),      # every tile shared by the full grid
-    ("persistent_2cta", 700, 1000, 520, 10, 0),
-    ("persistent_2cta", 300, 264, 2048, 6, 0),
-    ("persistent_2cta", 1280, 1024, 320, 14, 0),
+    ("persistent_2cta", 700, 1000, 520, 10, 256),
+    ("persistent_2cta", 300, 264, 2048, 6, 256),
+    ("persistent_2cta", 1280, 1024, 320, 14, 256),
+    ("persistent_2cta", 700, 1000, 520, 10, 128),
 ]
 
 
@@ -66,7 +67,7 @@ def test_stream_k_runs_are_bit_identical(variant):
     dA, dB = to_device(A), to_device(B)
     grid = 7 if variant == "persistent" else 4
     plan = pkg.Plan(M, N, K, out="f32", variant=variant, grid=grid, block_n=128 if
-                    variant == "persistent" else 0, stream_k="on")
+                    variant == "persistent" else 256, stream_k="on")
     assert plan.config()["sk_tiles"] > 0
     outs = []
     for _ in range(4):
@@ -84,8 +85,9 @@ def test_stream_k_runs_are_bit_identical(variant):
 def test_stream_k_off_and_on_agree_within_tolerance():
     M, N, K = 4000, 3000, 5000
     A, B = inputs.make_operands(M, N, K, "normal", 3)
-    on, _, d_on = run(A, B, "f32", stream_k="on")
-    off, _, d_off = run(A, B, "f32")
+    # 256-wide pair tiles leave a partial last wave (192 tiles over 76 pairs)
+    on, _, d_on = run(A, B, "f32", stream_k="on", block_n=256)
+    off, _, d_off = run(A, B, "f32", block_n=256)
     assert "stream_k=0/" in d_off and "stream_k=0/" not in d_on
     assert np.max(np.abs(on.astype(np.float64) - off)) <= 1e-3 * np.sqrt(K)
 
@@ -96,7 +98,7 @@ def test_stream_k_workloads_sampled(cfg):
     # the full-size workloads with the stream-K tail switched on
     M, N, K, out = cfg["M"], cfg["N"], cfg["K"], cfg["out"]
     A, B = inputs.make_operands(M, N, K, cfg["dist"], cfg["seed"])
-    got, _, desc = run(A, B, out, stream_k="on")
+    got, _, desc = run(A, B, out, stream_k="on", block_n=256 if M > 128 else 0)
     assert "stream_k=0/" not in desc, desc
     rng = np.random.default_rng(1)
     rows = rng.integers(0, M, 2000)

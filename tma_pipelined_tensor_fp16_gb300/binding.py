@@ -33,7 +33,7 @@ VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 class gemm_options(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("variant", "pipe_depth", "block_n", "group_m", "grid", "wait_budget_ms",
-                 "debug_stall", "stream_k")]
+                 "debug_stall", "stream_k", "l2_policy")]
 
 
 class gemm_config(ctypes.Structure):
@@ -74,6 +74,7 @@ _SIGS = {
     "gemm_sw128_offset": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int64]),
     "gemm_schedule_unit": (ctypes.c_int, [ctypes.POINTER(gemm_config), ctypes.c_int, ctypes.c_int]
                            + [ctypes.POINTER(ctypes.c_int)] * 5),
+    "gemm_set_trace": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]),
     "gemm_run_noalloc": (ctypes.c_int, [ctypes.c_int64] * 3 + [ctypes.c_int] + [ctypes.c_void_p] * 4
                          + [ctypes.POINTER(ctypes.c_int)]),
 }
@@ -112,10 +113,11 @@ STREAM_K = {"auto": 0, "off": 1, "on": 2}
 
 
 def make_options(variant="auto", pipe_depth=0, block_n=0, group_m=0, grid=0, wait_budget_ms=0,
-                 debug_stall=0, stream_k="auto"):
+                 debug_stall=0, stream_k="auto", l2_policy=0):
     v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
     sk = STREAM_K[stream_k] if isinstance(stream_k, str) else int(stream_k)
-    return gemm_options(v, pipe_depth, block_n, group_m, grid, wait_budget_ms, debug_stall, sk)
+    return gemm_options(v, pipe_depth, block_n, group_m, grid, wait_budget_ms, debug_stall, sk,
+                        l2_policy)
 
 
 # ---- the C entry points under their own names ------------------------------
@@ -148,6 +150,10 @@ def gemm_run_noalloc(M, N, K, dtype_out, A_ptr, B_ptr, C_ptr, stream_handle, wan
         return st, ds.value
     st = lib().gemm_run_noalloc(M, N, K, dtype_out, A_ptr, B_ptr, C_ptr, stream_handle, None)
     return st, None
+
+
+def gemm_set_trace(plan, device_ptr, units_per_cta):
+    return lib().gemm_set_trace(plan, device_ptr, units_per_cta)
 
 
 def gemm_get_device_status(plan):
@@ -247,6 +253,9 @@ class Plan:
 
     def device_status(self):
         return gemm_get_device_status(self._h)
+
+    def set_trace(self, device_ptr, units_per_cta):
+        _check(gemm_set_trace(self._h, device_ptr, units_per_cta))
 
     def __call__(self, A, B, C, stream=None):
         """C = A . B^T for torch CUDA tensors (A: M x K fp16, B: N x K fp16,

@@ -98,13 +98,49 @@ int choose_block_n(int variant, int64_t M, int64_t N, int sms)
     return best;
 }
 
-// Default kernel: CTA pairs (256x256 tiles, cta_group::2) when M spans more
-// than one 128-row tile and there are enough pair tiles to occupy every TPC;
+// Pair tile widths the CTA-pair kernel is built for: multiples of 32 for fp32
+// output (32-column store sub-tiles), of 64 for fp16 output.
+bool pair_width_ok(int bn, int dtype)
+{
+    if (dtype == GEMM_OUT_F16) return bn == 128 || bn == 192 || bn == 256;
+    return bn == 128 || bn == 160 || bn == 192 || bn == 224 || bn == 256;
+}
+
+// Pair tile width for an automatic plan: the fraction of launched tile slots
+// that do useful columns (waves over the SM pairs, and the last tile column's
+// overhang past N), weighted by the throughput of one tile of each width
+// relative to 256 columns, measured on GB300 (narrower tiles move more operand
+// bytes from L2 per FLOP, and the main loop is bound by operand arrival).
+int choose_pair_bn(int64_t M, int64_t N, int sms, int dtype)
+{
+    const int widths[5] = {256, 224, 192, 160, 128};
+    const double tile_eff[5] = {1.0, 0.92, 0.79, 0.73, 0.54};
+    const int64_t pairs = sms / 2;
+    const int64_t tm = ceil_div(M, 2 * BLK_M);
+    int best = 256;
+    double best_score = -1.0;
+    for (int i = 0; i < 5; ++i) {
+        const int bn = widths[i];
+        if (!pair_width_ok(bn, dtype)) continue;
+        const int64_t tn = ceil_div(N, bn);
+        const double cols = static_cast<double>(N) / static_cast<double>(tn * bn);
+        const double score = wave_efficiency(tm * tn, static_cast<int>(pairs)) * cols * tile_eff[i];
+        if (score > best_score + 1e-9) {
+            best_score = score;
+            best = bn;
+        }
+    }
+    return best;
+}
+
+// Default kernel: CTA pairs (256-row tiles, cta_group::2) when M spans more
+// than one 128-row tile and there are enough pair tiles (at the narrowest
+// width, 128) to occupy every TPC;
 // otherwise single-CTA persistent tiles, whose narrower widths keep more SMs
 // busy on small or skinny problems.
 int auto_variant(int64_t M, int64_t N, int sms)
 {
-    const int64_t pair_tiles = ceil_div(M, 2 * BLK_M) * ceil_div(N, 256);
+    const int64_t pair_tiles = ceil_div(M, 2 * BLK_M) * ceil_div(N, 128);
     if (M > BLK_M && pair_tiles >= sms / 2) return VAR_PERSISTENT_2CTA;
     return VAR_PERSISTENT;
 }
@@ -132,22 +168,28 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
         return fail(GEMM_ERR_INVALID_ARG, "unknown variant");
     if (opts.pipe_depth < 0 || opts.pipe_depth > MAX_STAGES)
         return fail(GEMM_ERR_INVALID_ARG, "pipe_depth must be 0 (auto) or 1..8");
-    if (opts.block_n != 0 && opts.block_n != 64 && opts.block_n != 128 && opts.block_n != 256)
+    const bool pair_requested = opts.variant == VAR_PERSISTENT_2CTA;
+    if (!pair_requested && opts.block_n != 0 && opts.block_n != 64 && opts.block_n != 128 &&
+        opts.block_n != 256)
         return fail(GEMM_ERR_INVALID_ARG, "block_n must be 0 (auto), 64, 128 or 256");
     if (opts.group_m < 0 || opts.grid < 0 || opts.wait_budget_ms < 0)
         return fail(GEMM_ERR_INVALID_ARG, "group_m, grid and wait_budget_ms must be >= 0");
     if (opts.stream_k < 0 || opts.stream_k > 2)
         return fail(GEMM_ERR_INVALID_ARG, "stream_k must be 0 (auto), 1 (off) or 2 (on)");
+    if (opts.l2_policy < 0 || opts.l2_policy > 3)
+        return fail(GEMM_ERR_INVALID_ARG, "l2_policy must be 0..3");
     if (sms < 1 || smem_optin < 1) return fail(GEMM_ERR_INVALID_ARG, "bad device limits");
 
     const int variant = opts.variant == VAR_AUTO ? auto_variant(M, N, sms) : opts.variant;
     if (opts.debug_stall && !is_ws(variant))
         return fail(GEMM_ERR_INVALID_ARG, "debug_stall needs a warp-specialised variant");
-    if (is_pair(variant) && opts.block_n != 0 && opts.block_n != 256)
-        return fail(GEMM_ERR_INVALID_ARG, "the CTA-pair variant uses 256x256 tiles (block_n 0 or 256)");
-    const int bn = is_pair(variant) ? 256
-                   : opts.block_n   ? opts.block_n
-                                    : choose_block_n(variant, M, N, sms);
+    if (is_pair(variant) && opts.block_n != 0 && !pair_width_ok(opts.block_n, dtype))
+        return fail(GEMM_ERR_INVALID_ARG,
+                    "CTA-pair tile width (block_n) must be 128, 192 or 256 for fp16 output, "
+                    "or 128, 160, 192, 224 or 256 for fp32 output");
+    const int bn = opts.block_n   ? opts.block_n
+                   : is_pair(variant) ? choose_pair_bn(M, N, sms, dtype)
+                                      : choose_block_n(variant, M, N, sms);
     // Shared memory per CTA holds B tiles of `bn_cta` rows: a CTA of a pair
     // keeps half of the pair tile's B rows.
     const int bn_cta = is_pair(variant) ? bn / 2 : bn;
@@ -235,7 +277,12 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     }
     c->threads = is_ws(variant) ? 192 : 128;
     c->smem_bytes = static_cast<int>(smem);
-    c->tmem_cols = (variant == VAR_PERSISTENT || is_pair(variant)) ? 2 * bn : bn;
+    {
+        int cols = (variant == VAR_PERSISTENT || is_pair(variant)) ? 2 * bn : bn;
+        int alloc = 32;
+        while (alloc < cols) alloc <<= 1;
+        c->tmem_cols = alloc;
+    }
     c->tx_bytes = static_cast<int>(is_pair(variant) ? 2 * stage_tx_bytes(bn_cta)
                                                     : stage_tx_bytes(bn));
 
@@ -315,6 +362,7 @@ struct gemm_plan {
     int device;
     unsigned long long budget_ns;
     int debug_stall;
+    int l2_policy;
     DevStatus* d_status;
     int epoch;
     // tensor maps for the last (A, B, C) triple
@@ -324,6 +372,9 @@ struct gemm_plan {
     CUtensorMap tmA, tmB, tmC;
     // stream-K workspace: partial tiles, then the ticket words
     void* d_workspace;
+    // optional timeline buffer (caller-owned device memory)
+    unsigned long long* trace;
+    int trace_units;
     // device buffers of gemm_run_host
     void* hA;
     void* hB;
@@ -383,6 +434,7 @@ gemm_plan* gemm_create_plan_ex(int64_t M, int64_t N, int64_t K, int dtype_out,
     const int budget_ms = (opts && opts->wait_budget_ms) ? opts->wait_budget_ms : 2000;
     p->budget_ns = static_cast<unsigned long long>(budget_ms) * 1000000ull;
     p->debug_stall = opts ? opts->debug_stall : 0;
+    p->l2_policy = opts ? opts->l2_policy : 0;
     e = cudaMalloc(&p->d_status, sizeof(DevStatus));
     if (e == cudaSuccess) e = cudaMemset(p->d_status, 0, sizeof(DevStatus));
     if (e == cudaSuccess && p->cfg.workspace_bytes > 0) {
@@ -454,7 +506,7 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
         plan->mapC_ptr = C;
     }
 
-    LaunchSpec s;
+    LaunchSpec s{};  // every field not set below is zero (trace and stream-K off)
     s.variant = c.variant;
     s.block_n = c.block_n;
     s.f16out = plan->dtype == GEMM_OUT_F16;
@@ -482,10 +534,13 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
     p.epoch = plan->epoch;
     p.budget_ns = plan->budget_ns;
     p.debug_stall = plan->debug_stall;
+    p.l2_policy = plan->l2_policy;
     p.dp_tiles = c.dp_tiles;
     p.sk_tiles = c.sk_tiles;
     p.sk_kb_per_worker = c.sk_kb_per_worker;
     p.sk_max_contrib = c.sk_max_contrib;
+    p.trace = plan->trace;
+    p.trace_units = plan->trace_units;
     if (c.sk_tiles > 0) {
         const int halves = is_pair(c.variant) ? 2 : 1;
         const size_t partial_bytes = static_cast<size_t>(c.sk_tiles) * c.sk_max_contrib * halves *
@@ -584,6 +639,21 @@ int gemm_schedule_tile(const gemm_config* cfg, int64_t tile, int* m_tile, int* n
         return fail(GEMM_ERR_INVALID_ARG, "tile index out of range");
     raster_tile(static_cast<int>(tile), cfg->tiles_m, cfg->tiles_n, cfg->group_m, *m_tile,
                 *n_tile);
+    return ok();
+}
+
+int gemm_set_trace(gemm_plan* plan, void* device_buffer, int units_per_cta)
+{
+    if (!plan) return fail(GEMM_ERR_INVALID_ARG, "plan is NULL");
+    if (device_buffer && units_per_cta < 1)
+        return fail(GEMM_ERR_INVALID_ARG, "units_per_cta must be >= 1");
+    if (device_buffer && (reinterpret_cast<uintptr_t>(device_buffer) & 7u))
+        return fail(GEMM_ERR_INVALID_ARG, "trace buffer must be 8-byte aligned");
+    if (device_buffer && plan->cfg.variant != VAR_PERSISTENT &&
+        plan->cfg.variant != VAR_PERSISTENT_2CTA && plan->cfg.variant != VAR_WS_PIPELINED)
+        return fail(GEMM_ERR_UNSUPPORTED, "the timeline is recorded by the warp-specialised variants");
+    plan->trace = static_cast<unsigned long long*>(device_buffer);
+    plan->trace_units = device_buffer ? units_per_cta : 0;
     return ok();
 }
 
@@ -732,7 +802,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     e = cudaMemsetAsync(scratch, 0, sizeof(DevStatus), stream);
     if (e != cudaSuccess) return cuda_fail("clearing the scratch status record", e);
 
-    LaunchSpec s;
+    LaunchSpec s{};  // every field not set below is zero (trace and stream-K off)
     s.variant = c.variant;
     s.block_n = c.block_n;
     s.f16out = dtype_out == GEMM_OUT_F16;

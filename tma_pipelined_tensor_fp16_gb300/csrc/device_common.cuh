@@ -90,6 +90,30 @@ __device__ __forceinline__ Watchdog make_watchdog(const Params& p)
     return w;
 }
 
+// ----------------------------------------------------------------- timeline
+
+__device__ __forceinline__ uint32_t sm_id()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+    return r;
+}
+
+// Unit `unit` of this CTA, word `word` (no-op when tracing is off or the unit
+// is past the buffer's capacity).
+__device__ __forceinline__ void trace_unit(const Params& p, int unit, int word,
+                                           unsigned long long v)
+{
+    if (p.trace != nullptr && unit < p.trace_units)
+        p.trace[trace_index(static_cast<int>(blockIdx.x), p.trace_units, 1 + unit, word)] = v;
+}
+
+__device__ __forceinline__ void trace_header(const Params& p, int word, unsigned long long v)
+{
+    if (p.trace != nullptr)
+        p.trace[trace_index(static_cast<int>(blockIdx.x), p.trace_units, 0, word)] = v;
+}
+
 // ----------------------------------------------------------------- epilogue
 //
 // "GEMM II -- pipelining with TMA", the TMA-store epilogue: TMEM -> registers

@@ -82,7 +82,39 @@ struct Params {
     int sk_max_contrib;         // most workers that can share one tile
     float* sk_partials;         // [sk_tiles][sk_max_contrib][halves][tile rows x cols] fp32
     unsigned* sk_tickets;       // [sk_tiles][halves] arrival tickets (epoch << 8 | count)
+    // Optional timeline (warp-specialised kernels): per CTA a header record
+    // and `trace_units` unit records of TRACE_WORDS 64-bit words (see
+    // TRACE_* below); nullptr = off.
+    unsigned long long* trace;
+    int trace_units;
+    // L2 eviction priority of the operand loads (warp-specialised kernels):
+    // 0 = default, 1 = A evict_last / B evict_first, 2 = A evict_first /
+    // B evict_last, 3 = both evict_last.
+    int l2_policy;
 };
+
+// Timeline record layout.  Header record of a CTA: TRACE_H_START (after
+// set-up), TRACE_H_END (before teardown), TRACE_H_SMID, TRACE_H_UNITS (units
+// processed).  Unit record: globaltimer stamps (ns) of the unit's milestones.
+constexpr int TRACE_WORDS = 10;
+enum : int {
+    TRACE_H_START = 0, TRACE_H_END = 1, TRACE_H_SMID = 2, TRACE_H_UNITS = 3,
+    TRACE_U_TILE = 0,        // (tile << 32) | number of K blocks
+    TRACE_U_LOAD_FIRST = 1,  // producer: first stage of the unit issued
+    TRACE_U_LOAD_LAST = 2,   // producer: last stage of the unit issued
+    TRACE_U_ACC_FREE = 3,    // MMA issuer: accumulator free for this unit
+    TRACE_U_MMA_FIRST = 4,   // MMA issuer: first stage landed, first MMA issued
+    TRACE_U_MMA_LAST = 5,    // MMA issuer: last MMAs issued and committed
+    TRACE_U_EPI_START = 6,   // epilogue: accumulator complete
+    TRACE_U_EPI_END = 7,     // epilogue: last store of the unit issued
+    TRACE_U_FULL_WAIT = 8,   // MMA issuer: ns spent waiting for loaded stages
+    TRACE_U_EMPTY_WAIT = 9   // producer: ns spent waiting for free stages
+};
+
+TG_HD size_t trace_index(int cta, int trace_units, int record, int word)
+{
+    return (static_cast<size_t>(cta) * (trace_units + 1) + record) * TRACE_WORDS + word;
+}
 
 // One unit of a persistent worker's work: K blocks [kb0, kb1) of one output
 // tile.  sk_index < 0: a whole tile of the data-parallel part; otherwise the

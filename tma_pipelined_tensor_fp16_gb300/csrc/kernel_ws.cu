@@ -106,11 +106,17 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    if (tid == 0) {
+        trace_header(p, TRACE_H_START, globaltimer_ns());
+        trace_header(p, TRACE_H_SMID, sm_id());
+    }
 
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
             const uint32_t tx = stage_tx_bytes(BN);
+            const uint64_t pol_a = (p.l2_policy == 2) ? policy_evict_first() : policy_evict_last();
+            const uint64_t pol_b = (p.l2_policy == 1) ? policy_evict_first() : policy_evict_last();
             if (p.debug_stall) wd.wait(bar_addr(bars, BAR_STALL), 0, WAIT_STALL, -1, -1);
             int stage = 0;
             uint32_t phase = 0;
@@ -119,22 +125,38 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
             uint32_t end_phase = 0;
             WorkIter units = units0;
             WorkUnit u;
+            int ui = 0;
             while (units.next(u)) {
                 const int t = u.tile;
+                trace_unit(p, ui, TRACE_U_TILE,
+                           (static_cast<unsigned long long>(t) << 32) |
+                               static_cast<unsigned>(u.kb1 - u.kb0));
+                unsigned long long empty_wait_ns = 0;
                 int mt, nt;
                 raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
                 const int m0 = mt * BLK_M, n0 = nt * BN;
                 for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     // a fresh barrier passes a wait on parity 1 at once: the
                     // first trip around the ring does not wait
+                    const unsigned long long tw0 = p.trace ? globaltimer_ns() : 0ull;
                     wd.wait(bar_addr(bars, BAR_EMPTY + stage), phase ^ 1u, WAIT_EMPTY, t, kb);
+                    if (p.trace) empty_wait_ns += globaltimer_ns() - tw0;
                     if (!wd.aborted) {
                         const uint32_t fb = bar_addr(bars, BAR_FULL + stage);
                         mbar_arrive_expect_tx(fb, tx);
-                        tma_load_2d(sA + stage * A_TILE_BYTES, &tmA, fb, kb * BLK_K, m0);
-                        tma_load_2d(sB + stage * b_tile_bytes(BN), &tmB, fb, kb * BLK_K, n0);
+                        if (p.l2_policy == 0) {
+                            tma_load_2d(sA + stage * A_TILE_BYTES, &tmA, fb, kb * BLK_K, m0);
+                            tma_load_2d(sB + stage * b_tile_bytes(BN), &tmB, fb, kb * BLK_K, n0);
+                        } else {
+                            tma_load_2d_hint(sA + stage * A_TILE_BYTES, &tmA, fb, kb * BLK_K, m0,
+                                             pol_a);
+                            tma_load_2d_hint(sB + stage * b_tile_bytes(BN), &tmB, fb, kb * BLK_K,
+                                             n0, pol_b);
+                        }
                         ++issued;
                     }
+                    if (kb == u.kb0) trace_unit(p, ui, TRACE_U_LOAD_FIRST, globaltimer_ns());
+                    if (kb == u.kb1 - 1) trace_unit(p, ui, TRACE_U_LOAD_LAST, globaltimer_ns());
                     if (++stage == D) {
                         stage = 0;
                         phase ^= 1u;
@@ -144,6 +166,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
                         end_phase = phase;
                     }
                 }
+                trace_unit(p, ui, TRACE_U_EMPTY_WAIT, empty_wait_ns);
+                ++ui;
             }
             // drain: the last min(D, issued) loads have landed before exit
             if (wd.aborted) {
@@ -169,6 +193,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
+            int mui = 0;
             WorkIter units = units0;
             WorkUnit u;
             while (units.next(u)) {
@@ -177,11 +202,16 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
                 wd.wait(bar_addr(bars, BAR_TMEM_EMPTY + acc), acc_phase ^ 1u, WAIT_TMEM_EMPTY,
                         t, -1);
                 tc_fence_after_sync();
+                trace_unit(p, mui, TRACE_U_ACC_FREE, globaltimer_ns());
+                unsigned long long full_wait_ns = 0;
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = u.kb0; kb < u.kb1; ++kb) {
+                    const unsigned long long tw0 = p.trace ? globaltimer_ns() : 0ull;
                     wd.wait(bar_addr(bars, BAR_FULL + stage), phase, WAIT_FULL, t, kb);
+                    if (p.trace) full_wait_ns += globaltimer_ns() - tw0;
                     if (!wd.aborted) {
                         tc_fence_after_sync();
+                        if (kb == u.kb0) trace_unit(p, mui, TRACE_U_MMA_FIRST, globaltimer_ns());
                         const uint64_t adesc = sw128_kmajor_desc(sA + stage * A_TILE_BYTES);
                         const uint64_t bdesc = sw128_kmajor_desc(sB + stage * b_tile_bytes(BN));
 #pragma unroll
@@ -198,6 +228,9 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
                     }
                 }
                 if (!wd.aborted) mma_commit(bar_addr(bars, BAR_TMEM_FULL + acc));
+                trace_unit(p, mui, TRACE_U_MMA_LAST, globaltimer_ns());
+                trace_unit(p, mui, TRACE_U_FULL_WAIT, full_wait_ns);
+                ++mui;
                 if (ACC == 2) {
                     acc ^= 1;
                     if (acc == 0) acc_phase ^= 1u;
@@ -221,12 +254,14 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
         WorkUnit u;
         volatile uint32_t* ticket_smem =
             reinterpret_cast<volatile uint32_t*>(sm.gen + L.bars + TICKET_SLOT_OFFSET);
+        int eui = 0;
         while (units.next(u)) {
             const int t = u.tile;
             int mt, nt;
             raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
             wd.wait(bar_addr(bars, BAR_TMEM_FULL + acc), acc_phase, WAIT_TMEM_FULL, t, -1);
             tc_fence_after_sync();
+            if (issuer) trace_unit(p, eui, TRACE_U_EPI_START, globaltimer_ns());
             const uint32_t tmem_acc = tmem_base + static_cast<uint32_t>(acc * BN);
             const uint32_t empty_bar = bar_addr(bars, BAR_TMEM_EMPTY + acc);
             if (u.ncontrib == 1) {
@@ -247,6 +282,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
                                             mbar_arrive(empty_bar);
                                         });
             }
+            if (issuer) trace_unit(p, eui, TRACE_U_EPI_END, globaltimer_ns());
+            ++eui;
             if (ACC == 2) {
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
@@ -255,10 +292,12 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
             }
         }
         if (issuer) bulk_wait_group<0>();
+        if (issuer) trace_header(p, TRACE_H_UNITS, static_cast<unsigned long long>(eui));
     }
 
     tc_fence_before_sync();
     __syncthreads();
+    if (tid == 0) trace_header(p, TRACE_H_END, globaltimer_ns());
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, TMEM_COLS);

@@ -51,17 +51,28 @@ __device__ __forceinline__ uint32_t bar_addr(uint32_t bars, int slot)
 
 constexpr int PAIR_THREADS = 192;
 constexpr int PAIR_BM = 2 * BLK_M;   // 256 output rows per pair tile
-constexpr int PAIR_BN = 256;         // output columns per pair tile
-constexpr int HALF_BN = PAIR_BN / 2; // B rows held by each CTA
 constexpr uint32_t PAIR_EPI_BAR_ID = 1;
 
-template <bool F16OUT>
+__host__ __device__ constexpr uint32_t pow2_at_least(uint32_t x)
+{
+    uint32_t r = 32;
+    while (r < x) r <<= 1;
+    return r;
+}
+
+// PAIR_BN: output columns per pair tile (a multiple of 32 up to 256; each CTA
+// holds PAIR_BN / 2 rows of B per stage).
+template <int PAIR_BN, bool F16OUT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
     k_ws2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
           const __grid_constant__ CUtensorMap tmC, const Params p)
 {
+    static_assert(PAIR_BN % 32 == 0 && PAIR_BN >= 64 && PAIR_BN <= 256, "pair tile width");
+    static_assert(!F16OUT || PAIR_BN % 64 == 0, "fp16 output stores 64-column sub-tiles");
+    constexpr int HALF_BN = PAIR_BN / 2;  // B rows held by each CTA
     constexpr int ACC = 2;
-    constexpr uint32_t TMEM_COLS = ACC * PAIR_BN;  // 512: the whole TMEM of each SM
+    // two accumulators of PAIR_BN columns, rounded up to a legal allocation
+    constexpr uint32_t TMEM_COLS = pow2_at_least(ACC * PAIR_BN);
     const int D = p.pipe_depth;
     const CtaSmem sm = cta_smem();
     const SmemLayout L = smem_layout(D, HALF_BN, NUM_STAGING);
@@ -107,11 +118,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
     cluster_sync_all();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    if (tid == 0) {
+        trace_header(p, TRACE_H_START, globaltimer_ns());
+        trace_header(p, TRACE_H_SMID, sm_id());
+    }
 
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
             const uint32_t pair_tx = 2u * stage_tx_bytes(HALF_BN);  // both CTAs' A and B
+            const uint64_t pol_a = (p.l2_policy == 2) ? policy_evict_first() : policy_evict_last();
+            const uint64_t pol_b = (p.l2_policy == 1) ? policy_evict_first() : policy_evict_last();
             if (p.debug_stall) wd.wait(bar_addr(bars, BAR_STALL), 0, WAIT_STALL, -1, -1);
             int stage = 0;
             uint32_t phase = 0;
@@ -120,14 +137,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
             uint32_t end_phase = 0;
             WorkIter units = units0;
             WorkUnit u;
+            int ui = 0;
             while (units.next(u)) {
                 const int t = u.tile;
+                trace_unit(p, ui, TRACE_U_TILE,
+                           (static_cast<unsigned long long>(t) << 32) |
+                               static_cast<unsigned>(u.kb1 - u.kb0));
+                unsigned long long empty_wait_ns = 0;
                 int mt, nt;
                 raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
                 const int m0 = mt * PAIR_BM + static_cast<int>(rank) * BLK_M;
                 const int nb = nt * PAIR_BN + static_cast<int>(rank) * HALF_BN;
                 for (int kb = u.kb0; kb < u.kb1; ++kb) {
+                    const unsigned long long tw0 = p.trace ? globaltimer_ns() : 0ull;
                     wd.wait(bar_addr(bars, BAR_EMPTY + stage), phase ^ 1u, WAIT_EMPTY, t, kb);
+                    if (p.trace) empty_wait_ns += globaltimer_ns() - tw0;
                     if (!wd.aborted) {
                         const uint32_t fb_local = bar_addr(bars, BAR_FULL + stage);
                         const uint32_t fb_leader = map_shared_rank(fb_local, 0);
@@ -135,10 +159,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                             mbar_arrive_expect_tx(fb_local, pair_tx);
                             ++armed;
                         }
-                        tma_load_2d_pair(sA + stage * A_TILE_BYTES, &tmA, fb_leader, kb * BLK_K, m0);
-                        tma_load_2d_pair(sB + stage * b_tile_bytes(HALF_BN), &tmB, fb_leader,
-                                         kb * BLK_K, nb);
+                        if (p.l2_policy == 0) {
+                            tma_load_2d_pair(sA + stage * A_TILE_BYTES, &tmA, fb_leader,
+                                             kb * BLK_K, m0);
+                            tma_load_2d_pair(sB + stage * b_tile_bytes(HALF_BN), &tmB, fb_leader,
+                                             kb * BLK_K, nb);
+                        } else {
+                            tma_load_2d_pair_hint(sA + stage * A_TILE_BYTES, &tmA, fb_leader,
+                                                  kb * BLK_K, m0, pol_a);
+                            tma_load_2d_pair_hint(sB + stage * b_tile_bytes(HALF_BN), &tmB,
+                                                  fb_leader, kb * BLK_K, nb, pol_b);
+                        }
                     }
+                    if (kb == u.kb0) trace_unit(p, ui, TRACE_U_LOAD_FIRST, globaltimer_ns());
+                    if (kb == u.kb1 - 1) trace_unit(p, ui, TRACE_U_LOAD_LAST, globaltimer_ns());
                     if (++stage == D) {
                         stage = 0;
                         phase ^= 1u;
@@ -148,6 +182,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                         end_phase = phase;
                     }
                 }
+                trace_unit(p, ui, TRACE_U_EMPTY_WAIT, empty_wait_ns);
+                ++ui;
             }
             if (wd.aborted) {
                 // Let copies already in flight land before the CTA can exit:
@@ -181,6 +217,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
+            int mui = 0;
             WorkIter units = units0;
             WorkUnit u;
             while (units.next(u)) {
@@ -188,11 +225,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                 wd.wait(bar_addr(bars, BAR_TMEM_EMPTY + acc), acc_phase ^ 1u, WAIT_TMEM_EMPTY,
                         t, -1);
                 tc_fence_after_sync();
+                trace_unit(p, mui, TRACE_U_ACC_FREE, globaltimer_ns());
+                unsigned long long full_wait_ns = 0;
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PAIR_BN);
                 for (int kb = u.kb0; kb < u.kb1; ++kb) {
+                    const unsigned long long tw0 = p.trace ? globaltimer_ns() : 0ull;
                     wd.wait(bar_addr(bars, BAR_FULL + stage), phase, WAIT_FULL, t, kb);
+                    if (p.trace) full_wait_ns += globaltimer_ns() - tw0;
                     if (!wd.aborted) {
                         tc_fence_after_sync();
+                        if (kb == u.kb0) trace_unit(p, mui, TRACE_U_MMA_FIRST, globaltimer_ns());
                         const uint64_t adesc = sw128_kmajor_desc(sA + stage * A_TILE_BYTES);
                         const uint64_t bdesc =
                             sw128_kmajor_desc(sB + stage * b_tile_bytes(HALF_BN));
@@ -210,6 +252,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                     }
                 }
                 if (!wd.aborted) mma_commit_pair_multicast(bar_addr(bars, BAR_TMEM_FULL + acc), 0x3);
+                trace_unit(p, mui, TRACE_U_MMA_LAST, globaltimer_ns());
+                trace_unit(p, mui, TRACE_U_FULL_WAIT, full_wait_ns);
+                ++mui;
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
@@ -229,6 +274,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
         WorkUnit u;
         volatile uint32_t* ticket_smem =
             reinterpret_cast<volatile uint32_t*>(sm.gen + L.bars + TICKET_SLOT_OFFSET);
+        int eui = 0;
         while (units.next(u)) {
             const int t = u.tile;
             int mt, nt;
@@ -236,6 +282,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
             const int m0 = mt * PAIR_BM + static_cast<int>(rank) * BLK_M;
             wd.wait(bar_addr(bars, BAR_TMEM_FULL + acc), acc_phase, WAIT_TMEM_FULL, t, -1);
             tc_fence_after_sync();
+            if (issuer) trace_unit(p, eui, TRACE_U_EPI_START, globaltimer_ns());
             const uint32_t tmem_acc = tmem_base + static_cast<uint32_t>(acc * PAIR_BN);
             const uint32_t empty_leader =
                 map_shared_rank(bar_addr(bars, BAR_TMEM_EMPTY + acc), 0);
@@ -261,16 +308,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                                              u.ncontrib, p.sk_tickets + u.sk_index * 2 + rank,
                                              p.epoch, ticket_smem, release);
             }
+            if (issuer) trace_unit(p, eui, TRACE_U_EPI_END, globaltimer_ns());
+            ++eui;
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
         if (issuer) bulk_wait_group<0>();
+        if (issuer) trace_header(p, TRACE_H_UNITS, static_cast<unsigned long long>(eui));
         __syncwarp();
     }
 
     // nothing of either CTA is touched remotely after this point
     tc_fence_before_sync();
     cluster_sync_all();
+    if (tid == 0) trace_header(p, TRACE_H_END, globaltimer_ns());
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc_pair(tmem_base, TMEM_COLS);
@@ -293,10 +344,23 @@ cudaError_t launch_pair_kernel(KernelT kernel, const LaunchSpec& s, cudaStream_t
 
 cudaError_t launch_pair(const LaunchSpec& s, cudaStream_t stream)
 {
-    if (s.variant != VAR_PERSISTENT_2CTA || s.block_n != PAIR_BN || (s.grid & 1))
-        return cudaErrorInvalidValue;
-    return s.f16out ? launch_pair_kernel(k_ws2<true>, s, stream)
-                    : launch_pair_kernel(k_ws2<false>, s, stream);
+    if (s.variant != VAR_PERSISTENT_2CTA || (s.grid & 1)) return cudaErrorInvalidValue;
+    if (s.f16out) {
+        switch (s.block_n) {
+        case 128: return launch_pair_kernel(k_ws2<128, true>, s, stream);
+        case 192: return launch_pair_kernel(k_ws2<192, true>, s, stream);
+        case 256: return launch_pair_kernel(k_ws2<256, true>, s, stream);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (s.block_n) {
+    case 128: return launch_pair_kernel(k_ws2<128, false>, s, stream);
+    case 160: return launch_pair_kernel(k_ws2<160, false>, s, stream);
+    case 192: return launch_pair_kernel(k_ws2<192, false>, s, stream);
+    case 224: return launch_pair_kernel(k_ws2<224, false>, s, stream);
+    case 256: return launch_pair_kernel(k_ws2<256, false>, s, stream);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace tg

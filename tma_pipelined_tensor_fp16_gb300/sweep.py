@@ -32,7 +32,10 @@ def main(argv=None):
     ap.add_argument("--block-n", default="64,128,256")
     ap.add_argument("--stream-k", default="auto", help="comma list of auto,off,on")
     ap.add_argument("--group-m", default="0", help="comma list of raster group heights")
+    ap.add_argument("--l2-policy", default="0", help="comma list of L2 load policies 0..3")
     ap.add_argument("--iters", type=int, default=20)
+    ap.add_argument("--cooldown", type=float, default=0.0,
+                    help="seconds of idle GPU before each configuration's timing")
     ap.add_argument("--rounds", type=int, default=1,
                     help="interleaved rounds over all configurations")
     ap.add_argument("--out", default="")
@@ -60,13 +63,14 @@ def main(argv=None):
             depths = [int(x) for x in a.depths.split(",")]
             if variant in ("sync_tiled", "tma_serial"):
                 depths = [1]
-            for d, sk, gm in [(d, sk, gm) for d in depths for sk in a.stream_k.split(",")
-                              for gm in [int(x) for x in a.group_m.split(",")]]:
+            for d, sk, gm, l2 in [(d, sk, gm, l2) for d in depths for sk in a.stream_k.split(",")
+                                  for gm in [int(x) for x in a.group_m.split(",")]
+                                  for l2 in [int(x) for x in a.l2_policy.split(",")]]:
                 rec = {"workload": cfg["name"], "variant": variant, "block_n": bn, "depth": d,
-                       "stream_k": sk, "group_m": gm}
+                       "stream_k": sk, "group_m": gm, "l2_policy": l2}
                 try:
                     plan = binding.Plan(M, N, K, out=cfg["out"], variant=variant, block_n=bn,
-                                        pipe_depth=d, stream_k=sk, group_m=gm)
+                                        pipe_depth=d, stream_k=sk, group_m=gm, l2_policy=l2)
                 except binding.GemmError as e:
                     rec["error"] = str(e)
                     _emit(rec, sink)
@@ -78,6 +82,10 @@ def main(argv=None):
     # (power and temperature) fall on all of them alike.
     for _ in range(a.rounds):
         for rec, plan, ms in plans:
+            if a.cooldown > 0:
+                import time
+                torch.cuda.synchronize()
+                time.sleep(a.cooldown)
             for _ in range(3):
                 plan.run(*args)
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
