@@ -96,6 +96,12 @@ typedef struct {
                            variants): 0 = default, 1 = A evict_last and B
                            evict_first, 2 = A evict_first and B evict_last,
                            3 = both evict_last */
+    int k_order;        /* persistent warp-specialised variants: 0 = auto (snake),
+                           1 = every tile walks K upwards, 2 = "snake": a CTA walks K
+                           downwards on every other tile, so each tile starts on
+                           the A slices its predecessor (the previous wave of
+                           the same raster group) used last and that are still
+                           in L2 */
 } gemm_options;
 
 /* Resolved configuration of a plan (also returned by gemm_select_config). */
@@ -145,9 +151,14 @@ TMAGEMM_API int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C,
 
 /* End-to-end variant of gemm_run for HOST buffers: copies A and B to device
  * buffers owned by the plan (allocated on first use, reused after), runs the
- * GEMM on `cuda_stream`, copies C back and synchronises the stream.  A, B, C
- * are host pointers (page-locked memory gives full copy bandwidth).  Returns
- * GEMM_ERR_TIMEOUT if the kernel's watchdog fired. */
+ * GEMM, copies C back and synchronises `cuda_stream`.  A, B, C are host
+ * pointers.  When all three are page-locked and M >= 2048, the round trip is
+ * pipelined in bands of rows: B and then A band by band go in on a copy
+ * stream, each band's GEMM runs on `cuda_stream` (through a sub-plan per band)
+ * as soon as its rows of A have landed, and each band of C comes back on a
+ * second copy stream while later bands compute; otherwise the copies and the
+ * GEMM run one after the other on `cuda_stream`.  Returns GEMM_ERR_TIMEOUT if
+ * a kernel's watchdog fired. */
 TMAGEMM_API int gemm_run_host(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_stream);
 
 /* Read (and clear) the plan's device status record.  Call after

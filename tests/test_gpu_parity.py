@@ -121,6 +121,44 @@ def test_run_host_entry_point():
     plan.close()
 
 
+@pytest.mark.parametrize("out", ["f32", "f16"])
+@pytest.mark.parametrize("variant", ["auto", "persistent"])
+def test_run_host_banded_pipeline(out, variant):
+    # M >= 2048 with page-locked buffers: B, then A band by band, band GEMMs
+    # as rows arrive, C bands copied back while later bands compute; the last
+    # band is shorter than the others
+    import torch
+
+    import tma_pipelined_tensor_fp16_gb300 as pkg
+    M, N, K = 2304, 520, 264
+    A, B = inputs.make_operands(M, N, K, "uniform", 14)
+    hA = torch.from_numpy(A.view(np.float16)).pin_memory()
+    hB = torch.from_numpy(B.view(np.float16)).pin_memory()
+    dt = torch.float16 if out == "f16" else torch.float32
+    hC = torch.full((M, N), float("nan"), dtype=dt).pin_memory()
+    plan = pkg.Plan(M, N, K, out=out, variant=variant)
+    ref = oracle.gemm(A, B)
+    s = torch.cuda.Stream()
+    for _ in range(2):
+        plan.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), s.cuda_stream)
+        got = hC.numpy().astype(np.float64)
+        assert np.isfinite(got).all()
+        assert_close(got, ref, K, out, "banded run_host")
+        hC.fill_(float("nan"))
+    plan.close()
+
+
+def test_run_host_pageable_buffers():
+    import tma_pipelined_tensor_fp16_gb300 as pkg
+    M, N, K = 2304, 264, 128
+    A, B = inputs.make_operands(M, N, K, "normal", 15)
+    C = np.zeros((M, N), dtype=np.float32)
+    plan = pkg.Plan(M, N, K, out="f32")
+    plan.run_host(A.ctypes.data, B.ctypes.data, C.ctypes.data, 0)
+    assert_close(C, oracle.gemm(A, B), K, "f32", "pageable run_host")
+    plan.close()
+
+
 def test_argument_errors_are_reported():
     import torch
 

@@ -91,7 +91,19 @@ struct Params {
     // 0 = default, 1 = A evict_last / B evict_first, 2 = A evict_first /
     // B evict_last, 3 = both evict_last.
     int l2_policy;
+    // 1: a persistent worker walks the K blocks of its odd-numbered units
+    // backwards, so a unit starts on the operand slices its predecessor (the
+    // previous wave, which shares the A rows within a raster group) touched
+    // last and that are still in L2.  0: always ascending.
+    int k_snake;
 };
+
+// The i-th K block (i = 0, 1, ...) processed for work unit number `unit` of a
+// worker, for a unit covering blocks [kb0, kb1).
+TG_HD int kblock_at(int i, int unit, int kb0, int kb1, int k_snake)
+{
+    return (k_snake && (unit & 1)) ? kb1 - 1 - i : kb0 + i;
+}
 
 // Timeline record layout.  Header record of a CTA: TRACE_H_START (after
 // set-up), TRACE_H_END (before teardown), TRACE_H_SMID, TRACE_H_UNITS (units

@@ -148,7 +148,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                 raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
                 const int m0 = mt * PAIR_BM + static_cast<int>(rank) * BLK_M;
                 const int nb = nt * PAIR_BN + static_cast<int>(rank) * HALF_BN;
-                for (int kb = u.kb0; kb < u.kb1; ++kb) {
+                for (int ki = 0; ki < u.kb1 - u.kb0; ++ki) {
+                    const int kb = kblock_at(ki, ui, u.kb0, u.kb1, p.k_snake);
                     const unsigned long long tw0 = p.trace ? globaltimer_ns() : 0ull;
                     wd.wait(bar_addr(bars, BAR_EMPTY + stage), phase ^ 1u, WAIT_EMPTY, t, kb);
                     if (p.trace) empty_wait_ns += globaltimer_ns() - tw0;
@@ -171,8 +172,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                                                   fb_leader, kb * BLK_K, nb, pol_b);
                         }
                     }
-                    if (kb == u.kb0) trace_unit(p, ui, TRACE_U_LOAD_FIRST, globaltimer_ns());
-                    if (kb == u.kb1 - 1) trace_unit(p, ui, TRACE_U_LOAD_LAST, globaltimer_ns());
+                    if (ki == 0) trace_unit(p, ui, TRACE_U_LOAD_FIRST, globaltimer_ns());
+                    if (ki == u.kb1 - u.kb0 - 1)
+                        trace_unit(p, ui, TRACE_U_LOAD_LAST, globaltimer_ns());
                     if (++stage == D) {
                         stage = 0;
                         phase ^= 1u;
@@ -228,13 +230,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                 trace_unit(p, mui, TRACE_U_ACC_FREE, globaltimer_ns());
                 unsigned long long full_wait_ns = 0;
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PAIR_BN);
-                for (int kb = u.kb0; kb < u.kb1; ++kb) {
+                for (int ki = 0; ki < u.kb1 - u.kb0; ++ki) {
+                    const int kb = kblock_at(ki, mui, u.kb0, u.kb1, p.k_snake);
                     const unsigned long long tw0 = p.trace ? globaltimer_ns() : 0ull;
                     wd.wait(bar_addr(bars, BAR_FULL + stage), phase, WAIT_FULL, t, kb);
                     if (p.trace) full_wait_ns += globaltimer_ns() - tw0;
                     if (!wd.aborted) {
                         tc_fence_after_sync();
-                        if (kb == u.kb0) trace_unit(p, mui, TRACE_U_MMA_FIRST, globaltimer_ns());
+                        if (ki == 0) trace_unit(p, mui, TRACE_U_MMA_FIRST, globaltimer_ns());
                         const uint64_t adesc = sw128_kmajor_desc(sA + stage * A_TILE_BYTES);
                         const uint64_t bdesc =
                             sw128_kmajor_desc(sB + stage * b_tile_bytes(HALF_BN));
@@ -242,7 +245,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                         for (int kk = 0; kk < BLK_K / MMA_K; ++kk)
                             mma_f16_ss_pair(d_tmem, adesc + static_cast<uint64_t>(kk * 2),
                                             bdesc + static_cast<uint64_t>(kk * 2), idesc,
-                                            (kb == u.kb0 && kk == 0) ? 0u : 1u);
+                                            (ki == 0 && kk == 0) ? 0u : 1u);
                         // frees stage `stage` in both CTAs once these MMAs have read it
                         mma_commit_pair_multicast(bar_addr(bars, BAR_EMPTY + stage), 0x3);
                     }
