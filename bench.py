@@ -232,6 +232,29 @@ def run_reference(args, cfg, rank):
 METRIC = "fp16 GEMM TFLOP/s at 8192^3 (1 GB300) and % of dense fp16 tensor peak"
 
 
+# ------------------------------------------------------------- several ranks
+#
+# Under torchrun every rank runs the same GEMM on its own GPU (the GEMM needs
+# no exchange: output tiles are independent, so N GPUs are N replicas --
+# weak scaling).  The only collectives are a barrier around the timed region
+# and the maximum of the ranks' times.
+
+def max_over_ranks(value, dist, device):
+    """The largest `value` over all ranks (the value itself without a process group)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, work_per_step, steps, max_ms, scale=1e12):
+    """Aggregate rate of `world` replicas that each did `steps` steps of
+    `work_per_step` units, timed by the slowest rank (`max_ms`)."""
+    return world * work_per_step * steps / (max_ms * 1e-3) / scale
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -321,14 +344,11 @@ def main():
         raise SystemExit("timed run failed: " + pkg.gemm_last_error())
     total_ms = t_start.elapsed_time(t_end)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
-    if dist is not None:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, "cuda")
 
     flops, nbytes = algorithmic(cfg)
     ms_per_step = total_ms / args.steps
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_rate(world, flops, args.steps, total_ms)
     avg_launch_s = statistics.mean(launch_ms) * 1e-3
 
     # --------------------------------------------------- end to end, host buffers
@@ -349,12 +369,8 @@ def main():
             plan.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), sh)
         e1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1)
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, "cuda")
+        e2e = {"value": whole_job_rate(world, flops, e2e_steps, e2e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(A.nbytes + B.nbytes),
                "d2h_bytes_per_step": int(hC.numel() * hC.element_size()),
                "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
