@@ -121,6 +121,9 @@ typedef struct {
     int sk_kb_per_worker; /* K blocks of the stream-K part per CTA / pair */
     int sk_max_contrib; /* most CTAs / pairs that share one stream-K tile */
     long long workspace_bytes; /* device workspace the plan allocates for stream-K */
+    int a_rows;         /* rows of A per stage: 128, or 64 when M <= 64 (single-CTA
+                           warp-specialised variants; the MMA still computes 128
+                           rows and rows past M are never stored) */
 } gemm_config;
 
 /* Create a plan for C[M x N] = A[M x K] . B[N x K]^T on the current CUDA

@@ -256,3 +256,13 @@ def test_stream_k_choice(b):
     assert c.grid == 152 and c.sk_tiles == c.num_tiles == 128 and c.dp_tiles == 0
     st, c = b.gemm_select_config(64, 16384, 16384, 1)
     assert c.grid == 128 and c.sk_tiles == 0
+
+
+def test_half_height_a_slots_for_at_most_64_rows(b):
+    st, c = b.gemm_select_config(64, 16384, 16384, 1)
+    assert st == 0 and c.a_rows == 64 and c.pipe_depth == 8
+    assert c.tx_bytes == (64 * 64 + c.block_n * 64) * 2
+    st, c = b.gemm_select_config(65, 16384, 16384, 1, b.make_options(variant="persistent"))
+    assert c.a_rows == 128
+    st, c = b.gemm_select_config(64, 1024, 1024, 1, b.make_options(variant="pipelined"))
+    assert c.a_rows == 128  # lock-step kernels keep full-height slots

@@ -81,6 +81,21 @@ def test_every_tile_width(variant, block_n, out):
     assert_close(got, oracle.gemm(A, B), K, out, desc)
 
 
+@pytest.mark.parametrize("variant", ["persistent", "ws_pipelined"])
+@pytest.mark.parametrize("M", [1, 17, 64])
+@pytest.mark.parametrize("depth", [1, 4, 8])
+def test_at_most_64_rows_use_half_height_a_slots(variant, M, depth):
+    # 64-row A stages: the MMA's rows 64..127 read whatever follows the slot
+    # and must never reach C (the NaN guard band would show it)
+    for out in ("f32", "f16"):
+        for N, K in ((8, 8), (520, 1000)):
+            A, B = inputs.make_operands(M, N, K, "normal", 70 + M + depth)
+            got, guard, desc = run(A, B, out, guard_rows=80, variant=variant, pipe_depth=depth,
+                                   block_n=128)
+            assert_close(got, oracle.gemm(A, B), K, out, desc)
+            assert np.isnan(guard.astype(np.float32)).all(), "wrote past row M"
+
+
 @pytest.mark.parametrize("group_m", [1, 3, 8])
 @pytest.mark.parametrize("grid", [1, 7, 0])
 def test_persistent_schedules(group_m, grid):

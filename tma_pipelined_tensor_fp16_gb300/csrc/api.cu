@@ -198,6 +198,9 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     const int bn_cta = is_pair(variant) ? bn / 2 : bn;
     const int bm = is_pair(variant) ? 2 * BLK_M : BLK_M;
     const int staging = variant == VAR_SYNC_TILED ? 0 : NUM_STAGING;
+    // A problem of at most 64 rows keeps 64-row A slots (more stages fit).
+    const int a_rows = (M <= 64 && (variant == VAR_PERSISTENT || variant == VAR_WS_PIPELINED))
+                           ? 64 : BLK_M;
 
     int depth;
     if (!has_ring(variant)) {
@@ -206,7 +209,7 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
         depth = 1;
     } else if (opts.pipe_depth) {
         depth = opts.pipe_depth;
-        const uint32_t need = smem_layout(depth, bn_cta, staging).total;
+        const uint32_t need = smem_layout(depth, bn_cta, staging, a_rows).total;
         if (need > static_cast<uint32_t>(smem_optin)) {
             char buf[200];
             std::snprintf(buf, sizeof(buf),
@@ -217,7 +220,7 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     } else {
         depth = 0;
         for (int d = MAX_STAGES; d >= 1; --d)
-            if (smem_layout(d, bn_cta, staging).total <= static_cast<uint32_t>(smem_optin)) {
+            if (smem_layout(d, bn_cta, staging, a_rows).total <= static_cast<uint32_t>(smem_optin)) {
                 depth = d;
                 break;
             }
@@ -227,7 +230,7 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     const int64_t tm = ceil_div(M, bm), tn = ceil_div(N, bn);
     const int64_t tiles = tm * tn;
     if (tiles > LIM) return fail(GEMM_ERR_UNSUPPORTED, "too many output tiles");
-    uint32_t smem = smem_layout(depth, bn_cta, staging).total;
+    uint32_t smem = smem_layout(depth, bn_cta, staging, a_rows).total;
     if (is_persistent(variant)) {
         // One resident CTA per SM: ask for more than half of the SM's shared
         // memory so that a second CTA can never be co-scheduled.
@@ -287,7 +290,8 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
         c->tmem_cols = alloc;
     }
     c->tx_bytes = static_cast<int>(is_pair(variant) ? 2 * stage_tx_bytes(bn_cta)
-                                                    : stage_tx_bytes(bn));
+                                                    : stage_tx_bytes(bn, a_rows));
+    c->a_rows = a_rows;
 
     // Stream-K tail: whole waves stay data-parallel; the tiles of a partial
     // last wave are cut into equal K-block ranges, one per worker.
@@ -501,7 +505,7 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
     const gemm_config& c = plan->cfg;
     if (A != plan->mapA_ptr || B != plan->mapB_ptr || C != plan->mapC_ptr) {
         int r = encode_2d(&plan->tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, plan->K, plan->M,
-                          plan->K * 2, BLK_K, BLK_M, "A");
+                          plan->K * 2, BLK_K, static_cast<uint32_t>(c.a_rows), "A");
         if (r == GEMM_OK)
             r = encode_2d(&plan->tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, plan->K, plan->N,
                           plan->K * 2, BLK_K, is_pair(c.variant) ? c.block_n / 2 : c.block_n,
@@ -553,6 +557,7 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
     p.debug_stall = plan->debug_stall;
     p.l2_policy = plan->l2_policy;
     p.k_snake = plan->k_snake;
+    p.a_rows = c.a_rows;
     p.dp_tiles = c.dp_tiles;
     p.sk_tiles = c.sk_tiles;
     p.sk_kb_per_worker = c.sk_kb_per_worker;
@@ -933,7 +938,8 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     if (r != GEMM_OK) return r;
 
     CUtensorMap tmA, tmB, tmC;
-    r = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, K * 2, BLK_K, BLK_M, "A");
+    r = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, K * 2, BLK_K,
+                  static_cast<uint32_t>(c.a_rows), "A");
     if (r == GEMM_OK)
         r = encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, K * 2, BLK_K, c.block_n,
                       "B");
@@ -987,6 +993,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     p.sk_max_contrib = 0;
     p.sk_partials = nullptr;
     p.sk_tickets = nullptr;
+    p.a_rows = c.a_rows;
     e = launch_ws(s, stream);
     if (e != cudaSuccess) return cuda_fail("kernel launch", e);
 

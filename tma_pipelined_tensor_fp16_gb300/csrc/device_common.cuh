@@ -272,7 +272,10 @@ __device__ __forceinline__ void sk_write_partial(uint32_t tmem_acc, int q, uint3
 }
 
 // Sum the `ncontrib` partial slots (slot0, slot0 + slot_stride, ...) in order
-// and store the tile like epilogue_tma_store.
+// and store the tile like epilogue_tma_store.  The loads of up to four
+// contributors' 16-column groups are issued together before they are added
+// (in contributor order), so each thread keeps 16 loads in flight instead of
+// one contributor's worth.
 template <int BLOCK_N, bool F16OUT>
 __device__ __forceinline__ void sk_reduce_store(const float* slot0, size_t slot_stride,
                                                 int ncontrib, int q, uint32_t lane, bool issuer,
@@ -290,15 +293,33 @@ __device__ __forceinline__ void sk_reduce_store(const float* slot0, size_t slot_
 #pragma unroll
         for (int i = 0; i < S::SUB_COLS; ++i) acc[i] = 0.0f;
         if (row_valid) {
-            for (int cj = 0; cj < ncontrib; ++cj) {
-                const float4* src = reinterpret_cast<const float4*>(slot0 + cj * slot_stride);
 #pragma unroll
-                for (int c = 0; c < S::SUB_COLS / 4; ++c) {
-                    const float4 x = __ldcg(src + (j * (S::SUB_COLS / 4) + c) * 128 + row);
-                    acc[4 * c + 0] += x.x;
-                    acc[4 * c + 1] += x.y;
-                    acc[4 * c + 2] += x.z;
-                    acc[4 * c + 3] += x.w;
+            for (int g = 0; g < S::SUB_COLS / 16; ++g) {  // 16-column groups
+                const int c4 = j * (S::SUB_COLS / 4) + g * 4;
+#pragma unroll 1
+                for (int cj0 = 0; cj0 < ncontrib; cj0 += 4) {
+                    float4 x[4][4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        if (cj0 + u < ncontrib) {
+                            const float4* src =
+                                reinterpret_cast<const float4*>(slot0 + (cj0 + u) * slot_stride);
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) x[u][c] = __ldcg(src + (c4 + c) * 128 + row);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        if (cj0 + u < ncontrib) {
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                acc[g * 16 + 4 * c + 0] += x[u][c].x;
+                                acc[g * 16 + 4 * c + 1] += x[u][c].y;
+                                acc[g * 16 + 4 * c + 2] += x[u][c].z;
+                                acc[g * 16 + 4 * c + 3] += x[u][c].w;
+                            }
+                        }
+                    }
                 }
             }
         }

@@ -29,9 +29,9 @@ constexpr int NUM_STAGING = 2;            // double-buffered output staging
 // engine delivers the whole box even where it hangs past the tensor's edge
 // (the out-of-bounds part arrives zero-filled), so the count never shrinks
 // for ragged tiles.
-TG_HD uint32_t stage_tx_bytes(int block_n)
+TG_HD uint32_t stage_tx_bytes(int block_n, int a_rows = BLK_M)
 {
-    return static_cast<uint32_t>((BLK_M * BLK_K + block_n * BLK_K) * 2);
+    return static_cast<uint32_t>((a_rows * BLK_K + block_n * BLK_K) * 2);
 }
 
 // Error codes written by a kernel to its status record (same values as the
@@ -91,6 +91,9 @@ struct Params {
     // 0 = default, 1 = A evict_last / B evict_first, 2 = A evict_first /
     // B evict_last, 3 = both evict_last.
     int l2_policy;
+    // Rows of A per stage in the single-CTA warp-specialised kernels (128, or
+    // 64 when M <= 64; see a_slot_bytes).
+    int a_rows;
     // 1: a persistent worker walks the K blocks of its odd-numbered units
     // backwards, so a unit starts on the operand slices its predecessor (the
     // previous wave, which shares the A rows within a raster group) touched
@@ -235,11 +238,16 @@ constexpr uint32_t BAR_AREA_BYTES = 256;
 
 TG_HD uint32_t b_tile_bytes(int block_n) { return static_cast<uint32_t>(block_n * BLK_K * 2); }
 
-TG_HD SmemLayout smem_layout(int stages, int block_n, int staging)
+// `a_rows`: rows of A one stage holds (128, or 64 when the whole problem has at
+// most 64 rows: the MMA still computes 128 rows, and rows 64..127 -- read from
+// whatever follows the 64-row slot -- are never stored).
+TG_HD uint32_t a_slot_bytes(int a_rows) { return static_cast<uint32_t>(a_rows * BLK_K * 2); }
+
+TG_HD SmemLayout smem_layout(int stages, int block_n, int staging, int a_rows = BLK_M)
 {
     SmemLayout L;
     L.a = 0;
-    L.b = L.a + static_cast<uint32_t>(stages) * A_TILE_BYTES;
+    L.b = L.a + static_cast<uint32_t>(stages) * a_slot_bytes(a_rows);
     L.staging = L.b + static_cast<uint32_t>(stages) * b_tile_bytes(block_n);
     L.bars = L.staging + static_cast<uint32_t>(staging) * STAGING_BYTES;
     L.total = L.bars + BAR_AREA_BYTES + 1024;

@@ -66,7 +66,9 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
     constexpr uint32_t TMEM_COLS = ACC * BN;  // 64..512, a power of two
     const int D = p.pipe_depth;
     const CtaSmem sm = cta_smem();
-    const SmemLayout L = smem_layout(D, BN, NUM_STAGING);
+    const int a_rows = p.a_rows == 64 ? 64 : BLK_M;
+    const uint32_t a_slot = a_slot_bytes(a_rows);
+    const SmemLayout L = smem_layout(D, BN, NUM_STAGING, a_rows);
     const uint32_t sA = sm.base + L.a;
     const uint32_t sB = sm.base + L.b;
     const uint32_t staging = sm.base + L.staging;
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            const uint32_t tx = stage_tx_bytes(BN);
+            const uint32_t tx = stage_tx_bytes(BN, a_rows);
             const uint64_t pol_a = (p.l2_policy == 2) ? policy_evict_first() : policy_evict_last();
             const uint64_t pol_b = (p.l2_policy == 1) ? policy_evict_first() : policy_evict_last();
             if (p.debug_stall) wd.wait(bar_addr(bars, BAR_STALL), 0, WAIT_STALL, -1, -1);
@@ -146,10 +148,10 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
                         const uint32_t fb = bar_addr(bars, BAR_FULL + stage);
                         mbar_arrive_expect_tx(fb, tx);
                         if (p.l2_policy == 0) {
-                            tma_load_2d(sA + stage * A_TILE_BYTES, &tmA, fb, kb * BLK_K, m0);
+                            tma_load_2d(sA + stage * a_slot, &tmA, fb, kb * BLK_K, m0);
                             tma_load_2d(sB + stage * b_tile_bytes(BN), &tmB, fb, kb * BLK_K, n0);
                         } else {
-                            tma_load_2d_hint(sA + stage * A_TILE_BYTES, &tmA, fb, kb * BLK_K, m0,
+                            tma_load_2d_hint(sA + stage * a_slot, &tmA, fb, kb * BLK_K, m0,
                                              pol_a);
                             tma_load_2d_hint(sB + stage * b_tile_bytes(BN), &tmB, fb, kb * BLK_K,
                                              n0, pol_b);
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
                     if (!wd.aborted) {
                         tc_fence_after_sync();
                         if (ki == 0) trace_unit(p, mui, TRACE_U_MMA_FIRST, globaltimer_ns());
-                        const uint64_t adesc = sw128_kmajor_desc(sA + stage * A_TILE_BYTES);
+                        const uint64_t adesc = sw128_kmajor_desc(sA + stage * a_slot);
                         const uint64_t bdesc = sw128_kmajor_desc(sB + stage * b_tile_bytes(BN));
 #pragma unroll
                         for (int kk = 0; kk < BLK_K / MMA_K; ++kk)
