@@ -69,8 +69,8 @@ typedef enum {
                                        (clusters of 2): 256 x block_n tiles with
                                        tcgen05.mma.cta_group::2, each CTA loading
                                        its own half of the operands; block_n 128,
-                                       192 or 256 (fp16 out), 128, 160, 192, 224 or
-                                       256 (fp32 out), chosen by wave efficiency */
+                                       160, 192, 224 or 256, chosen by wave
+                                       efficiency */
 } gemm_variant;
 
 /* Plan options; a zero field means "choose automatically". */

@@ -56,7 +56,8 @@ def test_pair_many_tiles_per_cluster(grid):
 
 
 @pytest.mark.parametrize("out,bn", [("f32", 128), ("f32", 160), ("f32", 192), ("f32", 224),
-                                    ("f32", 256), ("f16", 128), ("f16", 192), ("f16", 256)])
+                                    ("f32", 256), ("f16", 128), ("f16", 160), ("f16", 192),
+                                    ("f16", 224), ("f16", 256)])
 def test_pair_tile_widths(out, bn):
     # ragged in every dimension, several tiles per pair and a second CTA whose
     # rows run past M in the last tile row

@@ -35,6 +35,7 @@ CASES = [
     ("persistent_2cta", 300, 264, 2048, 6, 256),
     ("persistent_2cta", 1280, 1024, 320, 14, 256),
     ("persistent_2cta", 700, 1000, 520, 10, 128),
+    ("persistent_2cta", 520, 1000, 776, 8, 224),     # fp16: 32-column remainder stored directly
 ]
 
 

@@ -18,6 +18,34 @@
 
 using namespace tg;
 
+namespace tg {
+
+namespace {
+std::mutex g_smem_mutex;
+std::vector<std::pair<const void*, unsigned>> g_smem_limits;
+}  // namespace
+
+bool smem_limit_known(const void* kernel, unsigned bytes)
+{
+    std::lock_guard<std::mutex> lock(g_smem_mutex);
+    for (const auto& kv : g_smem_limits)
+        if (kv.first == kernel) return bytes <= kv.second;
+    return false;
+}
+
+void smem_limit_record(const void* kernel, unsigned bytes)
+{
+    std::lock_guard<std::mutex> lock(g_smem_mutex);
+    for (auto& kv : g_smem_limits)
+        if (kv.first == kernel) {
+            if (bytes > kv.second) kv.second = bytes;
+            return;
+        }
+    g_smem_limits.emplace_back(kernel, bytes);
+}
+
+}  // namespace tg
+
 namespace {
 
 thread_local std::string g_err;
@@ -99,11 +127,12 @@ int choose_block_n(int variant, int64_t M, int64_t N, int sms)
     return best;
 }
 
-// Pair tile widths the CTA-pair kernel is built for: multiples of 32 for fp32
-// output (32-column store sub-tiles), of 64 for fp16 output.
+// Pair tile widths the CTA-pair kernel is built for: multiples of 32 (fp32
+// output stores 32-column sub-tiles; fp16 output 64-column sub-tiles plus a
+// directly stored 32-column remainder for widths 160 and 224).
 bool pair_width_ok(int bn, int dtype)
 {
-    if (dtype == GEMM_OUT_F16) return bn == 128 || bn == 192 || bn == 256;
+    (void)dtype;  // fp16 widths of 160 / 224 store their last 32 columns directly
     return bn == 128 || bn == 160 || bn == 192 || bn == 224 || bn == 256;
 }
 
@@ -188,8 +217,7 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
         return fail(GEMM_ERR_INVALID_ARG, "debug_stall needs a warp-specialised variant");
     if (is_pair(variant) && opts.block_n != 0 && !pair_width_ok(opts.block_n, dtype))
         return fail(GEMM_ERR_INVALID_ARG,
-                    "CTA-pair tile width (block_n) must be 128, 192 or 256 for fp16 output, "
-                    "or 128, 160, 192, 224 or 256 for fp32 output");
+                    "CTA-pair tile width (block_n) must be 128, 160, 192, 224 or 256");
     const int bn = opts.block_n   ? opts.block_n
                    : is_pair(variant) ? choose_pair_bn(M, N, sms, dtype)
                                       : choose_block_n(variant, M, N, sms);

@@ -194,6 +194,30 @@ __device__ __forceinline__ void stage_and_store(const uint32_t* v, uint32_t row,
     ++sub_count;
 }
 
+// A 32-column remainder of a tile whose width is not a whole number of
+// 128-byte sub-tiles (fp16 output, widths 160 and 224): row `gm`, columns
+// gn0..gn0+31, written straight from registers with 16-byte stores (N and
+// the row are checked; N * 2 is a multiple of 16 bytes, so a chunk of 8
+// halves is wholly inside or wholly outside the matrix).
+__device__ __forceinline__ void direct_store_row32_f16(const uint32_t* v, void* C, int M, int N,
+                                                       int gm, int gn0, bool do_store)
+{
+    if (!do_store || gm >= M) return;
+    __half* crow = static_cast<__half*>(C) + static_cast<size_t>(gm) * N;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int gn = gn0 + 8 * c;
+        if (gn < N) {
+            uint4 w;
+            w.x = pack_half2(v[8 * c + 0], v[8 * c + 1]);
+            w.y = pack_half2(v[8 * c + 2], v[8 * c + 3]);
+            w.z = pack_half2(v[8 * c + 4], v[8 * c + 5]);
+            w.w = pack_half2(v[8 * c + 6], v[8 * c + 7]);
+            *reinterpret_cast<uint4*>(crow + gn) = w;
+        }
+    }
+}
+
 // The whole 128 x BLOCK_N accumulator at TMEM column `tmem_acc`, sub-tile by
 // sub-tile: TMEM -> registers -> staging -> TMA store.
 template <int BLOCK_N, bool F16OUT>
@@ -201,11 +225,20 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t tmem_acc, int q, uin
                                                    bool issuer, uint32_t staging,
                                                    const CUtensorMap* tmap_c, int m0, int n0,
                                                    int N, uint32_t& sub_count, uint32_t bar_id,
-                                                   bool do_store)
+                                                   bool do_store, void* C = nullptr, int M = 0)
 {
     using S = EpilogueShape<BLOCK_N, F16OUT>;
     const uint32_t row = static_cast<uint32_t>(q) * 32u + lane;
     const uint32_t taddr = tmem_acc + (static_cast<uint32_t>(q * 32) << 16);
+    if constexpr (BLOCK_N % S::SUB_COLS != 0) {
+        static_assert(F16OUT && BLOCK_N % S::SUB_COLS == 32, "32-column remainder");
+        const int tail = S::NUM_SUB * S::SUB_COLS;
+        if (n0 + tail < N) {
+            uint32_t v[32];
+            tmem_load_32cols(taddr + tail, v);
+            direct_store_row32_f16(v, C, M, N, m0 + static_cast<int>(row), n0 + tail, do_store);
+        }
+    }
 #pragma unroll 1
     for (int j = 0; j < S::NUM_SUB; ++j) {
         const int col0 = n0 + j * S::SUB_COLS;
@@ -281,10 +314,32 @@ __device__ __forceinline__ void sk_reduce_store(const float* slot0, size_t slot_
                                                 int ncontrib, int q, uint32_t lane, bool issuer,
                                                 uint32_t staging, const CUtensorMap* tmap_c,
                                                 int m0, int n0, int N, uint32_t& sub_count,
-                                                uint32_t bar_id, bool do_store, bool row_valid)
+                                                uint32_t bar_id, bool do_store, bool row_valid,
+                                                void* C = nullptr, int M = 0)
 {
     using S = EpilogueShape<BLOCK_N, F16OUT>;
     const uint32_t row = static_cast<uint32_t>(q) * 32u + lane;
+    if constexpr (BLOCK_N % S::SUB_COLS != 0) {
+        const int tail = S::NUM_SUB * S::SUB_COLS;
+        if (n0 + tail < N && row_valid) {
+            float acc[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+            for (int cj = 0; cj < ncontrib; ++cj) {
+                const float4* src = reinterpret_cast<const float4*>(slot0 + cj * slot_stride);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const float4 x = __ldcg(src + (tail / 4 + c) * 128 + row);
+                    acc[4 * c + 0] += x.x;
+                    acc[4 * c + 1] += x.y;
+                    acc[4 * c + 2] += x.z;
+                    acc[4 * c + 3] += x.w;
+                }
+            }
+            direct_store_row32_f16(reinterpret_cast<const uint32_t*>(acc), C, M, N,
+                                   m0 + static_cast<int>(row), n0 + tail, do_store);
+        }
+    }
 #pragma unroll 1
     for (int j = 0; j < S::NUM_SUB; ++j) {
         const int col0 = n0 + j * S::SUB_COLS;
@@ -339,7 +394,8 @@ __device__ __forceinline__ void sk_epilogue(uint32_t tmem_acc, int q, uint32_t l
                                             uint32_t bar_id, bool aborted, float* slot0,
                                             size_t slot_stride, int contrib, int ncontrib,
                                             unsigned* ticket_word, int epoch,
-                                            volatile uint32_t* ticket_smem, Release release)
+                                            volatile uint32_t* ticket_smem, Release release,
+                                            void* C = nullptr)
 {
     const uint32_t row = static_cast<uint32_t>(q) * 32u + lane;
     const bool row_valid = m0 + static_cast<int>(row) < M;
@@ -361,7 +417,7 @@ __device__ __forceinline__ void sk_epilogue(uint32_t tmem_acc, int q, uint32_t l
         __threadfence();
         sk_reduce_store<BLOCK_N, F16OUT>(slot0, slot_stride, ncontrib, q, lane, issuer, staging,
                                          tmap_c, m0, n0, N, sub_count, bar_id, !aborted,
-                                         row_valid);
+                                         row_valid, C, M);
     }
 }
 

@@ -314,8 +314,7 @@ namespace {
 template <typename KernelT>
 cudaError_t launch_kernel(KernelT kernel, const LaunchSpec& s, cudaStream_t stream)
 {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(s.smem_bytes));
+    cudaError_t e = ensure_smem_limit(kernel, s.smem_bytes);
     if (e != cudaSuccess) return e;
     kernel<<<s.grid, WS_THREADS, s.smem_bytes, stream>>>(*s.tmA, *s.tmB, *s.tmC, s.p);
     return cudaGetLastError();

@@ -68,7 +68,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
           const __grid_constant__ CUtensorMap tmC, const Params p)
 {
     static_assert(PAIR_BN % 32 == 0 && PAIR_BN >= 64 && PAIR_BN <= 256, "pair tile width");
-    static_assert(!F16OUT || PAIR_BN % 64 == 0, "fp16 output stores 64-column sub-tiles");
+    static_assert(!F16OUT || PAIR_BN % 64 == 0 || PAIR_BN % 64 == 32,
+                  "fp16 output: 64-column sub-tiles plus at most one 32-column remainder");
     constexpr int HALF_BN = PAIR_BN / 2;  // B rows held by each CTA
     constexpr int ACC = 2;
     // two accumulators of PAIR_BN columns, rounded up to a legal allocation
@@ -297,7 +298,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
             if (u.ncontrib == 1) {
                 epilogue_tma_store<PAIR_BN, F16OUT>(tmem_acc, q, lane, issuer, staging, &tmC, m0,
                                                     nt * PAIR_BN, p.N, sub_count,
-                                                    PAIR_EPI_BAR_ID, !wd.aborted && m0 < p.M);
+                                                    PAIR_EPI_BAR_ID, !wd.aborted && m0 < p.M,
+                                                    p.C, p.M);
                 release();
             } else {
                 // each CTA fixes up its own 128 rows of the pair tile
@@ -309,7 +311,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                                              nt * PAIR_BN, p.M, p.N, sub_count, PAIR_EPI_BAR_ID,
                                              wd.aborted, slot0, 2 * slot_elems, u.contrib,
                                              u.ncontrib, p.sk_tickets + u.sk_index * 2 + rank,
-                                             p.epoch, ticket_smem, release);
+                                             p.epoch, ticket_smem, release, p.C);
             }
             if (issuer) trace_unit(p, eui, TRACE_U_EPI_END, globaltimer_ns());
             ++eui;
@@ -336,8 +338,7 @@ namespace {
 template <typename KernelT>
 cudaError_t launch_pair_kernel(KernelT kernel, const LaunchSpec& s, cudaStream_t stream)
 {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(s.smem_bytes));
+    cudaError_t e = ensure_smem_limit(kernel, s.smem_bytes);
     if (e != cudaSuccess) return e;
     kernel<<<s.grid, PAIR_THREADS, s.smem_bytes, stream>>>(*s.tmA, *s.tmB, *s.tmC, s.p);
     return cudaGetLastError();
@@ -351,7 +352,9 @@ cudaError_t launch_pair(const LaunchSpec& s, cudaStream_t stream)
     if (s.f16out) {
         switch (s.block_n) {
         case 128: return launch_pair_kernel(k_ws2<128, true>, s, stream);
+        case 160: return launch_pair_kernel(k_ws2<160, true>, s, stream);
         case 192: return launch_pair_kernel(k_ws2<192, true>, s, stream);
+        case 224: return launch_pair_kernel(k_ws2<224, true>, s, stream);
         case 256: return launch_pair_kernel(k_ws2<256, true>, s, stream);
         default: return cudaErrorInvalidValue;
         }

@@ -376,8 +376,7 @@ namespace {
 template <typename KernelT, typename... Args>
 cudaError_t launch_one(KernelT kernel, const LaunchSpec& s, cudaStream_t stream, Args... args)
 {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(s.smem_bytes));
+    cudaError_t e = ensure_smem_limit(kernel, s.smem_bytes);
     if (e != cudaSuccess) return e;
     kernel<<<s.grid, s.threads, s.smem_bytes, stream>>>(args...);
     return cudaGetLastError();

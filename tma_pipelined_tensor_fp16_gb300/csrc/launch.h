@@ -43,4 +43,21 @@ cudaError_t launch_ws(const LaunchSpec& s, cudaStream_t stream);
 // Warp-specialised persistent GEMM on CTA pairs: VAR_PERSISTENT_2CTA.
 cudaError_t launch_pair(const LaunchSpec& s, cudaStream_t stream);
 
+// Raise `kernel`'s dynamic shared-memory limit to at least `bytes`, calling
+// the runtime only when a larger limit than any set before for that kernel is
+// needed (the limit belongs to the kernel, for the whole process).
+bool smem_limit_known(const void* kernel, unsigned bytes);
+void smem_limit_record(const void* kernel, unsigned bytes);
+
+template <typename KernelT>
+cudaError_t ensure_smem_limit(KernelT kernel, unsigned bytes)
+{
+    const void* key = reinterpret_cast<const void*>(kernel);
+    if (smem_limit_known(key, bytes)) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(bytes));
+    if (e == cudaSuccess) smem_limit_record(key, bytes);
+    return e;
+}
+
 }  // namespace tg
