@@ -65,12 +65,25 @@ typedef enum {
                                        raster, two TMEM accumulators */
     GEMM_VAR_PERSISTENT_LOCKSTEP = 6, /* Step 6 as printed: persistent CTAs running
                                        the lock-step Step-5 loop */
-    GEMM_VAR_PERSISTENT_2CTA = 7    /* warp-specialised, persistent, on CTA pairs
+    GEMM_VAR_PERSISTENT_2CTA = 7,   /* warp-specialised, persistent, on CTA pairs
                                        (clusters of 2): 256 x block_n tiles with
                                        tcgen05.mma.cta_group::2, each CTA loading
                                        its own half of the operands; block_n 128,
                                        160, 192, 224 or 256, chosen by wave
                                        efficiency */
+    GEMM_VAR_DYNAMIC_2CTA = 8       /* the CTA-pair kernel with a dynamic tile
+                                       schedule ("GEMM II -- pipelining with
+                                       TMA", Step 6: cluster launch control as
+                                       the upgrade of the static assignment):
+                                       the grid has one cluster per tile, and
+                                       a running cluster cancels clusters that
+                                       have not started
+                                       (clusterlaunchcontrol.try_cancel) and
+                                       computes their tiles.  grid must be 0;
+                                       stream_k = 2 is GEMM_ERR_UNSUPPORTED;
+                                       gemm_schedule_unit reports only each
+                                       cluster's own tile, the rest being
+                                       assigned at run time */
 } gemm_variant;
 
 /* Plan options; a zero field means "choose automatically". */

@@ -129,6 +129,35 @@ def test_pair_variant_constraints(b):
     assert st == 0  # 24 KB stages: eight fit
 
 
+def test_dynamic_pair_configuration(b):
+    # One cluster per pair tile; the clusters that run cancel the others
+    # ("GEMM II -- pipelining with TMA", Step 6: cluster launch control).
+    st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(variant="dynamic_2cta"))
+    assert st == 0, b.last_error()
+    assert c.variant == b.GEMM_VAR_DYNAMIC_2CTA
+    assert (c.block_m, c.block_n, c.pipe_depth, c.threads, c.tmem_cols) == (256, 256, 6, 192, 512)
+    assert c.grid == 2 * c.num_tiles == 2048
+    assert (c.dp_tiles, c.sk_tiles, c.workspace_bytes) == (1024, 0, 0)
+    assert c.smem_bytes <= 232448
+    st, c = b.gemm_select_config(4000, 3000, 5000, 0, b.make_options(variant="dynamic_2cta"))
+    assert st == 0 and c.block_n == 224 and c.grid == 2 * c.num_tiles
+    st, _ = b.gemm_select_config(8192, 8192, 8192, 1,
+                                 b.make_options(variant="dynamic_2cta", grid=152))
+    assert st == b.GEMM_ERR_INVALID_ARG and "grid" in b.last_error()
+    st, _ = b.gemm_select_config(8192, 8192, 8192, 1,
+                                 b.make_options(variant="dynamic_2cta", stream_k="on"))
+    assert st == b.GEMM_ERR_UNSUPPORTED and "stream-K" in b.last_error()
+    st, _ = b.gemm_select_config(8192, 8192, 8192, 1,
+                                 b.make_options(variant="dynamic_2cta", block_n=64))
+    assert st == b.GEMM_ERR_INVALID_ARG
+    # the schedule query reports each cluster's own tile; the rest is decided
+    # while the kernel runs
+    st, c = b.gemm_select_config(1000, 1000, 520, 1, b.make_options(variant="dynamic_2cta"))
+    assert st == 0
+    for w in range(c.grid // 2):
+        assert b.gemm_worker_units(c, w) == [(w, 0, c.k_blocks, 0, 1)]
+
+
 def test_stage_byte_count_matches_page_formula(b):
     # byte_count = (BLK_M*BLK_K + BLK_N*BLK_K) * 2 for fp16 tiles
     g = _golden("p1_step4_byte_count.txt")
@@ -214,12 +243,14 @@ def test_swizzle_map_matches_page_rule_and_bank_analysis(b):
     (64, 16384, 16384, {"stream_k": "on"}),                   # every tile shared
     (1000, 1000, 520, {"variant": "persistent", "grid": 7, "stream_k": "on"}),
     (1000, 1000, 520, {"variant": "persistent_2cta", "grid": 10, "stream_k": "on"}),
+    (1000, 1000, 520, {"variant": "dynamic_2cta"}),           # own tile per cluster
     (300, 520, 64, {"variant": "persistent", "stream_k": "on"}),   # one K block per tile
 ])
 def test_work_units_cover_every_k_block_once(b, M, N, K, opts):
     st, c = b.gemm_select_config(M, N, K, 1, b.make_options(**opts))
     assert st == 0, b.last_error()
-    workers = c.grid // 2 if c.variant == b.GEMM_VAR_PERSISTENT_2CTA else c.grid
+    pair = c.variant in (b.GEMM_VAR_PERSISTENT_2CTA, b.GEMM_VAR_DYNAMIC_2CTA)
+    workers = c.grid // 2 if pair else c.grid
     cover = np.zeros((c.num_tiles, c.k_blocks), dtype=np.int64)
     contribs = {}
     work = []

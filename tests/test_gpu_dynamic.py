@@ -1,0 +1,129 @@
+"""GPU parity of the dynamic CTA-pair schedule (dynamic_2cta) against the CPU
+oracle.  The grid holds one cluster per pair tile; a running cluster cancels
+clusters that have not started (cluster launch control) and computes their
+tiles ("GEMM II -- pipelining with TMA", Step 6: hardware work-stealing in
+place of the precomputed tile assignment).
+
+Covers one tile (the first request finds nothing to cancel), tile counts below
+and above the number of resident clusters, every pair width, integer inputs
+bit-exact, the five workload shapes at full size, that the tile sequence
+visits every tile exactly once (from the device timeline), that results are
+identical bit for bit to the static schedule's and from run to run, and the
+watchdog.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from tma_pipelined_tensor_fp16_gb300 import inputs
+
+from gpu_util import assert_close, assert_exact, run
+
+pytestmark = pytest.mark.gpu
+V = "dynamic_2cta"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+@pytest.mark.parametrize("out", ["f32", "f16"])
+@pytest.mark.parametrize("shape", [(1, 8, 8), (100, 256, 64), (300, 520, 328), (640, 776, 456),
+                                   (1280, 1024, 320), (2304, 2560, 192)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_dynamic_small_shapes(out, shape):
+    M, N, K = shape
+    A, B = inputs.make_operands(M, N, K, "uniform", 500 + M + N + K)
+    got, guard, desc = run(A, B, out, guard_rows=3, variant=V)
+    assert_close(got, oracle.gemm(A, B), K, out, desc)
+    assert np.isnan(guard.astype(np.float32)).all(), "wrote past the end of C"
+
+
+@pytest.mark.parametrize("out,bn", [("f32", 128), ("f32", 160), ("f32", 192), ("f32", 224),
+                                    ("f32", 256), ("f16", 128), ("f16", 160), ("f16", 192),
+                                    ("f16", 224), ("f16", 256)])
+def test_dynamic_tile_widths(out, bn):
+    # 80 to 160 tiles: more than the 76 clusters that fit at once, so most
+    # tiles are taken over by cancellation; ragged in every dimension
+    M, N, K = 5000, 1000, 136
+    A, B = inputs.make_operands(M, N, K, "normal", 1900 + bn)
+    got, guard, desc = run(A, B, out, guard_rows=2, variant=V, block_n=bn)
+    assert "x%d" % bn in desc, desc
+    assert_close(got, oracle.gemm(A, B), K, out, desc)
+    assert np.isnan(guard.astype(np.float32)).all()
+    Ai, Bi = inputs.make_operands(M, N, K, "int", 15)
+    goti, _, _ = run(Ai, Bi, out, variant=V, block_n=bn)
+    assert_exact(goti, oracle.gemm(Ai, Bi), out, desc)
+
+
+@pytest.mark.parametrize("depth", [1, 3, 6])
+def test_dynamic_depths_short_k(depth):
+    for kt in sorted({1, depth, depth + 1}):
+        M, N, K = 2560, 2048, 64 * kt - 8 * (kt % 2)
+        A, B = inputs.make_operands(M, N, K, "normal", 3000 + depth * 16 + kt)
+        got, _, desc = run(A, B, "f32", variant=V, pipe_depth=depth)
+        assert_close(got, oracle.gemm(A, B), K, "f32", "K tiles=%d %s" % (kt, desc))
+
+
+def _sample(M, N, count, seed):
+    rng = np.random.default_rng(seed)
+    rows = np.concatenate([rng.integers(0, M, count), [0, M - 1, min(255, M - 1)]])
+    cols = np.concatenate([rng.integers(0, N, count), [N - 1, 0, min(255, N - 1)]])
+    return rows.astype(np.int64), cols.astype(np.int64)
+
+
+@pytest.mark.parametrize("cfg", inputs.CONFIGS, ids=[c["name"] for c in inputs.CONFIGS])
+def test_dynamic_workloads_match_static_schedule(cfg):
+    # Every tile walks K in the same direction under both schedules, so the
+    # fp32 sums are formed in the same order and the outputs agree bit for bit.
+    M, N, K, out = cfg["M"], cfg["N"], cfg["K"], cfg["out"]
+    A, B = inputs.make_operands(M, N, K, cfg["dist"], cfg["seed"])
+    got, _, desc = run(A, B, out, variant=V)
+    ref_static, _, desc_s = run(A, B, out, variant="persistent_2cta")
+    assert np.array_equal(got.view(np.uint8), ref_static.view(np.uint8)), (desc, desc_s)
+    rows, cols = _sample(M, N, 2000, cfg["seed"])
+    assert_close(got[rows, cols], oracle.gemm_entries(A, B, rows, cols), K, out, desc)
+    again, _, _ = run(A, B, out, variant=V)
+    assert np.array_equal(got.view(np.uint8), again.view(np.uint8)), "run-to-run difference"
+
+
+def test_dynamic_visits_every_tile_once():
+    from tma_pipelined_tensor_fp16_gb300 import timeline
+    M = N = K = 4096
+    tr, cfg = timeline.record(M, N, K, "f16", "uniform", 1, warmup=2, units=64, variant=V)
+    live = timeline.ran(tr)
+    assert len(live) % 2 == 0 and len(live) < cfg["grid"]  # most clusters were cancelled
+    seen = []
+    for b in live:
+        n = int(tr[b, 0, timeline.H_UNITS])
+        assert 0 < n <= 64
+        tiles = [int(tr[b, 1 + i, timeline.U_TILE]) >> 32 for i in range(n)]
+        if b % 2 == 0:
+            seen.extend(tiles)
+        else:  # both CTAs of a cluster walk the same sequence
+            assert tiles == [int(tr[b - 1, 1 + i, timeline.U_TILE]) >> 32 for i in range(n)]
+    assert sorted(seen) == list(range(cfg["num_tiles"]))
+
+
+def test_dynamic_watchdog_timeout():
+    import torch
+
+    import tma_pipelined_tensor_fp16_gb300 as pkg
+    from tma_pipelined_tensor_fp16_gb300 import binding
+    M, N, K = 2048, 2048, 256
+    A, B = inputs.make_operands(M, N, K, "uniform", 3)
+    dA = torch.from_numpy(A.view(np.float16)).cuda()
+    dB = torch.from_numpy(B.view(np.float16)).cuda()
+    C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    plan = pkg.Plan(M, N, K, out="f32", variant=V, debug_stall=1, wait_budget_ms=100)
+    plan(dA, dB, C)
+    torch.cuda.synchronize()
+    assert plan.device_status() == binding.GEMM_ERR_TIMEOUT
+    plan.close()
+    got, _, desc = run(A, B, "f32", variant=V)
+    assert_close(got, oracle.gemm(A, B), K, "f32", "after timeout: " + desc)

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -81,19 +82,24 @@ const char* variant_name(int v)
     case VAR_PERSISTENT: return "persistent";
     case VAR_PERSISTENT_LOCKSTEP: return "persistent_lockstep";
     case VAR_PERSISTENT_2CTA: return "persistent_2cta";
+    case VAR_DYNAMIC_2CTA: return "dynamic_2cta";
     default: return "?";
     }
 }
 
 bool is_ws(int v)
 {
-    return v == VAR_WS_PIPELINED || v == VAR_PERSISTENT || v == VAR_PERSISTENT_2CTA;
+    return v == VAR_WS_PIPELINED || v == VAR_PERSISTENT || v == VAR_PERSISTENT_2CTA ||
+           v == VAR_DYNAMIC_2CTA;
 }
+// One resident CTA per SM that takes tile after tile (statically or by
+// cancelling clusters that have not started).
 bool is_persistent(int v)
 {
-    return v == VAR_PERSISTENT || v == VAR_PERSISTENT_LOCKSTEP || v == VAR_PERSISTENT_2CTA;
+    return v == VAR_PERSISTENT || v == VAR_PERSISTENT_LOCKSTEP || v == VAR_PERSISTENT_2CTA ||
+           v == VAR_DYNAMIC_2CTA;
 }
-bool is_pair(int v) { return v == VAR_PERSISTENT_2CTA; }
+bool is_pair(int v) { return v == VAR_PERSISTENT_2CTA || v == VAR_DYNAMIC_2CTA; }
 bool has_ring(int v) { return v != VAR_SYNC_TILED && v != VAR_TMA_SERIAL; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -194,11 +200,11 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     if ((N * elt) % 16 != 0)
         return fail(GEMM_ERR_UNSUPPORTED,
                     "N * sizeof(output) must be a multiple of 16 bytes (TMA row stride of C)");
-    if (opts.variant < 0 || opts.variant > VAR_PERSISTENT_2CTA)
+    if (opts.variant < 0 || opts.variant > VAR_DYNAMIC_2CTA)
         return fail(GEMM_ERR_INVALID_ARG, "unknown variant");
     if (opts.pipe_depth < 0 || opts.pipe_depth > MAX_STAGES)
         return fail(GEMM_ERR_INVALID_ARG, "pipe_depth must be 0 (auto) or 1..8");
-    const bool pair_requested = opts.variant == VAR_PERSISTENT_2CTA;
+    const bool pair_requested = is_pair(opts.variant);
     if (!pair_requested && opts.block_n != 0 && opts.block_n != 64 && opts.block_n != 128 &&
         opts.block_n != 256)
         return fail(GEMM_ERR_INVALID_ARG, "block_n must be 0 (auto), 64, 128 or 256");
@@ -215,6 +221,12 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     const int variant = opts.variant == VAR_AUTO ? auto_variant(M, N, sms) : opts.variant;
     if (opts.debug_stall && !is_ws(variant))
         return fail(GEMM_ERR_INVALID_ARG, "debug_stall needs a warp-specialised variant");
+    if (variant == VAR_DYNAMIC_2CTA && opts.grid != 0)
+        return fail(GEMM_ERR_INVALID_ARG,
+                    "dynamic_2cta launches one cluster per tile: grid must be 0 (auto)");
+    if (variant == VAR_DYNAMIC_2CTA && opts.stream_k == 2)
+        return fail(GEMM_ERR_UNSUPPORTED,
+                    "dynamic_2cta schedules whole tiles: stream-K needs a static variant");
     if (is_pair(variant) && opts.block_n != 0 && !pair_width_ok(opts.block_n, dtype))
         return fail(GEMM_ERR_INVALID_ARG,
                     "CTA-pair tile width (block_n) must be 128, 160, 192, 224 or 256");
@@ -295,8 +307,12 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
         (void)L;
         return opts.stream_k == 2;
     };
-    const bool sk_capable = variant == VAR_PERSISTENT || is_pair(variant);
-    if (is_pair(variant)) {
+    const bool sk_capable = variant == VAR_PERSISTENT || variant == VAR_PERSISTENT_2CTA;
+    if (variant == VAR_DYNAMIC_2CTA) {
+        // one cluster per pair tile; running clusters cancel the rest
+        if (2 * tiles > LIM) return fail(GEMM_ERR_UNSUPPORTED, "too many output tiles");
+        c->grid = static_cast<int>(2 * tiles);
+    } else if (is_pair(variant)) {
         // clusters of two CTAs, one pair tile per cluster at a time
         int64_t pairs = (opts.grid ? opts.grid : sms) / 2;
         if (pairs < 1) pairs = 1;
@@ -399,6 +415,7 @@ struct gemm_plan {
     int debug_stall;
     int l2_policy;
     int k_snake;
+    int snake_span;  // dynamic schedule: see Params::snake_span
     DevStatus* d_status;
     int epoch;
     // tensor maps for the last (A, B, C) triple
@@ -484,6 +501,9 @@ gemm_plan* gemm_create_plan_ex(int64_t M, int64_t N, int64_t K, int dtype_out,
     // downwards (measured: 14 % less DRAM traffic at 8192^3, L2 hit rate
     // 73 % -> 80 %).
     p->k_snake = (opts && opts->k_order == 1) ? 0 : 1;
+    // The dynamic schedule takes each tile's K direction from the tile index,
+    // as the static schedule of a full grid (SM count / 2 clusters) would.
+    p->snake_span = std::max(1, std::min(sms / 2, p->cfg.num_tiles));
     e = cudaMalloc(&p->d_status, sizeof(DevStatus));
     if (e == cudaSuccess) e = cudaMemset(p->d_status, 0, sizeof(DevStatus));
     if (e == cudaSuccess && p->cfg.workspace_bytes > 0) {
@@ -585,6 +605,7 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
     p.debug_stall = plan->debug_stall;
     p.l2_policy = plan->l2_policy;
     p.k_snake = plan->k_snake;
+    p.snake_span = plan->snake_span;
     p.a_rows = c.a_rows;
     p.dp_tiles = c.dp_tiles;
     p.sk_tiles = c.sk_tiles;
@@ -830,8 +851,8 @@ int gemm_set_trace(gemm_plan* plan, void* device_buffer, int units_per_cta)
         return fail(GEMM_ERR_INVALID_ARG, "units_per_cta must be >= 1");
     if (device_buffer && (reinterpret_cast<uintptr_t>(device_buffer) & 7u))
         return fail(GEMM_ERR_INVALID_ARG, "trace buffer must be 8-byte aligned");
-    if (device_buffer && plan->cfg.variant != VAR_PERSISTENT &&
-        plan->cfg.variant != VAR_PERSISTENT_2CTA && plan->cfg.variant != VAR_WS_PIPELINED)
+    if (device_buffer && plan->cfg.variant != VAR_PERSISTENT && !is_pair(plan->cfg.variant) &&
+        plan->cfg.variant != VAR_WS_PIPELINED)
         return fail(GEMM_ERR_UNSUPPORTED, "the timeline is recorded by the warp-specialised variants");
     plan->trace = static_cast<unsigned long long*>(device_buffer);
     plan->trace_units = device_buffer ? units_per_cta : 0;

@@ -21,6 +21,10 @@ constexpr int BLK_M = 128;
 constexpr int BLK_K = 64;
 constexpr int MMA_K = 16;
 constexpr int MAX_STAGES = 8;
+// Depth of the cluster-launch-control response ring: the producer requests
+// the next tile when it starts a tile, while the epilogue still reads the
+// tile before last, so up to three responses are live at once.
+constexpr int CLC_SLOTS = 4;
 constexpr int STAGING_BYTES = 128 * 128;  // one 128-row x 128-byte output sub-tile
 constexpr int NUM_STAGING = 2;            // double-buffered output staging
 
@@ -46,7 +50,9 @@ enum : int {
     WAIT_TMEM_FULL = 4,   // epilogue waiting for an accumulator
     WAIT_TMEM_EMPTY = 5,  // MMA issuer waiting for the epilogue to drain TMEM
     WAIT_DRAIN = 6,       // teardown waiting for in-flight copies / MMAs
-    WAIT_STALL = 7        // the stall-test barrier that nothing completes
+    WAIT_STALL = 7,       // the stall-test barrier that nothing completes
+    WAIT_CLC_FULL = 8,    // waiting for a cluster-launch-control response
+    WAIT_CLC_EMPTY = 9    // scheduler waiting for every reader of a response slot
 };
 
 // Device-side status record, one per plan (device memory, 32 bytes).
@@ -99,6 +105,12 @@ struct Params {
     // previous wave, which shares the A rows within a raster group) touched
     // last and that are still in L2.  0: always ascending.
     int k_snake;
+    // Dynamic tile schedule: which cluster computes a tile, and in which
+    // position of its sequence, depends on timing.  So the K direction of
+    // tile t is taken from the tile itself: descending when t / snake_span is
+    // odd.  With snake_span equal to the static schedule's cluster count,
+    // every tile walks K in the same direction under both schedules.
+    int snake_span;
 };
 
 // The i-th K block (i = 0, 1, ...) processed for work unit number `unit` of a
@@ -234,7 +246,7 @@ struct SmemLayout {
 };
 
 constexpr uint32_t A_TILE_BYTES = BLK_M * BLK_K * 2;  // 16 KB
-constexpr uint32_t BAR_AREA_BYTES = 256;
+constexpr uint32_t BAR_AREA_BYTES = 384;
 
 TG_HD uint32_t b_tile_bytes(int block_n) { return static_cast<uint32_t>(block_n * BLK_K * 2); }
 
@@ -263,10 +275,18 @@ enum : int {
     BAR_MMA = BAR_TMEM_EMPTY + 2,            // MMA batch complete (lock-step variants)
     BAR_DRAIN = BAR_MMA + 1,                 // teardown drain of in-flight MMAs
     BAR_STALL = BAR_DRAIN + 1,               // stall test: never completed
-    BAR_COUNT = BAR_STALL + 1
+    BAR_CLC_FULL = BAR_STALL + 1,            // [CLC_SLOTS] cancellation response landed
+    BAR_CLC_EMPTY = BAR_CLC_FULL + CLC_SLOTS,  // [CLC_SLOTS] every reader done (leader)
+    BAR_COUNT = BAR_CLC_EMPTY + CLC_SLOTS
 };
 constexpr uint32_t TMEM_SLOT_OFFSET = BAR_COUNT * 8;     // u32 TMEM base address
 constexpr uint32_t TICKET_SLOT_OFFSET = TMEM_SLOT_OFFSET + 4;  // u32 stream-K ticket broadcast
-static_assert(TICKET_SLOT_OFFSET + 4 <= BAR_AREA_BYTES, "barrier area too small");
+// Cluster-launch-control responses: CLC_SLOTS opaque 16-byte records, 16-byte
+// aligned (the barrier area starts on a 1024-byte boundary).
+constexpr uint32_t CLC_RESP_OFFSET = 256;
+constexpr uint32_t CLC_RESP_BYTES = 16;
+static_assert(TICKET_SLOT_OFFSET + 4 <= CLC_RESP_OFFSET, "barrier area too small");
+static_assert(CLC_RESP_OFFSET + CLC_SLOTS * CLC_RESP_BYTES <= BAR_AREA_BYTES,
+              "barrier area too small for the response ring");
 
 }  // namespace tg

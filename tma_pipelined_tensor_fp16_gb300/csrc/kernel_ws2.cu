@@ -1,372 +1,15 @@
-// kernel_ws2.cu -- the persistent, warp-specialised GEMM on CTA pairs: a
-// cluster of two CTAs on the two SMs of a TPC computes one 256 x 256 output
-// tile with tcgen05.mma.cta_group::2 issued by the pair's leader.
-//
-// Why pairs: with one CTA per tile the 128 x 256 tile leaves room for only
-// four 48 KB stages beside the output staging, and the main loop is latency
-// bound at that depth (the PIPE_DEPTH sweep: 906 / 1441 / 1625 TFLOP/s at depth
-// 2 / 3 / 4 on 8192^3).  In a pair each CTA keeps its own 128 rows of A and
-// half of B (128 rows) per stage -- 32 KB -- so six stages fit, and every byte
-// of B fetched from L2 now feeds 256 rows of A instead of 128.
-//
-// No TMA multicast is used: each CTA loads its own tiles into its own shared
-// memory.  Both CTAs' copies signal the LEADER's full[s] barrier (the
-// .cta_group::2 form of the bulk tensor copy), which the leader's producer
-// arms with the pair's whole byte budget; the leader's MMA commits are
-// multicast to both CTAs' empty[s] / tmem_full[a] barriers; both CTAs'
-// epilogue warps arrive on the leader's tmem_empty[a].
-//
-// Roles per CTA (192 threads), as in kernel_ws.cu:
-//   warp 0 lane 0   TMA producer (both CTAs)
-//   warp 1 lane 0   MMA issuer (leader only); warp 1 of each CTA allocates TMEM
-//   warps 2..5      epilogue of this CTA's 128 rows of the pair tile
-// The ring position {stage, phase} and the accumulator position run on
-// continuously across tiles.
-#include "device_common.cuh"
-#include "launch.h"
+// kernel_ws2.cu -- the CTA-pair GEMM (kernel_ws2.cuh) with the static
+// persistent schedule: one cluster per TPC walking its WorkIter sequence.
+#include "kernel_ws2.cuh"
 
 namespace tg {
 
-namespace {
-
-struct CtaSmem {
-    uint8_t* gen;
-    uint32_t base;
-};
-
-__device__ __forceinline__ CtaSmem cta_smem()
-{
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = align1024(raw);
-    return CtaSmem{smem_raw + (base - raw), base};
-}
-
-__device__ __forceinline__ uint32_t bar_addr(uint32_t bars, int slot)
-{
-    return bars + static_cast<uint32_t>(slot) * 8u;
-}
-
-}  // namespace
-
-constexpr int PAIR_THREADS = 192;
-constexpr int PAIR_BM = 2 * BLK_M;   // 256 output rows per pair tile
-constexpr uint32_t PAIR_EPI_BAR_ID = 1;
-
-__host__ __device__ constexpr uint32_t pow2_at_least(uint32_t x)
-{
-    uint32_t r = 32;
-    while (r < x) r <<= 1;
-    return r;
-}
-
-// PAIR_BN: output columns per pair tile (a multiple of 32 up to 256; each CTA
-// holds PAIR_BN / 2 rows of B per stage).
-template <int PAIR_BN, bool F16OUT>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
-    k_ws2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-          const __grid_constant__ CUtensorMap tmC, const Params p)
-{
-    static_assert(PAIR_BN % 32 == 0 && PAIR_BN >= 64 && PAIR_BN <= 256, "pair tile width");
-    static_assert(!F16OUT || PAIR_BN % 64 == 0 || PAIR_BN % 64 == 32,
-                  "fp16 output: 64-column sub-tiles plus at most one 32-column remainder");
-    constexpr int HALF_BN = PAIR_BN / 2;  // B rows held by each CTA
-    constexpr int ACC = 2;
-    // two accumulators of PAIR_BN columns, rounded up to a legal allocation
-    constexpr uint32_t TMEM_COLS = pow2_at_least(ACC * PAIR_BN);
-    const int D = p.pipe_depth;
-    const CtaSmem sm = cta_smem();
-    const SmemLayout L = smem_layout(D, HALF_BN, NUM_STAGING);
-    const uint32_t sA = sm.base + L.a;
-    const uint32_t sB = sm.base + L.b;
-    const uint32_t staging = sm.base + L.staging;
-    const uint32_t bars = sm.base + L.bars;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm.gen + L.bars + TMEM_SLOT_OFFSET);
-    const int tid = static_cast<int>(threadIdx.x);
-    const int warp = tid >> 5;
-    const uint32_t lane = lane_id();
-    const uint32_t rank = cluster_ctarank();  // 0 = leader
-    const bool leader = rank == 0;
-    Watchdog wd = make_watchdog(p);
-    const int pair = static_cast<int>(blockIdx.x >> 1);
-    const int npairs = static_cast<int>(gridDim.x >> 1);
-    const int KB = p.k_blocks;
-    WorkIter units0;
-    units0.init(pair, npairs, p.dp_tiles, p.sk_tiles, KB, p.sk_kb_per_worker);
-
-    if (warp == 0 && lane == 0) {
-        prefetch_tensormap(&tmA);
-        prefetch_tensormap(&tmB);
-        prefetch_tensormap(&tmC);
-        for (int s = 0; s < D; ++s) {
-            mbar_init(bar_addr(bars, BAR_FULL + s), 1);   // leader: its producer's expect_tx
-            mbar_init(bar_addr(bars, BAR_EMPTY + s), 1);  // the leader's multicast commit
-        }
-        for (int a = 0; a < ACC; ++a) {
-            mbar_init(bar_addr(bars, BAR_TMEM_FULL + a), 1);   // the leader's multicast commit
-            mbar_init(bar_addr(bars, BAR_TMEM_EMPTY + a), 8);  // leader: 4 epilogue warps x 2 CTAs
-        }
-        mbar_init(bar_addr(bars, BAR_DRAIN), 1);
-        mbar_init(bar_addr(bars, BAR_STALL), 1);
-        fence_mbar_init();
-    }
-    if (warp == 1) {
-        tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
-        tmem_relinquish_alloc_permit_pair();
-    }
-    // both CTAs' barriers exist before either touches the other's
-    tc_fence_before_sync();
-    cluster_sync_all();
-    tc_fence_after_sync();
-    const uint32_t tmem_base = *tmem_slot;
-    if (tid == 0) {
-        trace_header(p, TRACE_H_START, globaltimer_ns());
-        trace_header(p, TRACE_H_SMID, sm_id());
-    }
-
-    if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------ TMA producer
-            const uint32_t pair_tx = 2u * stage_tx_bytes(HALF_BN);  // both CTAs' A and B
-            const uint64_t pol_a = (p.l2_policy == 2) ? policy_evict_first() : policy_evict_last();
-            const uint64_t pol_b = (p.l2_policy == 1) ? policy_evict_first() : policy_evict_last();
-            if (p.debug_stall) wd.wait(bar_addr(bars, BAR_STALL), 0, WAIT_STALL, -1, -1);
-            int stage = 0;
-            uint32_t phase = 0;
-            int armed = 0;
-            int end_stage = 0;       // ring position just after the last armed stage
-            uint32_t end_phase = 0;
-            WorkIter units = units0;
-            WorkUnit u;
-            int ui = 0;
-            while (units.next(u)) {
-                const int t = u.tile;
-                trace_unit(p, ui, TRACE_U_TILE,
-                           (static_cast<unsigned long long>(t) << 32) |
-                               static_cast<unsigned>(u.kb1 - u.kb0));
-                unsigned long long empty_wait_ns = 0;
-                int mt, nt;
-                raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
-                const int m0 = mt * PAIR_BM + static_cast<int>(rank) * BLK_M;
-                const int nb = nt * PAIR_BN + static_cast<int>(rank) * HALF_BN;
-                for (int ki = 0; ki < u.kb1 - u.kb0; ++ki) {
-                    const int kb = kblock_at(ki, ui, u.kb0, u.kb1, p.k_snake);
-                    const unsigned long long tw0 = p.trace ? globaltimer_ns() : 0ull;
-                    wd.wait(bar_addr(bars, BAR_EMPTY + stage), phase ^ 1u, WAIT_EMPTY, t, kb);
-                    if (p.trace) empty_wait_ns += globaltimer_ns() - tw0;
-                    if (!wd.aborted) {
-                        const uint32_t fb_local = bar_addr(bars, BAR_FULL + stage);
-                        const uint32_t fb_leader = map_shared_rank(fb_local, 0);
-                        if (leader) {
-                            mbar_arrive_expect_tx(fb_local, pair_tx);
-                            ++armed;
-                        }
-                        if (p.l2_policy == 0) {
-                            tma_load_2d_pair(sA + stage * A_TILE_BYTES, &tmA, fb_leader,
-                                             kb * BLK_K, m0);
-                            tma_load_2d_pair(sB + stage * b_tile_bytes(HALF_BN), &tmB, fb_leader,
-                                             kb * BLK_K, nb);
-                        } else {
-                            tma_load_2d_pair_hint(sA + stage * A_TILE_BYTES, &tmA, fb_leader,
-                                                  kb * BLK_K, m0, pol_a);
-                            tma_load_2d_pair_hint(sB + stage * b_tile_bytes(HALF_BN), &tmB,
-                                                  fb_leader, kb * BLK_K, nb, pol_b);
-                        }
-                    }
-                    if (ki == 0) trace_unit(p, ui, TRACE_U_LOAD_FIRST, globaltimer_ns());
-                    if (ki == u.kb1 - u.kb0 - 1)
-                        trace_unit(p, ui, TRACE_U_LOAD_LAST, globaltimer_ns());
-                    if (++stage == D) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                    if (!wd.aborted) {
-                        end_stage = stage;
-                        end_phase = phase;
-                    }
-                }
-                trace_unit(p, ui, TRACE_U_EMPTY_WAIT, empty_wait_ns);
-                ++ui;
-            }
-            if (wd.aborted) {
-                // Let copies already in flight land before the CTA can exit:
-                // the leader drains the phases it armed, the peer waits one
-                // budget-bounded grace period (its copies signal the leader).
-                if (leader) {
-                    int st = end_stage;
-                    uint32_t ph = end_phase;
-                    for (int i = 0; i < D && i < armed; ++i) {
-                        if (st == 0) {
-                            st = D - 1;
-                            ph ^= 1u;
-                        } else {
-                            --st;
-                        }
-                        wd.drain(bar_addr(bars, BAR_FULL + st), ph);
-                    }
-                } else {
-                    const uint64_t t0 = globaltimer_ns();
-                    while (globaltimer_ns() - t0 < 200000ull) {
-                    }
-                }
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        if (lane == 0 && leader) {
-            // ------------------------------------------- MMA issuer (leader)
-            constexpr uint32_t idesc = idesc_f16_f32(PAIR_BM, PAIR_BN);
-            int stage = 0;
-            uint32_t phase = 0;
-            int acc = 0;
-            uint32_t acc_phase = 0;
-            int mui = 0;
-            WorkIter units = units0;
-            WorkUnit u;
-            while (units.next(u)) {
-                const int t = u.tile;
-                wd.wait(bar_addr(bars, BAR_TMEM_EMPTY + acc), acc_phase ^ 1u, WAIT_TMEM_EMPTY,
-                        t, -1);
-                tc_fence_after_sync();
-                trace_unit(p, mui, TRACE_U_ACC_FREE, globaltimer_ns());
-                unsigned long long full_wait_ns = 0;
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PAIR_BN);
-                for (int ki = 0; ki < u.kb1 - u.kb0; ++ki) {
-                    const int kb = kblock_at(ki, mui, u.kb0, u.kb1, p.k_snake);
-                    const unsigned long long tw0 = p.trace ? globaltimer_ns() : 0ull;
-                    wd.wait(bar_addr(bars, BAR_FULL + stage), phase, WAIT_FULL, t, kb);
-                    if (p.trace) full_wait_ns += globaltimer_ns() - tw0;
-                    if (!wd.aborted) {
-                        tc_fence_after_sync();
-                        if (ki == 0) trace_unit(p, mui, TRACE_U_MMA_FIRST, globaltimer_ns());
-                        const uint64_t adesc = sw128_kmajor_desc(sA + stage * A_TILE_BYTES);
-                        const uint64_t bdesc =
-                            sw128_kmajor_desc(sB + stage * b_tile_bytes(HALF_BN));
-#pragma unroll
-                        for (int kk = 0; kk < BLK_K / MMA_K; ++kk)
-                            mma_f16_ss_pair(d_tmem, adesc + static_cast<uint64_t>(kk * 2),
-                                            bdesc + static_cast<uint64_t>(kk * 2), idesc,
-                                            (ki == 0 && kk == 0) ? 0u : 1u);
-                        // frees stage `stage` in both CTAs once these MMAs have read it
-                        mma_commit_pair_multicast(bar_addr(bars, BAR_EMPTY + stage), 0x3);
-                    }
-                    if (++stage == D) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!wd.aborted) mma_commit_pair_multicast(bar_addr(bars, BAR_TMEM_FULL + acc), 0x3);
-                trace_unit(p, mui, TRACE_U_MMA_LAST, globaltimer_ns());
-                trace_unit(p, mui, TRACE_U_FULL_WAIT, full_wait_ns);
-                ++mui;
-                acc ^= 1;
-                if (acc == 0) acc_phase ^= 1u;
-            }
-            // every pair MMA has completed before TMEM is released
-            mma_commit_pair_multicast(bar_addr(bars, BAR_DRAIN), 0x1);
-            wd.drain(bar_addr(bars, BAR_DRAIN), 0);
-        }
-        __syncwarp();
-    } else {
-        // -------------------------------------------------------- epilogue
-        const int q = warp & 3;
-        const bool issuer = (tid == 2 * 32);
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        uint32_t sub_count = 0;
-        WorkIter units = units0;
-        WorkUnit u;
-        volatile uint32_t* ticket_smem =
-            reinterpret_cast<volatile uint32_t*>(sm.gen + L.bars + TICKET_SLOT_OFFSET);
-        int eui = 0;
-        while (units.next(u)) {
-            const int t = u.tile;
-            int mt, nt;
-            raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
-            const int m0 = mt * PAIR_BM + static_cast<int>(rank) * BLK_M;
-            wd.wait(bar_addr(bars, BAR_TMEM_FULL + acc), acc_phase, WAIT_TMEM_FULL, t, -1);
-            tc_fence_after_sync();
-            if (issuer) trace_unit(p, eui, TRACE_U_EPI_START, globaltimer_ns());
-            const uint32_t tmem_acc = tmem_base + static_cast<uint32_t>(acc * PAIR_BN);
-            const uint32_t empty_leader =
-                map_shared_rank(bar_addr(bars, BAR_TMEM_EMPTY + acc), 0);
-            auto release = [&] {
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(empty_leader);
-            };
-            if (u.ncontrib == 1) {
-                epilogue_tma_store<PAIR_BN, F16OUT>(tmem_acc, q, lane, issuer, staging, &tmC, m0,
-                                                    nt * PAIR_BN, p.N, sub_count,
-                                                    PAIR_EPI_BAR_ID, !wd.aborted && m0 < p.M,
-                                                    p.C, p.M);
-                release();
-            } else {
-                // each CTA fixes up its own 128 rows of the pair tile
-                const size_t slot_elems = static_cast<size_t>(BLK_M) * PAIR_BN;
-                float* slot0 = p.sk_partials +
-                               (static_cast<size_t>(u.sk_index) * p.sk_max_contrib * 2 + rank) *
-                                   slot_elems;
-                sk_epilogue<PAIR_BN, F16OUT>(tmem_acc, q, lane, issuer, staging, &tmC, m0,
-                                             nt * PAIR_BN, p.M, p.N, sub_count, PAIR_EPI_BAR_ID,
-                                             wd.aborted, slot0, 2 * slot_elems, u.contrib,
-                                             u.ncontrib, p.sk_tickets + u.sk_index * 2 + rank,
-                                             p.epoch, ticket_smem, release, p.C);
-            }
-            if (issuer) trace_unit(p, eui, TRACE_U_EPI_END, globaltimer_ns());
-            ++eui;
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1u;
-        }
-        if (issuer) bulk_wait_group<0>();
-        if (issuer) trace_header(p, TRACE_H_UNITS, static_cast<unsigned long long>(eui));
-        __syncwarp();
-    }
-
-    // nothing of either CTA is touched remotely after this point
-    tc_fence_before_sync();
-    cluster_sync_all();
-    if (tid == 0) trace_header(p, TRACE_H_END, globaltimer_ns());
-    if (warp == 1) {
-        tc_fence_after_sync();
-        tmem_dealloc_pair(tmem_base, TMEM_COLS);
-    }
-}
-
-namespace {
-
-template <typename KernelT>
-cudaError_t launch_pair_kernel(KernelT kernel, const LaunchSpec& s, cudaStream_t stream)
-{
-    cudaError_t e = ensure_smem_limit(kernel, s.smem_bytes);
-    if (e != cudaSuccess) return e;
-    kernel<<<s.grid, PAIR_THREADS, s.smem_bytes, stream>>>(*s.tmA, *s.tmB, *s.tmC, s.p);
-    return cudaGetLastError();
-}
-
-}  // namespace
-
 cudaError_t launch_pair(const LaunchSpec& s, cudaStream_t stream)
 {
-    if (s.variant != VAR_PERSISTENT_2CTA || (s.grid & 1)) return cudaErrorInvalidValue;
-    if (s.f16out) {
-        switch (s.block_n) {
-        case 128: return launch_pair_kernel(k_ws2<128, true>, s, stream);
-        case 160: return launch_pair_kernel(k_ws2<160, true>, s, stream);
-        case 192: return launch_pair_kernel(k_ws2<192, true>, s, stream);
-        case 224: return launch_pair_kernel(k_ws2<224, true>, s, stream);
-        case 256: return launch_pair_kernel(k_ws2<256, true>, s, stream);
-        default: return cudaErrorInvalidValue;
-        }
-    }
-    switch (s.block_n) {
-    case 128: return launch_pair_kernel(k_ws2<128, false>, s, stream);
-    case 160: return launch_pair_kernel(k_ws2<160, false>, s, stream);
-    case 192: return launch_pair_kernel(k_ws2<192, false>, s, stream);
-    case 224: return launch_pair_kernel(k_ws2<224, false>, s, stream);
-    case 256: return launch_pair_kernel(k_ws2<256, false>, s, stream);
-    default: return cudaErrorInvalidValue;
-    }
+    if (s.grid & 1) return cudaErrorInvalidValue;
+    if (s.variant == VAR_DYNAMIC_2CTA) return launch_pair_dynamic(s, stream);
+    if (s.variant != VAR_PERSISTENT_2CTA) return cudaErrorInvalidValue;
+    return launch_pair_width<false>(s, stream);
 }
 
 }  // namespace tg

@@ -17,7 +17,8 @@ enum : int {
     VAR_WS_PIPELINED = 4,
     VAR_PERSISTENT = 5,
     VAR_PERSISTENT_LOCKSTEP = 6,
-    VAR_PERSISTENT_2CTA = 7
+    VAR_PERSISTENT_2CTA = 7,
+    VAR_DYNAMIC_2CTA = 8
 };
 
 struct LaunchSpec {
@@ -40,8 +41,10 @@ cudaError_t launch_ladder(const LaunchSpec& s, cudaStream_t stream);
 // Warp-specialised variants: VAR_WS_PIPELINED, VAR_PERSISTENT.
 cudaError_t launch_ws(const LaunchSpec& s, cudaStream_t stream);
 
-// Warp-specialised persistent GEMM on CTA pairs: VAR_PERSISTENT_2CTA.
+// Warp-specialised GEMM on CTA pairs: VAR_PERSISTENT_2CTA (static schedule)
+// and VAR_DYNAMIC_2CTA (cluster launch control, via launch_pair_dynamic).
 cudaError_t launch_pair(const LaunchSpec& s, cudaStream_t stream);
+cudaError_t launch_pair_dynamic(const LaunchSpec& s, cudaStream_t stream);
 
 // Raise `kernel`'s dynamic shared-memory limit to at least `bytes`, calling
 // the runtime only when a larger limit than any set before for that kernel is

@@ -376,4 +376,43 @@ __device__ __forceinline__ void mma_commit_pair_multicast(uint32_t bar, uint16_t
         : "memory");
 }
 
+// ------------------------------------------------- cluster launch control
+// (PTX ISA: clusterlaunchcontrol.try_cancel / query_cancel, sm_100 and later.)
+
+// Ask the hardware to cancel one cluster of this grid that has not started
+// yet.  The opaque 16-byte response lands at local shared offset `resp` in
+// every CTA of the calling cluster, and each CTA's mbarrier at local offset
+// `bar` receives 16 bytes of complete_tx.  After a response that reports no
+// cancellation, no further request may be issued.
+__device__ __forceinline__ void clc_try_cancel_multicast(uint32_t resp, uint32_t bar)
+{
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
+        ".multicast::cluster::all.b128 [%0], [%1];" ::"r"(resp),
+        "r"(bar)
+        : "memory");
+}
+
+// Decode a response: true if a cluster was cancelled, with the x index of its
+// first CTA in `cta_x` (left unset otherwise).
+__device__ __forceinline__ bool clc_decode(uint32_t resp, uint32_t& cta_x)
+{
+    uint32_t ok, x;
+    asm volatile(
+        "{\n\t"
+        ".reg .b128 r;\n\t"
+        ".reg .pred p;\n\t"
+        "ld.shared.b128 r, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "mov.u32 %1, 0;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t"
+        "}\n"
+        : "=r"(ok), "=r"(x)
+        : "r"(resp)
+        : "memory");
+    if (ok) cta_x = x;
+    return ok != 0;
+}
+
 }  // namespace tg

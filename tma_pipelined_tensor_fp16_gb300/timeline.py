@@ -61,14 +61,21 @@ def record(M, N, K, out, dist, seed, warmup=5, units=64, **opts):
     return tr, cfg
 
 
+def ran(tr):
+    """Indices of the CTAs that ran: under the dynamic schedule most CTAs of
+    the grid are cancelled before they start and leave their records zero."""
+    return [b for b in range(tr.shape[0]) if int(tr[b, 0, H_START]) != 0]
+
+
 def summarize(tr, cfg):
     import numpy as np
-    grid = tr.shape[0]
-    t0 = int(tr[:, 0, H_START].min())
+    live = ran(tr)
+    grid = len(live)
+    t0 = int(tr[live, 0, H_START].min())
     rel = lambda x: (int(x) - t0) / 1000.0  # us
     ctas = []
     units_all = []
-    for b in range(grid):
+    for b in live:
         h = tr[b, 0]
         n = int(h[H_UNITS])
         us = tr[b, 1:1 + min(n, tr.shape[1] - 1)]
@@ -108,6 +115,7 @@ def summarize(tr, cfg):
     return {
         "plan": {k: cfg[k] for k in ("variant", "block_m", "block_n", "pipe_depth", "grid",
                                      "num_tiles", "k_blocks", "sk_tiles")},
+        "ctas_ran": grid,
         "span_us": span,
         "cta_busy_fraction": busy,
         "cta_end_us": {"min": ends[0], "median": ends[len(ends) // 2], "max": ends[-1]},
@@ -119,7 +127,7 @@ def summarize(tr, cfg):
         "unit_mma_full_wait_us": stats("mma_full_wait", units_all),
         "producer_empty_wait_us_per_unit": stats("empty_wait", [
             {"empty_wait": int(u[U_EMPTY_WAIT]) / 1000.0}
-            for b in range(tr.shape[0]) for u in tr[b, 1:1 + min(int(tr[b, 0, H_UNITS]),
+            for b in live for u in tr[b, 1:1 + min(int(tr[b, 0, H_UNITS]),
                                                                   tr.shape[1] - 1)]
             if u[U_LOAD_FIRST]]),
         "unit_mma_gap_us": stats("mma_gap", units_all),
@@ -131,8 +139,9 @@ def summarize(tr, cfg):
 
 
 def gantt(tr, ctas_to_show, width=120):
-    t0 = int(tr[:, 0, 0].min())
-    t1 = int(tr[:, 0, 1].max())
+    live = ran(tr)
+    t0 = int(tr[live, 0, 0].min())
+    t1 = int(tr[live, 0, 1].max())
     scale = (t1 - t0) / width
     lines = []
     for b in ctas_to_show:
@@ -176,8 +185,9 @@ def main(argv=None):
     s["workload"] = cfg["name"]
     print(json.dumps(s, indent=1))
     if a.gantt:
-        step = max(1, pcfg["grid"] // a.gantt)
-        print(gantt(tr, list(range(0, pcfg["grid"], step))[:a.gantt]))
+        live = ran(tr)
+        step = max(1, len(live) // a.gantt)
+        print(gantt(tr, live[::step][:a.gantt]))
     if a.json:
         with open(a.json, "w") as f:
             json.dump(s, f, indent=1)
