@@ -31,8 +31,8 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["csrc/ptx.cuh", "csrc/gemm_common.h", "csrc/device_common.cuh",
-                  "csrc/kernel_ws.cu", "csrc/kernel_ws2.cu", "csrc/kernels_ladder.cu",
-                  "csrc/api.cu"]
+                  "csrc/kernel_ws.cu", "csrc/kernel_ws2.cuh", "csrc/kernel_ws2.cu",
+                  "csrc/kernel_ws2_dyn.cu", "csrc/kernels_ladder.cu", "csrc/api.cu"]
 
 
 def kernel_source_hash():
@@ -389,6 +389,8 @@ def main():
     out_tag = "f16" if cfg["out"] == "f16" else "f32"
     if pcfg["variant"] == 7:
         kernel_key = "k_ws2<%s>" % out_tag
+    elif pcfg["variant"] == 8:
+        kernel_key = "k_ws2<%s,dynamic>" % out_tag
     else:
         kernel_key = "k_ws<%d,%s,%s>" % (pcfg["block_n"], out_tag,
                                           "persistent" if pcfg["variant"] == 5 else

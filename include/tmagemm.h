@@ -53,9 +53,12 @@ typedef enum {
 /* Kernel variants: the ablation ladder of "GEMM II -- pipelining with TMA"
  * (Steps 3-6) plus the warp-specialised forms. */
 typedef enum {
-    GEMM_VAR_AUTO = 0,              /* GEMM_VAR_PERSISTENT_2CTA when M > 128 and there
-                                       are at least (SM count / 2) 256x128 tiles,
-                                       else GEMM_VAR_PERSISTENT */
+    GEMM_VAR_AUTO = 0,              /* CTA pairs when M > 128 and there are at
+                                       least (SM count / 2) 256x128 tiles --
+                                       GEMM_VAR_DYNAMIC_2CTA, or
+                                       GEMM_VAR_PERSISTENT_2CTA when the options
+                                       set grid or stream_k = 2 -- else
+                                       GEMM_VAR_PERSISTENT */
     GEMM_VAR_SYNC_TILED = 1,        /* Step 3: thread copies, one MMA at a time */
     GEMM_VAR_TMA_SERIAL = 2,        /* Step 4: TMA load + expect_tx, serial loop */
     GEMM_VAR_PIPELINED = 3,         /* Step 5: PIPE_DEPTH ring, lock-step prefetch */

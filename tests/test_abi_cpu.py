@@ -88,19 +88,23 @@ def test_depth_that_does_not_fit_is_rejected(b):
 def test_headline_configuration(b):
     st, c = b.gemm_select_config(8192, 8192, 8192, 1)
     assert st == 0
-    assert c.variant == b.GEMM_VAR_PERSISTENT_2CTA
+    assert c.variant == b.GEMM_VAR_DYNAMIC_2CTA
     assert (c.block_m, c.block_n, c.block_k) == (256, 256, 64)
-    assert c.pipe_depth == 6 and c.grid == 152 and c.threads == 192
+    assert c.pipe_depth == 6 and c.grid == 2048 and c.threads == 192
     assert c.num_tiles == 1024 and c.k_blocks == 128 and c.tmem_cols == 512
     assert c.tx_bytes == 2 * (128 * 64 + 128 * 64) * 2  # both CTAs' A and half-B tiles
+    # a grid size or stream-K keeps the static pair schedule
+    for o in ({"grid": 152}, {"stream_k": "on"}):
+        st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(**o))
+        assert st == 0 and c.variant == b.GEMM_VAR_PERSISTENT_2CTA and c.grid == 152
     st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(variant="persistent"))
     assert st == 0 and (c.block_m, c.block_n, c.pipe_depth, c.num_tiles) == (128, 256, 4, 2048)
 
 
 @pytest.mark.parametrize("M,N,K,dt,variant,bn", [(256, 256, 256, 0, 5, 64),
-                                                 (4096, 4096, 4096, 1, 7, 224),
-                                                 (8192, 8192, 8192, 1, 7, 256),
-                                                 (4000, 3000, 5000, 0, 7, 224),
+                                                 (4096, 4096, 4096, 1, 8, 224),
+                                                 (8192, 8192, 8192, 1, 8, 256),
+                                                 (4000, 3000, 5000, 0, 8, 224),
                                                  (64, 16384, 16384, 1, 5, 128),
                                                  (128, 65536, 64, 1, 5, 256)])
 def test_auto_variant_choice(b, M, N, K, dt, variant, bn):

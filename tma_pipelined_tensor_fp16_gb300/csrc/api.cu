@@ -171,13 +171,17 @@ int choose_pair_bn(int64_t M, int64_t N, int sms, int dtype)
 
 // Default kernel: CTA pairs (256-row tiles, cta_group::2) when M spans more
 // than one 128-row tile and there are enough pair tiles (at the narrowest
-// width, 128) to occupy every TPC;
-// otherwise single-CTA persistent tiles, whose narrower widths keep more SMs
-// busy on small or skinny problems.
-int auto_variant(int64_t M, int64_t N, int sms)
+// width, 128) to occupy every TPC; otherwise single-CTA persistent tiles,
+// whose narrower widths keep more SMs busy on small or skinny problems.
+// Pairs take the dynamic schedule (cluster launch control) unless the options
+// ask for something only the static one has (a grid size, stream-K): measured
+// on GB300 it runs each tile about 5 % faster at 8192^3 (the clusters no
+// longer start every tile in lock-step) and gives bit-identical results.
+int auto_variant(int64_t M, int64_t N, int sms, const gemm_options& opts)
 {
     const int64_t pair_tiles = ceil_div(M, 2 * BLK_M) * ceil_div(N, 128);
-    if (M > BLK_M && pair_tiles >= sms / 2) return VAR_PERSISTENT_2CTA;
+    if (M > BLK_M && pair_tiles >= sms / 2)
+        return (opts.grid == 0 && opts.stream_k != 2) ? VAR_DYNAMIC_2CTA : VAR_PERSISTENT_2CTA;
     return VAR_PERSISTENT;
 }
 
@@ -218,7 +222,7 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
         return fail(GEMM_ERR_INVALID_ARG, "k_order must be 0 (auto), 1 (ascending) or 2 (snake)");
     if (sms < 1 || smem_optin < 1) return fail(GEMM_ERR_INVALID_ARG, "bad device limits");
 
-    const int variant = opts.variant == VAR_AUTO ? auto_variant(M, N, sms) : opts.variant;
+    const int variant = opts.variant == VAR_AUTO ? auto_variant(M, N, sms, opts) : opts.variant;
     if (opts.debug_stall && !is_ws(variant))
         return fail(GEMM_ERR_INVALID_ARG, "debug_stall needs a warp-specialised variant");
     if (variant == VAR_DYNAMIC_2CTA && opts.grid != 0)
