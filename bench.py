@@ -265,6 +265,7 @@ def main():
     ap.add_argument("--variant", default="auto")
     ap.add_argument("--depth", type=int, default=0)
     ap.add_argument("--block-n", type=int, default=0)
+    ap.add_argument("--block-k", type=int, default=0, choices=[0, 64, 128])
     ap.add_argument("--group-m", type=int, default=0)
     ap.add_argument("--stream-k", default="auto", choices=["auto", "off", "on"])
     ap.add_argument("--k-order", default="auto", choices=["auto", "up", "snake"])
@@ -310,7 +311,7 @@ def main():
     dC = torch.empty((M, N), dtype=out_dt, device="cuda")
     plan = pkg.Plan(M, N, K, out=cfg["out"], variant=args.variant, pipe_depth=args.depth,
                     block_n=args.block_n, group_m=args.group_m, stream_k=args.stream_k,
-                    k_order=args.k_order)
+                    k_order=args.k_order, block_k=args.block_k)
     stream = torch.cuda.Stream()
     sh = stream.cuda_stream
 
@@ -387,10 +388,9 @@ def main():
     peaks, peak_kind = load_peaks()
     memory_bound = cfg["name"].startswith("gemm_skinny")
     out_tag = "f16" if cfg["out"] == "f16" else "f32"
-    if pcfg["variant"] == 7:
-        kernel_key = "k_ws2<%s>" % out_tag
-    elif pcfg["variant"] == 8:
-        kernel_key = "k_ws2<%s,dynamic>" % out_tag
+    if pcfg["variant"] in (7, 8):
+        kernel_key = "k_ws2<%s%s%s>" % (out_tag, ",dynamic" if pcfg["variant"] == 8 else "",
+                                        ",k128" if pcfg["block_k"] == 128 else "")
     else:
         kernel_key = "k_ws<%d,%s,%s>" % (pcfg["block_n"], out_tag,
                                           "persistent" if pcfg["variant"] == 5 else

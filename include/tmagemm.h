@@ -118,6 +118,17 @@ typedef struct {
                            the A slices its predecessor (the previous wave of
                            the same raster group) used last and that are still
                            in L2 */
+    int block_k;        /* K extent of one pipeline stage: 64 = one 128-byte
+                           swizzle atom (64 fp16); 128 = two atoms per stage
+                           ("05 Async Data Movement - TMA", Using 3D TMA to Move
+                           Multiple Swizzle Atoms), loaded as two boxes and
+                           consumed by 8 MMAs behind one barrier round trip
+                           (CTA-pair variants only, not with stream_k = 2;
+                           pipe_depth then counts 128-wide stages).  A second
+                           block past K arrives zero-filled and is skipped.
+                           0 = auto: 128 for the CTA-pair variants when K is a
+                           multiple of 64 (128-byte aligned operand rows) and
+                           neither stream_k = 2 nor pipe_depth is set, else 64 */
 } gemm_options;
 
 /* Resolved configuration of a plan (also returned by gemm_select_config). */

@@ -89,10 +89,14 @@ def test_headline_configuration(b):
     st, c = b.gemm_select_config(8192, 8192, 8192, 1)
     assert st == 0
     assert c.variant == b.GEMM_VAR_DYNAMIC_2CTA
-    assert (c.block_m, c.block_n, c.block_k) == (256, 256, 64)
-    assert c.pipe_depth == 6 and c.grid == 2048 and c.threads == 192
+    assert (c.block_m, c.block_n, c.block_k) == (256, 256, 128)
+    assert c.pipe_depth == 3 and c.grid == 2048 and c.threads == 192
     assert c.num_tiles == 1024 and c.k_blocks == 128 and c.tmem_cols == 512
-    assert c.tx_bytes == 2 * (128 * 64 + 128 * 64) * 2  # both CTAs' A and half-B tiles
+    # both CTAs' A and half-B tiles, two 64-wide K blocks each
+    assert c.tx_bytes == 2 * 2 * (128 * 64 + 128 * 64) * 2
+    # an explicit ring depth keeps stages of one 64-wide block
+    st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(pipe_depth=6))
+    assert st == 0 and (c.block_k, c.pipe_depth) == (64, 6)
     # a grid size or stream-K keeps the static pair schedule
     for o in ({"grid": 152}, {"stream_k": "on"}):
         st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(**o))
@@ -120,7 +124,8 @@ def test_pair_variant_constraints(b):
         assert (st == 0) == ok, (bn, dt)
         if ok:
             assert c.block_n == bn and c.block_m == 256
-            assert c.tx_bytes == 2 * (128 * 64 + (bn // 2) * 64) * 2
+            ks = c.block_k // 64  # K blocks of 64 per stage (auto: 2)
+            assert c.tx_bytes == 2 * ks * (128 * 64 + (bn // 2) * 64) * 2
             assert c.tmem_cols >= 2 * bn and c.tmem_cols & (c.tmem_cols - 1) == 0
     st, c = b.gemm_select_config(1024, 1024, 64, 1, b.make_options(variant="persistent_2cta",
                                                                     grid=7))
@@ -139,7 +144,7 @@ def test_dynamic_pair_configuration(b):
     st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(variant="dynamic_2cta"))
     assert st == 0, b.last_error()
     assert c.variant == b.GEMM_VAR_DYNAMIC_2CTA
-    assert (c.block_m, c.block_n, c.pipe_depth, c.threads, c.tmem_cols) == (256, 256, 6, 192, 512)
+    assert (c.block_m, c.block_n, c.pipe_depth, c.threads, c.tmem_cols) == (256, 256, 3, 192, 512)
     assert c.grid == 2 * c.num_tiles == 2048
     assert (c.dp_tiles, c.sk_tiles, c.workspace_bytes) == (1024, 0, 0)
     assert c.smem_bytes <= 232448
@@ -160,6 +165,35 @@ def test_dynamic_pair_configuration(b):
     assert st == 0
     for w in range(c.grid // 2):
         assert b.gemm_worker_units(c, w) == [(w, 0, c.k_blocks, 0, 1)]
+
+
+def test_block_k_128_stages(b):
+    # a stage of K = 128 as two 128-byte swizzle groups of 64 fp16 ("05 Async
+    # Data Movement - TMA", Using 3D TMA to Move Multiple Swizzle Atoms): twice
+    # the bytes per barrier phase, half as many stages fit
+    for v in ("persistent_2cta", "dynamic_2cta"):
+        st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(variant=v, block_k=128))
+        assert st == 0, b.last_error()
+        assert (c.block_k, c.pipe_depth, c.k_blocks) == (128, 3, 128)
+        assert c.tx_bytes == 2 * 2 * (128 * 64 + 128 * 64) * 2
+        assert c.smem_bytes <= 232448
+    st, _ = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(
+        variant="persistent_2cta", block_k=128, pipe_depth=4))
+    assert st == b.GEMM_ERR_UNSUPPORTED and "does not fit" in b.last_error()
+    st, _ = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(variant="persistent",
+                                                                     block_k=128))
+    assert st == b.GEMM_ERR_INVALID_ARG
+    st, _ = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(block_k=96))
+    assert st == b.GEMM_ERR_INVALID_ARG
+    st, _ = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(
+        variant="persistent_2cta", block_k=128, stream_k="on"))
+    assert st == b.GEMM_ERR_UNSUPPORTED
+    st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(block_k=64))
+    assert st == 0 and c.block_k == 64 and c.pipe_depth == 6
+    # automatic: 128-wide stages only over 128-byte aligned rows (K % 64 == 0)
+    for K, bk in [(4992, 128), (5056, 128), (5000, 64), (5064, 64)]:
+        st, c = b.gemm_select_config(4000, 3000, K, 0)
+        assert st == 0 and c.block_k == bk, K
 
 
 def test_stage_byte_count_matches_page_formula(b):

@@ -44,20 +44,21 @@ def test_dynamic_small_shapes(out, shape):
     assert np.isnan(guard.astype(np.float32)).all(), "wrote past the end of C"
 
 
+@pytest.mark.parametrize("bk", [64, 128])
 @pytest.mark.parametrize("out,bn", [("f32", 128), ("f32", 160), ("f32", 192), ("f32", 224),
                                     ("f32", 256), ("f16", 128), ("f16", 160), ("f16", 192),
                                     ("f16", 224), ("f16", 256)])
-def test_dynamic_tile_widths(out, bn):
+def test_dynamic_tile_widths(out, bn, bk):
     # 80 to 160 tiles: more than the 76 clusters that fit at once, so most
     # tiles are taken over by cancellation; ragged in every dimension
     M, N, K = 5000, 1000, 136
     A, B = inputs.make_operands(M, N, K, "normal", 1900 + bn)
-    got, guard, desc = run(A, B, out, guard_rows=2, variant=V, block_n=bn)
-    assert "x%d" % bn in desc, desc
+    got, guard, desc = run(A, B, out, guard_rows=2, variant=V, block_n=bn, block_k=bk)
+    assert "x%dx%d" % (bn, bk) in desc, desc
     assert_close(got, oracle.gemm(A, B), K, out, desc)
     assert np.isnan(guard.astype(np.float32)).all()
     Ai, Bi = inputs.make_operands(M, N, K, "int", 15)
-    goti, _, _ = run(Ai, Bi, out, variant=V, block_n=bn)
+    goti, _, _ = run(Ai, Bi, out, variant=V, block_n=bn, block_k=bk)
     assert_exact(goti, oracle.gemm(Ai, Bi), out, desc)
 
 

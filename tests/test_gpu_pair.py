@@ -3,7 +3,9 @@ tcgen05.mma.cta_group::2, 256 x 256 pair tiles) against the CPU oracle.
 
 Covers pair tiles whose second CTA is partly or wholly past the last row,
 ragged N and K, every depth 1..6 against short K loops, many tiles per pair,
-integer inputs bit-exact and the five workload shapes at full size.
+integer inputs bit-exact and the five workload shapes at full size; and
+stages of K = 128 (block_k = 128, two 64-wide swizzle groups per stage) under
+both tile schedules.
 """
 import numpy as np
 import pytest
@@ -26,14 +28,15 @@ def _built():
     __graft_entry__.build()
 
 
+@pytest.mark.parametrize("bk", [0, 64])
 @pytest.mark.parametrize("out", ["f32", "f16"])
 @pytest.mark.parametrize("shape", [(1, 8, 8), (100, 256, 64), (129, 136, 200), (256, 256, 256),
                                    (300, 520, 328), (640, 776, 456)],
                          ids=lambda s: "x".join(map(str, s)))
-def test_pair_small_shapes(out, shape):
+def test_pair_small_shapes(out, shape, bk):
     M, N, K = shape
     A, B = inputs.make_operands(M, N, K, "uniform", 300 + M + N + K)
-    got, guard, desc = run(A, B, out, guard_rows=3, variant=V)
+    got, guard, desc = run(A, B, out, guard_rows=3, variant=V, block_k=bk)
     assert_close(got, oracle.gemm(A, B), K, out, desc)
     assert np.isnan(guard.astype(np.float32)).all(), "wrote past the end of C"
 
@@ -55,20 +58,21 @@ def test_pair_many_tiles_per_cluster(grid):
     assert_close(got, oracle.gemm(A, B), K, "f16", desc)
 
 
+@pytest.mark.parametrize("bk", [64, 128])
 @pytest.mark.parametrize("out,bn", [("f32", 128), ("f32", 160), ("f32", 192), ("f32", 224),
                                     ("f32", 256), ("f16", 128), ("f16", 160), ("f16", 192),
                                     ("f16", 224), ("f16", 256)])
-def test_pair_tile_widths(out, bn):
+def test_pair_tile_widths(out, bn, bk):
     # ragged in every dimension, several tiles per pair and a second CTA whose
     # rows run past M in the last tile row
     M, N, K = 700, 1000, 456
     A, B = inputs.make_operands(M, N, K, "normal", 900 + bn)
-    got, guard, desc = run(A, B, out, guard_rows=2, variant=V, block_n=bn, grid=8)
-    assert "x%d" % bn in desc, desc
+    got, guard, desc = run(A, B, out, guard_rows=2, variant=V, block_n=bn, grid=8, block_k=bk)
+    assert "x%dx%d" % (bn, bk) in desc, desc
     assert_close(got, oracle.gemm(A, B), K, out, desc)
     assert np.isnan(guard.astype(np.float32)).all()
     Ai, Bi = inputs.make_operands(M, N, K, "int", 5)
-    goti, _, _ = run(Ai, Bi, out, variant=V, block_n=bn, grid=8)
+    goti, _, _ = run(Ai, Bi, out, variant=V, block_n=bn, grid=8, block_k=bk)
     assert_exact(goti, oracle.gemm(Ai, Bi), out, desc)
 
 
@@ -117,3 +121,35 @@ def test_pair_watchdog_timeout():
     plan.close()
     got, _, desc = run(A, B, "f32", variant=V)
     assert_close(got, oracle.gemm(A, B), K, "f32", "after timeout: " + desc)
+
+
+@pytest.mark.parametrize("variant", ["persistent_2cta", "dynamic_2cta"])
+@pytest.mark.parametrize("out", ["f32", "f16"])
+@pytest.mark.parametrize("K", [8, 136, 520, 1032])
+def test_pair_block_k_128(variant, out, K):
+    # stages of K = 128 as two 64-wide swizzle groups; an odd number of 64-wide
+    # K blocks leaves the second group of the last stage past K (zero-filled,
+    # its MMAs skipped)
+    M, N = 1100, 1000
+    A, B = inputs.make_operands(M, N, K, "normal", 4100 + K)
+    for depth in (0, 1, 2):
+        got, guard, desc = run(A, B, out, guard_rows=2, variant=variant, block_k=128,
+                               pipe_depth=depth)
+        assert desc.split("tile=")[1].split()[0].endswith("x128"), desc
+        assert_close(got, oracle.gemm(A, B), K, out, desc)
+        assert np.isnan(guard.astype(np.float32)).all()
+    Ai, Bi = inputs.make_operands(M, N, K, "int", 41)
+    goti, _, desc = run(Ai, Bi, out, variant=variant, block_k=128)
+    assert_exact(goti, oracle.gemm(Ai, Bi), out, desc)
+
+
+@pytest.mark.parametrize("cfg", [c for c in inputs.CONFIGS if c["M"] > 128],
+                         ids=[c["name"] for c in inputs.CONFIGS if c["M"] > 128])
+def test_pair_block_k_128_workloads(cfg):
+    M, N, K, out = cfg["M"], cfg["N"], cfg["K"], cfg["out"]
+    A, B = inputs.make_operands(M, N, K, cfg["dist"], cfg["seed"])
+    got, _, desc = run(A, B, out, variant="dynamic_2cta", block_k=128)
+    stat, _, _ = run(A, B, out, variant="persistent_2cta", block_k=128)
+    assert np.array_equal(got.view(np.uint8), stat.view(np.uint8)), desc
+    rows, cols = _sample(M, N, 2000, cfg["seed"] + 7)
+    assert_close(got[rows, cols], oracle.gemm_entries(A, B, rows, cols), K, out, desc)

@@ -34,7 +34,7 @@ VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 class gemm_options(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("variant", "pipe_depth", "block_n", "group_m", "grid", "wait_budget_ms",
-                 "debug_stall", "stream_k", "l2_policy", "k_order")]
+                 "debug_stall", "stream_k", "l2_policy", "k_order", "block_k")]
 
 
 class gemm_config(ctypes.Structure):
@@ -116,12 +116,12 @@ K_ORDER = {"auto": 0, "up": 1, "snake": 2}
 
 
 def make_options(variant="auto", pipe_depth=0, block_n=0, group_m=0, grid=0, wait_budget_ms=0,
-                 debug_stall=0, stream_k="auto", l2_policy=0, k_order="auto"):
+                 debug_stall=0, stream_k="auto", l2_policy=0, k_order="auto", block_k=0):
     v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
     sk = STREAM_K[stream_k] if isinstance(stream_k, str) else int(stream_k)
     ko = K_ORDER[k_order] if isinstance(k_order, str) else int(k_order)
     return gemm_options(v, pipe_depth, block_n, group_m, grid, wait_budget_ms, debug_stall, sk,
-                        l2_policy, ko)
+                        l2_policy, ko, block_k)
 
 
 # ---- the C entry points under their own names ------------------------------

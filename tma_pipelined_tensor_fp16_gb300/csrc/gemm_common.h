@@ -111,6 +111,10 @@ struct Params {
     // odd.  With snake_span equal to the static schedule's cluster count,
     // every tile walks K in the same direction under both schedules.
     int snake_span;
+    // K blocks of 64 per pipeline stage in the CTA-pair kernel: 1, or 2 (a
+    // stage of K = 128 as two 128-byte swizzle atoms, one barrier round trip
+    // per 8 MMAs).  The single-CTA kernels use 1.
+    int ksub;
 };
 
 // The i-th K block (i = 0, 1, ...) processed for work unit number `unit` of a

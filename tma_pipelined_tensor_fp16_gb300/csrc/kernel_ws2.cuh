@@ -165,7 +165,7 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t x)
 
 // PAIR_BN: output columns per pair tile (a multiple of 32 up to 256; each CTA
 // holds PAIR_BN / 2 rows of B per stage).
-template <int PAIR_BN, bool F16OUT, bool DYN>
+template <int PAIR_BN, bool F16OUT, bool DYN, int KS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
     k_ws2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
           const __grid_constant__ CUtensorMap tmC, const Params p)
@@ -179,7 +179,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
     constexpr uint32_t TMEM_COLS = pow2_at_least(ACC * PAIR_BN);
     const int D = p.pipe_depth;
     const CtaSmem sm = cta_smem();
-    const SmemLayout L = smem_layout(D, HALF_BN, NUM_STAGING);
+    // A stage holds KS K blocks of 64, each in a sub-slot of its own (sub-slot
+    // stage * KS + s).  KS = 2 is the K = 128 stage of "05 Async Data Movement
+    // - TMA" (Using 3D TMA to Move Multiple Swizzle Atoms): the 128-wide slice
+    // is split into two 64-wide groups, each a 128-byte swizzle row.  The page
+    // writes both groups with one 3-D copy; here each group is its own 2-D box,
+    // which lands the same bytes and keeps the zero fill past a ragged K edge
+    // (a 3-D view of a row-major matrix would read the next row there).
+    static_assert(KS == 1 || KS == 2, "K blocks of 64 per stage");
+    const SmemLayout L = smem_layout(D * KS, HALF_BN, NUM_STAGING);
     const uint32_t sA = sm.base + L.a;
     const uint32_t sB = sm.base + L.b;
     const uint32_t staging = sm.base + L.staging;
@@ -193,7 +201,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
     Watchdog wd = make_watchdog(p);
     const int pair = static_cast<int>(blockIdx.x >> 1);
     const int npairs = static_cast<int>(gridDim.x >> 1);
-    const int KB = p.k_blocks;
+    const int KB = (p.k_blocks + KS - 1) / KS;  // stages per tile
     PairTiles<DYN> tiles0;
     tiles0.it.init(pair, npairs, p.dp_tiles, p.sk_tiles, KB, p.sk_kb_per_worker);
     tiles0.own = pair;
@@ -244,7 +252,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            const uint32_t pair_tx = 2u * stage_tx_bytes(HALF_BN);  // both CTAs' A and B
+            // both CTAs' A and B, all KS blocks (a block past K arrives zero-filled)
+            const uint32_t pair_tx = 2u * stage_tx_bytes(HALF_BN) * static_cast<uint32_t>(KS);
             const uint64_t pol_a = (p.l2_policy == 2) ? policy_evict_first() : policy_evict_last();
             const uint64_t pol_b = (p.l2_policy == 1) ? policy_evict_first() : policy_evict_last();
             if (p.debug_stall) wd.wait(bar_addr(bars, BAR_STALL), 0, WAIT_STALL, -1, -1);
@@ -295,16 +304,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                             mbar_arrive_expect_tx(fb_local, pair_tx);
                             ++armed;
                         }
-                        if (p.l2_policy == 0) {
-                            tma_load_2d_pair(sA + stage * A_TILE_BYTES, &tmA, fb_leader,
-                                             kb * BLK_K, m0);
-                            tma_load_2d_pair(sB + stage * b_tile_bytes(HALF_BN), &tmB, fb_leader,
-                                             kb * BLK_K, nb);
-                        } else {
-                            tma_load_2d_pair_hint(sA + stage * A_TILE_BYTES, &tmA, fb_leader,
-                                                  kb * BLK_K, m0, pol_a);
-                            tma_load_2d_pair_hint(sB + stage * b_tile_bytes(HALF_BN), &tmB,
-                                                  fb_leader, kb * BLK_K, nb, pol_b);
+#pragma unroll
+                        for (int s = 0; s < KS; ++s) {
+                            const int slot = stage * KS + s;
+                            const int kx = (kb * KS + s) * BLK_K;
+                            if (p.l2_policy == 0) {
+                                tma_load_2d_pair(sA + slot * A_TILE_BYTES, &tmA, fb_leader, kx,
+                                                 m0);
+                                tma_load_2d_pair(sB + slot * b_tile_bytes(HALF_BN), &tmB,
+                                                 fb_leader, kx, nb);
+                            } else {
+                                tma_load_2d_pair_hint(sA + slot * A_TILE_BYTES, &tmA, fb_leader,
+                                                      kx, m0, pol_a);
+                                tma_load_2d_pair_hint(sB + slot * b_tile_bytes(HALF_BN), &tmB,
+                                                      fb_leader, kx, nb, pol_b);
+                            }
                         }
                     }
                     if (ki == 0) trace_unit(p, ui, TRACE_U_LOAD_FIRST, globaltimer_ns());
@@ -382,14 +396,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                     if (!wd.aborted) {
                         tc_fence_after_sync();
                         if (ki == 0) trace_unit(p, mui, TRACE_U_MMA_FIRST, globaltimer_ns());
-                        const uint64_t adesc = sw128_kmajor_desc(sA + stage * A_TILE_BYTES);
-                        const uint64_t bdesc =
-                            sw128_kmajor_desc(sB + stage * b_tile_bytes(HALF_BN));
 #pragma unroll
-                        for (int kk = 0; kk < BLK_K / MMA_K; ++kk)
-                            mma_f16_ss_pair(d_tmem, adesc + static_cast<uint64_t>(kk * 2),
-                                            bdesc + static_cast<uint64_t>(kk * 2), idesc,
-                                            (ki == 0 && kk == 0) ? 0u : 1u);
+                        for (int s = 0; s < KS; ++s) {
+                            // the second block of the last stage may lie past K
+                            if (s > 0 && kb * KS + s >= p.k_blocks) break;
+                            const int slot = stage * KS + s;
+                            const uint64_t adesc = sw128_kmajor_desc(sA + slot * A_TILE_BYTES);
+                            const uint64_t bdesc =
+                                sw128_kmajor_desc(sB + slot * b_tile_bytes(HALF_BN));
+#pragma unroll
+                            for (int kk = 0; kk < BLK_K / MMA_K; ++kk)
+                                mma_f16_ss_pair(d_tmem, adesc + static_cast<uint64_t>(kk * 2),
+                                                bdesc + static_cast<uint64_t>(kk * 2), idesc,
+                                                (ki == 0 && s == 0 && kk == 0) ? 0u : 1u);
+                        }
                         // frees stage `stage` in both CTAs once these MMAs have read it
                         mma_commit_pair_multicast(bar_addr(bars, BAR_EMPTY + stage), 0x3);
                     }
@@ -485,28 +505,36 @@ cudaError_t launch_pair_kernel(KernelT kernel, const LaunchSpec& s, cudaStream_t
     return cudaGetLastError();
 }
 
-// Launch k_ws2<block_n, f16out, DYN> for one of the built pair tile widths.
-template <bool DYN>
+// Launch k_ws2<block_n, f16out, DYN, KS> for one of the built pair tile
+// widths.  Each (DYN, KS) pair is instantiated by a translation unit of its
+// own (kernel_ws2.cu, kernel_ws2_k2.cu, kernel_ws2_dyn.cu,
+// kernel_ws2_dyn_k2.cu), so that the four compile in parallel.
+template <bool DYN, int KS>
 cudaError_t launch_pair_width(const LaunchSpec& s, cudaStream_t stream)
 {
     if (s.f16out) {
         switch (s.block_n) {
-        case 128: return launch_pair_kernel(k_ws2<128, true, DYN>, s, stream);
-        case 160: return launch_pair_kernel(k_ws2<160, true, DYN>, s, stream);
-        case 192: return launch_pair_kernel(k_ws2<192, true, DYN>, s, stream);
-        case 224: return launch_pair_kernel(k_ws2<224, true, DYN>, s, stream);
-        case 256: return launch_pair_kernel(k_ws2<256, true, DYN>, s, stream);
+        case 128: return launch_pair_kernel(k_ws2<128, true, DYN, KS>, s, stream);
+        case 160: return launch_pair_kernel(k_ws2<160, true, DYN, KS>, s, stream);
+        case 192: return launch_pair_kernel(k_ws2<192, true, DYN, KS>, s, stream);
+        case 224: return launch_pair_kernel(k_ws2<224, true, DYN, KS>, s, stream);
+        case 256: return launch_pair_kernel(k_ws2<256, true, DYN, KS>, s, stream);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (s.block_n) {
-    case 128: return launch_pair_kernel(k_ws2<128, false, DYN>, s, stream);
-    case 160: return launch_pair_kernel(k_ws2<160, false, DYN>, s, stream);
-    case 192: return launch_pair_kernel(k_ws2<192, false, DYN>, s, stream);
-    case 224: return launch_pair_kernel(k_ws2<224, false, DYN>, s, stream);
-    case 256: return launch_pair_kernel(k_ws2<256, false, DYN>, s, stream);
+    case 128: return launch_pair_kernel(k_ws2<128, false, DYN, KS>, s, stream);
+    case 160: return launch_pair_kernel(k_ws2<160, false, DYN, KS>, s, stream);
+    case 192: return launch_pair_kernel(k_ws2<192, false, DYN, KS>, s, stream);
+    case 224: return launch_pair_kernel(k_ws2<224, false, DYN, KS>, s, stream);
+    case 256: return launch_pair_kernel(k_ws2<256, false, DYN, KS>, s, stream);
     default: return cudaErrorInvalidValue;
     }
 }
+
+extern template cudaError_t launch_pair_width<false, 1>(const LaunchSpec&, cudaStream_t);
+extern template cudaError_t launch_pair_width<false, 2>(const LaunchSpec&, cudaStream_t);
+extern template cudaError_t launch_pair_width<true, 1>(const LaunchSpec&, cudaStream_t);
+extern template cudaError_t launch_pair_width<true, 2>(const LaunchSpec&, cudaStream_t);
 
 }  // namespace tg

@@ -42,9 +42,9 @@ cudaError_t launch_ladder(const LaunchSpec& s, cudaStream_t stream);
 cudaError_t launch_ws(const LaunchSpec& s, cudaStream_t stream);
 
 // Warp-specialised GEMM on CTA pairs: VAR_PERSISTENT_2CTA (static schedule)
-// and VAR_DYNAMIC_2CTA (cluster launch control, via launch_pair_dynamic).
+// and VAR_DYNAMIC_2CTA (cluster launch control), with stages of p.ksub K
+// blocks of 64.
 cudaError_t launch_pair(const LaunchSpec& s, cudaStream_t stream);
-cudaError_t launch_pair_dynamic(const LaunchSpec& s, cudaStream_t stream);
 
 // Raise `kernel`'s dynamic shared-memory limit to at least `bytes`, calling
 // the runtime only when a larger limit than any set before for that kernel is

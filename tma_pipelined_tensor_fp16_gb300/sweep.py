@@ -34,6 +34,7 @@ def main(argv=None):
     ap.add_argument("--group-m", default="0", help="comma list of raster group heights")
     ap.add_argument("--l2-policy", default="0", help="comma list of L2 load policies 0..3")
     ap.add_argument("--k-order", default="auto", help="comma list of auto,up,snake")
+    ap.add_argument("--block-k", default="0", help="comma list of stage K extents 0,64,128")
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--cooldown", type=float, default=0.0,
                     help="seconds of idle GPU before each configuration's timing")
@@ -64,17 +65,19 @@ def main(argv=None):
             depths = [int(x) for x in a.depths.split(",")]
             if variant in ("sync_tiled", "tma_serial"):
                 depths = [1]
-            for d, sk, gm, l2, ko in [(d, sk, gm, l2, ko) for d in depths
-                                      for sk in a.stream_k.split(",")
-                                      for gm in [int(x) for x in a.group_m.split(",")]
-                                      for l2 in [int(x) for x in a.l2_policy.split(",")]
-                                      for ko in a.k_order.split(",")]:
+            for d, sk, gm, l2, ko, bk in [(d, sk, gm, l2, ko, bk) for d in depths
+                                          for sk in a.stream_k.split(",")
+                                          for gm in [int(x) for x in a.group_m.split(",")]
+                                          for l2 in [int(x) for x in a.l2_policy.split(",")]
+                                          for ko in a.k_order.split(",")
+                                          for bk in [int(x) for x in a.block_k.split(",")]]:
                 rec = {"workload": cfg["name"], "variant": variant, "block_n": bn, "depth": d,
-                       "stream_k": sk, "group_m": gm, "l2_policy": l2, "k_order": ko}
+                       "stream_k": sk, "group_m": gm, "l2_policy": l2, "k_order": ko,
+                       "block_k": bk}
                 try:
                     plan = binding.Plan(M, N, K, out=cfg["out"], variant=variant, block_n=bn,
                                         pipe_depth=d, stream_k=sk, group_m=gm, l2_policy=l2,
-                                        k_order=ko)
+                                        k_order=ko, block_k=bk)
                 except binding.GemmError as e:
                     rec["error"] = str(e)
                     _emit(rec, sink)
