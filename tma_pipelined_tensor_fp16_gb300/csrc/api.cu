@@ -145,12 +145,16 @@ bool pair_width_ok(int bn, int dtype)
 // Pair tile width for an automatic plan: the fraction of launched tile slots
 // that do useful columns (waves over the SM pairs, and the last tile column's
 // overhang past N), weighted by the throughput of one tile of each width
-// relative to 256 columns, measured on GB300 (narrower tiles move more operand
-// bytes from L2 per FLOP, and the main loop is bound by operand arrival).
-int choose_pair_bn(int64_t M, int64_t N, int sms, int dtype)
+// relative to 256 columns, measured on GB300 at 8192^3 and 4096^3 with the
+// wave and overhang losses divided out (narrower tiles issue more barrier
+// round trips and load more operand bytes per FLOP).  Stages of two K blocks
+// (ksub = 2) halve the round trips, and narrow tiles lose less.
+int choose_pair_bn(int64_t M, int64_t N, int sms, int dtype, int ksub)
 {
     const int widths[5] = {256, 224, 192, 160, 128};
-    const double tile_eff[5] = {1.0, 0.92, 0.79, 0.73, 0.54};
+    const double eff_k64[5] = {1.0, 0.92, 0.79, 0.73, 0.54};
+    const double eff_k128[5] = {1.0, 0.94, 0.89, 0.81, 0.70};
+    const double* tile_eff = ksub == 2 ? eff_k128 : eff_k64;
     const int64_t pairs = sms / 2;
     const int64_t tm = ceil_div(M, 2 * BLK_M);
     int best = 256;
@@ -252,7 +256,7 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
         return fail(GEMM_ERR_INVALID_ARG,
                     "CTA-pair tile width (block_n) must be 128, 160, 192, 224 or 256");
     const int bn = opts.block_n   ? opts.block_n
-                   : is_pair(variant) ? choose_pair_bn(M, N, sms, dtype)
+                   : is_pair(variant) ? choose_pair_bn(M, N, sms, dtype, ksub)
                                       : choose_block_n(variant, M, N, sms);
     // Shared memory per CTA holds B tiles of `bn_cta` rows: a CTA of a pair
     // keeps half of the pair tile's B rows.
@@ -404,6 +408,14 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
 // 2-D tensor map over a row-major matrix with `rows` rows of `cols` elements
 // (row pitch `pitch_bytes`), box = box_cols x box_rows, 128-byte swizzle,
 // out-of-bounds elements read as zero.
+//
+// L2 promotion: 256 bytes when every row starts on a 256-byte boundary (a box
+// row of 128 bytes then sits in one 256-byte block, and the promotion brings
+// in the row's next K block, which the next stage reads); 128 bytes when rows
+// start off such a boundary (there a 256-byte promotion fetches bytes of
+// neighbouring blocks that no box asks for).  Measured on GB300: K = 8192
+// 1799 vs 1742 TFLOP/s with 256 over 128 bytes; K = 5000 (10,000-byte rows)
+// 1222 vs 1174 with 128 over 256 bytes.
 int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t cols,
               uint64_t rows, uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows,
               const char* what)
@@ -414,9 +426,14 @@ int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64
     const cuuint64_t strides[1] = {pitch_bytes};
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
+    const bool rows_on_256 =
+        pitch_bytes % 256 == 0 && reinterpret_cast<uintptr_t>(base) % 256 == 0;
+    const CUtensorMapL2promotion promo = rows_on_256
+                                             ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                             : CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
     CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         char buf[160];
         std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what,
