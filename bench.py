@@ -266,6 +266,9 @@ def main():
     ap.add_argument("--depth", type=int, default=0)
     ap.add_argument("--block-n", type=int, default=0)
     ap.add_argument("--block-k", type=int, default=0, choices=[0, 64, 128])
+    ap.add_argument("--l2-flush", action="store_true",
+                    help="cold L2: write a scratch buffer of twice the L2 size before every timed "
+                         "launch; the rate is then taken from the launches' own events")
     ap.add_argument("--group-m", type=int, default=0)
     ap.add_argument("--stream-k", default="auto", choices=["auto", "off", "on"])
     ap.add_argument("--k-order", default="auto", choices=["auto", "up", "snake"])
@@ -321,6 +324,10 @@ def main():
     if plan.device_status() != 0:
         raise SystemExit("warm-up failed: " + pkg.gemm_last_error())
 
+    scratch = None
+    if args.l2_flush:
+        l2 = torch.cuda.get_device_properties(local_rank).L2_cache_size
+        scratch = torch.empty(2 * l2 // 4, dtype=torch.int32, device="cuda")
     sampler = ClockSampler(local_rank)
     sampler.start()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -333,6 +340,8 @@ def main():
     with torch.cuda.stream(stream):
         t_start.record(stream)
         for i in range(args.steps):
+            if scratch is not None:
+                scratch.fill_(i)  # evicts A, B and C from L2 (outside the launch's events)
             ev[i][0].record(stream)
             plan.run(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), sh)
             ev[i][1].record(stream)
@@ -345,6 +354,10 @@ def main():
         raise SystemExit("timed run failed: " + pkg.gemm_last_error())
     total_ms = t_start.elapsed_time(t_end)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if scratch is not None:
+        # the timed region also holds the flushes: the step time is the
+        # launches' own time
+        total_ms = sum(launch_ms)
     total_ms = max_over_ranks(total_ms, dist, "cuda")
 
     flops, nbytes = algorithmic(cfg)
@@ -434,8 +447,10 @@ def main():
         "dtype": "f16 (fp32 accumulate)", "data": "synthetic",
         "config": {"workload": cfg["name"], "M": M, "N": N, "K": K, "out": cfg["out"],
                    "operands": "%s seed %d" % (cfg["dist"], cfg["seed"]),
-                   "l2": "no flush: A+B+C exceed the L2" if M * K * 2 + N * K * 2 > 130e6
-                   else "operands fit in L2 (warm)",
+                   "l2": ("flushed: a 2 x L2 scratch write before every launch (cold)"
+                          if args.l2_flush else
+                          "no flush: A+B+C exceed the L2" if M * K * 2 + N * K * 2 > 130e6
+                          else "operands fit in L2 (warm)"),
                    "plan": plan_desc},
         "roofline": roof,
         "cpu_baseline": cpu,
