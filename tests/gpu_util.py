@@ -87,3 +87,34 @@ def run(A_bits, B_bits, out, guard_rows=0, stream=None, **opts):
         c = host[:M].numpy()
         g = host[M:].numpy()
     return c, g, desc
+
+
+def run_repeated(A_bits, B_bits, out, reps, **opts):
+    """Launch ONE plan `reps` times on one stream, refilling C with NaN on that
+    stream before every launch; returns the list of outputs (numpy).  This is
+    how bench.py uses a plan: per-plan device state (run epoch, status word,
+    stream-K tickets, tile-schedule barriers) carries over between launches."""
+    import torch
+
+    import tma_pipelined_tensor_fp16_gb300 as pkg
+    M, K = A_bits.shape
+    N = B_bits.shape[0]
+    dA, dB = to_device(A_bits), to_device(B_bits)
+    dt = torch.float16 if out == "f16" else torch.float32
+    C = torch.empty((M, N), dtype=dt, device="cuda")
+    st = torch.cuda.Stream()
+    plan = pkg.Plan(M, N, K, out=out, **opts)
+    outs = []
+    try:
+        for _ in range(reps):
+            with torch.cuda.stream(st):
+                C.fill_(float("nan"))
+            plan(dA, dB, C, stream=st)
+            st.synchronize()
+            s = plan.device_status()
+            if s != 0:
+                raise AssertionError("device status %d: %s" % (s, pkg.gemm_last_error()))
+            outs.append(C.cpu().numpy())
+    finally:
+        plan.close()
+    return outs

@@ -17,7 +17,7 @@ import pytest
 import oracle
 from tma_pipelined_tensor_fp16_gb300 import inputs
 
-from gpu_util import assert_close, assert_exact, run
+from gpu_util import assert_close, assert_exact, run, run_repeated
 
 pytestmark = pytest.mark.gpu
 V = "dynamic_2cta"
@@ -128,3 +128,25 @@ def test_dynamic_watchdog_timeout():
     plan.close()
     got, _, desc = run(A, B, "f32", variant=V)
     assert_close(got, oracle.gemm(A, B), K, "f32", "after timeout: " + desc)
+
+
+@pytest.mark.parametrize("opts", [{"variant": "dynamic_2cta", "block_k": 64},
+                                  {"variant": "dynamic_2cta", "block_k": 128},
+                                  {"variant": "persistent_2cta", "block_k": 128},
+                                  {"variant": "persistent_2cta", "stream_k": "on"},
+                                  {"variant": "persistent"}],
+                         ids=["dyn64", "dyn128", "static128", "static_streamk", "single"])
+def test_same_plan_launched_repeatedly(opts):
+    # one plan, five launches on one stream (as the benchmark runs it): every
+    # launch writes every output and all five agree bit for bit; several waves
+    # of tiles, so most clusters of the dynamic grid are cancelled each time
+    M, N, K = 3072, 4096, 1024
+    A, B = inputs.make_operands(M, N, K, "uniform", 66)
+    outs = run_repeated(A, B, "f16", 5, **opts)
+    variant = opts["variant"]
+    ref = outs[0]
+    assert not np.isnan(ref.astype(np.float32)).any()
+    rows, cols = _sample(M, N, 2000, 66)
+    assert_close(ref[rows, cols], oracle.gemm_entries(A, B, rows, cols), K, "f16", variant)
+    for i, o in enumerate(outs[1:], 1):
+        assert np.array_equal(o.view(np.uint16), ref.view(np.uint16)), "launch %d differs" % i

@@ -7,11 +7,13 @@
 // Tma Pipeline Designer", Case 1: the consumer waits on tma2mma[stage], the
 // producer waits on mma2tma[stage] before overwriting).
 //
-//   warp 0, one lane   TMA producer: wait empty[s], arrive.expect_tx(full[s]),
-//                      two bulk tensor loads into stage s.
-//   warp 1, one lane   MMA issuer: wait full[s], four tcgen05.mma into the
-//                      TMEM accumulator, tcgen05.commit -> empty[s]; after the
-//                      last K block, commit -> tmem_full[acc].
+//   warp 0             TMA producer: the warp waits empty[s]; lane 0 issues
+//                      arrive.expect_tx(full[s]) and two bulk tensor loads
+//                      into stage s ("one elected thread" of the pages).
+//   warp 1             MMA issuer: the warp waits full[s]; lane 0 issues four
+//                      tcgen05.mma into the TMEM accumulator and
+//                      tcgen05.commit -> empty[s]; after the last K block,
+//                      commit -> tmem_full[acc].
 //   warps 2..5         epilogue: wait tmem_full[acc], TMEM -> regs -> swizzled
 //                      staging -> TMA store, arrive tmem_empty[acc].
 //
@@ -113,137 +115,146 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
         trace_header(p, TRACE_H_SMID, sm_id());
     }
 
+    // The producer and MMA roles run as whole warps: every lane walks the
+    // loop and waits on each barrier, lane 0 issues the copies or the MMAs,
+    // and the warp reconverges after every stage (a role run by lane 0 alone,
+    // the other lanes parked at a warp barrier, measured up to 9% slower).
     if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------ TMA producer
-            const uint32_t tx = stage_tx_bytes(BN, a_rows);
-            const uint64_t pol_a = (p.l2_policy == 2) ? policy_evict_first() : policy_evict_last();
-            const uint64_t pol_b = (p.l2_policy == 1) ? policy_evict_first() : policy_evict_last();
-            if (p.debug_stall) wd.wait(bar_addr(bars, BAR_STALL), 0, WAIT_STALL, -1, -1);
-            int stage = 0;
-            uint32_t phase = 0;
-            int issued = 0;
-            int end_stage = 0;       // ring position just after the last issued load
-            uint32_t end_phase = 0;
-            WorkIter units = units0;
-            WorkUnit u;
-            int ui = 0;
-            while (units.next(u)) {
-                const int t = u.tile;
+        // ---------------------------------------------------- TMA producer
+        const uint32_t tx = stage_tx_bytes(BN, a_rows);
+        const uint64_t pol_a = (p.l2_policy == 2) ? policy_evict_first() : policy_evict_last();
+        const uint64_t pol_b = (p.l2_policy == 1) ? policy_evict_first() : policy_evict_last();
+        const bool tr = p.trace && lane == 0;
+        if (p.debug_stall) wd.wait(bar_addr(bars, BAR_STALL), 0, WAIT_STALL, -1, -1);
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
+        int end_stage = 0;       // ring position just after the last issued load
+        uint32_t end_phase = 0;
+        WorkIter units = units0;
+        WorkUnit u;
+        int ui = 0;
+        while (units.next(u)) {
+            const int t = u.tile;
+            if (tr)
                 trace_unit(p, ui, TRACE_U_TILE,
                            (static_cast<unsigned long long>(t) << 32) |
                                static_cast<unsigned>(u.kb1 - u.kb0));
-                unsigned long long empty_wait_ns = 0;
-                int mt, nt;
-                raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
-                const int m0 = mt * BLK_M, n0 = nt * BN;
-                for (int ki = 0; ki < u.kb1 - u.kb0; ++ki) {
-                    const int kb = kblock_at(ki, ui, u.kb0, u.kb1, p.k_snake);
-                    // a fresh barrier passes a wait on parity 1 at once: the
-                    // first trip around the ring does not wait
-                    const unsigned long long tw0 = p.trace ? globaltimer_ns() : 0ull;
+            unsigned long long empty_wait_ns = 0;
+            int mt, nt;
+            raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
+            const int m0 = mt * BLK_M, n0 = nt * BN;
+            for (int ki = 0; ki < u.kb1 - u.kb0; ++ki) {
+                const int kb = kblock_at(ki, ui, u.kb0, u.kb1, p.k_snake);
+                // a fresh barrier passes a wait on parity 1 at once: the first
+                // trip around the ring does not wait
+                const unsigned long long tw0 = tr ? globaltimer_ns() : 0ull;
+                const bool ok =
                     wd.wait(bar_addr(bars, BAR_EMPTY + stage), phase ^ 1u, WAIT_EMPTY, t, kb);
-                    if (p.trace) empty_wait_ns += globaltimer_ns() - tw0;
-                    if (!wd.aborted) {
-                        const uint32_t fb = bar_addr(bars, BAR_FULL + stage);
-                        mbar_arrive_expect_tx(fb, tx);
-                        if (p.l2_policy == 0) {
-                            tma_load_2d(sA + stage * a_slot, &tmA, fb, kb * BLK_K, m0);
-                            tma_load_2d(sB + stage * b_tile_bytes(BN), &tmB, fb, kb * BLK_K, n0);
-                        } else {
-                            tma_load_2d_hint(sA + stage * a_slot, &tmA, fb, kb * BLK_K, m0,
-                                             pol_a);
-                            tma_load_2d_hint(sB + stage * b_tile_bytes(BN), &tmB, fb, kb * BLK_K,
-                                             n0, pol_b);
-                        }
-                        ++issued;
-                    }
-                    if (ki == 0) trace_unit(p, ui, TRACE_U_LOAD_FIRST, globaltimer_ns());
-                    if (ki == u.kb1 - u.kb0 - 1)
-                        trace_unit(p, ui, TRACE_U_LOAD_LAST, globaltimer_ns());
-                    if (++stage == D) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                    if (!wd.aborted) {
-                        end_stage = stage;
-                        end_phase = phase;
-                    }
-                }
-                trace_unit(p, ui, TRACE_U_EMPTY_WAIT, empty_wait_ns);
-                ++ui;
-            }
-            // drain: the last min(D, issued) loads have landed before exit
-            if (wd.aborted) {
-                int st = end_stage;
-                uint32_t ph = end_phase;
-                for (int i = 0; i < D && i < issued; ++i) {
-                    if (st == 0) {
-                        st = D - 1;
-                        ph ^= 1u;
+                if (tr) empty_wait_ns += globaltimer_ns() - tw0;
+                if (lane == 0 && ok) {
+                    const uint32_t fb = bar_addr(bars, BAR_FULL + stage);
+                    mbar_arrive_expect_tx(fb, tx);
+                    if (p.l2_policy == 0) {
+                        tma_load_2d(sA + stage * a_slot, &tmA, fb, kb * BLK_K, m0);
+                        tma_load_2d(sB + stage * b_tile_bytes(BN), &tmB, fb, kb * BLK_K, n0);
                     } else {
-                        --st;
+                        tma_load_2d_hint(sA + stage * a_slot, &tmA, fb, kb * BLK_K, m0, pol_a);
+                        tma_load_2d_hint(sB + stage * b_tile_bytes(BN), &tmB, fb, kb * BLK_K, n0,
+                                         pol_b);
                     }
-                    wd.drain(bar_addr(bars, BAR_FULL + st), ph);
+                    ++issued;
                 }
+                if (tr && ki == 0) trace_unit(p, ui, TRACE_U_LOAD_FIRST, globaltimer_ns());
+                if (tr && ki == u.kb1 - u.kb0 - 1)
+                    trace_unit(p, ui, TRACE_U_LOAD_LAST, globaltimer_ns());
+                __syncwarp();
+                if (++stage == D) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                if (!wd.aborted) {
+                    end_stage = stage;
+                    end_phase = phase;
+                }
+            }
+            if (tr) trace_unit(p, ui, TRACE_U_EMPTY_WAIT, empty_wait_ns);
+            ++ui;
+        }
+        // drain: the last min(D, issued) loads have landed before exit
+        if (lane == 0 && wd.aborted) {
+            int st = end_stage;
+            uint32_t ph = end_phase;
+            for (int i = 0; i < D && i < issued; ++i) {
+                if (st == 0) {
+                    st = D - 1;
+                    ph ^= 1u;
+                } else {
+                    --st;
+                }
+                wd.drain(bar_addr(bars, BAR_FULL + st), ph);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------- MMA issuer
-            constexpr uint32_t idesc = idesc_f16_f32(BLK_M, BN);
-            int stage = 0;
-            uint32_t phase = 0;
-            int acc = 0;
-            uint32_t acc_phase = 0;
-            int mui = 0;
-            WorkIter units = units0;
-            WorkUnit u;
-            while (units.next(u)) {
-                const int t = u.tile;
-                // the epilogue has drained this accumulator (fresh: passes)
-                wd.wait(bar_addr(bars, BAR_TMEM_EMPTY + acc), acc_phase ^ 1u, WAIT_TMEM_EMPTY,
-                        t, -1);
-                tc_fence_after_sync();
-                trace_unit(p, mui, TRACE_U_ACC_FREE, globaltimer_ns());
-                unsigned long long full_wait_ns = 0;
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int ki = 0; ki < u.kb1 - u.kb0; ++ki) {
-                    const int kb = kblock_at(ki, mui, u.kb0, u.kb1, p.k_snake);
-                    const unsigned long long tw0 = p.trace ? globaltimer_ns() : 0ull;
-                    wd.wait(bar_addr(bars, BAR_FULL + stage), phase, WAIT_FULL, t, kb);
-                    if (p.trace) full_wait_ns += globaltimer_ns() - tw0;
-                    if (!wd.aborted) {
-                        tc_fence_after_sync();
-                        if (ki == 0) trace_unit(p, mui, TRACE_U_MMA_FIRST, globaltimer_ns());
-                        const uint64_t adesc = sw128_kmajor_desc(sA + stage * a_slot);
-                        const uint64_t bdesc = sw128_kmajor_desc(sB + stage * b_tile_bytes(BN));
+        // --------------------------------------------------------- MMA issuer
+        constexpr uint32_t idesc = idesc_f16_f32(BLK_M, BN);
+        const bool tr = p.trace && lane == 0;
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        int mui = 0;
+        WorkIter units = units0;
+        WorkUnit u;
+        while (units.next(u)) {
+            const int t = u.tile;
+            // the epilogue has drained this accumulator (fresh: passes)
+            wd.wait(bar_addr(bars, BAR_TMEM_EMPTY + acc), acc_phase ^ 1u, WAIT_TMEM_EMPTY, t, -1);
+            tc_fence_after_sync();
+            if (tr) trace_unit(p, mui, TRACE_U_ACC_FREE, globaltimer_ns());
+            unsigned long long full_wait_ns = 0;
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+            for (int ki = 0; ki < u.kb1 - u.kb0; ++ki) {
+                const int kb = kblock_at(ki, mui, u.kb0, u.kb1, p.k_snake);
+                const unsigned long long tw0 = tr ? globaltimer_ns() : 0ull;
+                const bool ok = wd.wait(bar_addr(bars, BAR_FULL + stage), phase, WAIT_FULL, t, kb);
+                if (tr) full_wait_ns += globaltimer_ns() - tw0;
+                if (lane == 0 && ok) {
+                    tc_fence_after_sync();
+                    if (tr && ki == 0) trace_unit(p, mui, TRACE_U_MMA_FIRST, globaltimer_ns());
+                    const uint64_t adesc = sw128_kmajor_desc(sA + stage * a_slot);
+                    const uint64_t bdesc = sw128_kmajor_desc(sB + stage * b_tile_bytes(BN));
 #pragma unroll
-                        for (int kk = 0; kk < BLK_K / MMA_K; ++kk)
-                            mma_f16_ss(d_tmem, adesc + static_cast<uint64_t>(kk * 2),
-                                       bdesc + static_cast<uint64_t>(kk * 2), idesc,
-                                       (ki == 0 && kk == 0) ? 0u : 1u);
-                        // frees the stage once these MMAs have read it
-                        mma_commit(bar_addr(bars, BAR_EMPTY + stage));
-                    }
-                    if (++stage == D) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                    for (int kk = 0; kk < BLK_K / MMA_K; ++kk)
+                        mma_f16_ss(d_tmem, adesc + static_cast<uint64_t>(kk * 2),
+                                   bdesc + static_cast<uint64_t>(kk * 2), idesc,
+                                   (ki == 0 && kk == 0) ? 0u : 1u);
+                    // frees the stage once these MMAs have read it
+                    mma_commit(bar_addr(bars, BAR_EMPTY + stage));
                 }
-                if (!wd.aborted) mma_commit(bar_addr(bars, BAR_TMEM_FULL + acc));
-                trace_unit(p, mui, TRACE_U_MMA_LAST, globaltimer_ns());
-                trace_unit(p, mui, TRACE_U_FULL_WAIT, full_wait_ns);
-                ++mui;
-                if (ACC == 2) {
-                    acc ^= 1;
-                    if (acc == 0) acc_phase ^= 1u;
-                } else {
-                    acc_phase ^= 1u;
+                __syncwarp();
+                if (++stage == D) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
-            // every MMA has completed before TMEM is released
+            if (lane == 0 && !wd.aborted) mma_commit(bar_addr(bars, BAR_TMEM_FULL + acc));
+            if (tr) {
+                trace_unit(p, mui, TRACE_U_MMA_LAST, globaltimer_ns());
+                trace_unit(p, mui, TRACE_U_FULL_WAIT, full_wait_ns);
+            }
+            __syncwarp();
+            ++mui;
+            if (ACC == 2) {
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            } else {
+                acc_phase ^= 1u;
+            }
+        }
+        // every MMA has completed before TMEM is released
+        if (lane == 0) {
             mma_commit(bar_addr(bars, BAR_DRAIN));
             wd.drain(bar_addr(bars, BAR_DRAIN), 0);
         }

@@ -18,9 +18,10 @@
 // multicast to both CTAs' empty[s] / tmem_full[a] barriers; both CTAs'
 // epilogue warps arrive on the leader's tmem_empty[a].
 //
-// Roles per CTA (192 threads), as in kernel_ws.cu:
-//   warp 0 lane 0   TMA producer (both CTAs)
-//   warp 1 lane 0   MMA issuer (leader only); warp 1 of each CTA allocates TMEM
+// Roles per CTA (192 threads):
+//   warp 0          TMA producer (both CTAs): the warp waits, lane 0 copies
+//   warp 1          MMA issuer (leader only): the warp waits, lane 0 issues;
+//                   warp 1 of each CTA allocates TMEM
 //   warps 2..5      epilogue of this CTA's 128 rows of the pair tile
 // The ring position {stage, phase} and the accumulator position run on
 // continuously across tiles.
@@ -119,17 +120,17 @@ struct PairTiles {
         }
     }
 
-    // Next unit for a whole warp: lane 0 reads the response, the tile is
-    // broadcast to the other lanes.
+    // Next unit for a whole warp: lane 0 reads the response (re-arming the
+    // slot when `arm`), the tile is broadcast to the other lanes.
     __device__ __forceinline__ bool next_warp(WorkUnit& u, uint32_t bars, Watchdog& wd,
-                                              uint32_t lane)
+                                              uint32_t lane, bool arm = false)
     {
         if constexpr (!DYN) {
             return it.next(u);
         } else {
             int t = own;
             if (use >= 0) {
-                t = lane == 0 ? clc_read(bars, use, wd, false) : -1;
+                t = lane == 0 ? clc_read(bars, use, wd, arm) : -1;
                 t = __shfl_sync(0xffffffffu, t, 0);
             }
             ++use;
@@ -249,129 +250,137 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
         trace_header(p, TRACE_H_SMID, sm_id());
     }
 
+    // The producer and MMA roles run as whole warps: every lane walks the
+    // loop and waits on each barrier, lane 0 issues the copies or the MMAs,
+    // and the warp reconverges after every stage.  With the other 31 lanes
+    // parked at a warp barrier while lane 0 ran the main loop alone, the same
+    // kernel measured 9% slower at 8192^3 on GB300 (1693 vs 1852 TFLOP/s).
     if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------ TMA producer
-            // both CTAs' A and B, all KS blocks (a block past K arrives zero-filled)
-            const uint32_t pair_tx = 2u * stage_tx_bytes(HALF_BN) * static_cast<uint32_t>(KS);
-            const uint64_t pol_a = (p.l2_policy == 2) ? policy_evict_first() : policy_evict_last();
-            const uint64_t pol_b = (p.l2_policy == 1) ? policy_evict_first() : policy_evict_last();
-            if (p.debug_stall) wd.wait(bar_addr(bars, BAR_STALL), 0, WAIT_STALL, -1, -1);
-            int stage = 0;
-            uint32_t phase = 0;
-            int armed = 0;
-            int end_stage = 0;       // ring position just after the last armed stage
-            uint32_t end_phase = 0;
-            int requests = 0;        // dynamic schedule: cancellation requests issued
-            PairTiles<DYN> tiles = tiles0;
-            WorkUnit u;
-            int ui = 0;
-            while (tiles.next(u, bars, wd, true)) {
-                const int t = u.tile;
-                if constexpr (DYN) {
-                    // Ask for the tile after this one now; its response is
-                    // read when this tile's loads have all been issued.
-                    if (leader && !wd.aborted) {
-                        const int slot = requests % CLC_SLOTS;
-                        const uint32_t free_parity =
-                            (static_cast<uint32_t>(requests / CLC_SLOTS) & 1u) ^ 1u;
-                        if (wd.wait(bar_addr(bars, BAR_CLC_EMPTY + slot), free_parity,
-                                    WAIT_CLC_EMPTY, t, -1)) {
-                            clc_try_cancel_multicast(clc_resp(bars, slot),
-                                                     bar_addr(bars, BAR_CLC_FULL + slot));
-                            ++requests;
-                        }
+        // ---------------------------------------------------- TMA producer
+        // both CTAs' A and B, all KS blocks (a block past K arrives zero-filled)
+        const uint32_t pair_tx = 2u * stage_tx_bytes(HALF_BN) * static_cast<uint32_t>(KS);
+        const uint64_t pol_a = (p.l2_policy == 2) ? policy_evict_first() : policy_evict_last();
+        const uint64_t pol_b = (p.l2_policy == 1) ? policy_evict_first() : policy_evict_last();
+        const bool tr = p.trace && lane == 0;
+        if (p.debug_stall) wd.wait(bar_addr(bars, BAR_STALL), 0, WAIT_STALL, -1, -1);
+        int stage = 0;
+        uint32_t phase = 0;
+        int armed = 0;
+        int end_stage = 0;       // ring position just after the last armed stage
+        uint32_t end_phase = 0;
+        int requests = 0;        // dynamic schedule: cancellation requests issued
+        PairTiles<DYN> tiles = tiles0;
+        WorkUnit u;
+        int ui = 0;
+        while (tiles.next_warp(u, bars, wd, lane, true)) {
+            const int t = u.tile;
+            if constexpr (DYN) {
+                // Ask for the tile after this one now; its response is read
+                // when this tile's loads have all been issued.
+                if (leader && lane == 0 && !wd.aborted) {
+                    const int slot = requests % CLC_SLOTS;
+                    const uint32_t free_parity =
+                        (static_cast<uint32_t>(requests / CLC_SLOTS) & 1u) ^ 1u;
+                    if (wd.wait(bar_addr(bars, BAR_CLC_EMPTY + slot), free_parity,
+                                WAIT_CLC_EMPTY, t, -1)) {
+                        clc_try_cancel_multicast(clc_resp(bars, slot),
+                                                 bar_addr(bars, BAR_CLC_FULL + slot));
+                        ++requests;
                     }
                 }
+                __syncwarp();
+            }
+            if (tr)
                 trace_unit(p, ui, TRACE_U_TILE,
                            (static_cast<unsigned long long>(t) << 32) |
                                static_cast<unsigned>(u.kb1 - u.kb0));
-                unsigned long long empty_wait_ns = 0;
-                int mt, nt;
-                raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
-                const int m0 = mt * PAIR_BM + static_cast<int>(rank) * BLK_M;
-                const int nb = nt * PAIR_BN + static_cast<int>(rank) * HALF_BN;
-                for (int ki = 0; ki < u.kb1 - u.kb0; ++ki) {
-                    const int kb = kblock_at(ki, DYN ? t / p.snake_span : ui, u.kb0, u.kb1,
-                                             p.k_snake);
-                    const unsigned long long tw0 = p.trace ? globaltimer_ns() : 0ull;
+            unsigned long long empty_wait_ns = 0;
+            int mt, nt;
+            raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
+            const int m0 = mt * PAIR_BM + static_cast<int>(rank) * BLK_M;
+            const int nb = nt * PAIR_BN + static_cast<int>(rank) * HALF_BN;
+            for (int ki = 0; ki < u.kb1 - u.kb0; ++ki) {
+                const int kb = kblock_at(ki, DYN ? t / p.snake_span : ui, u.kb0, u.kb1,
+                                         p.k_snake);
+                const unsigned long long tw0 = tr ? globaltimer_ns() : 0ull;
+                const bool ok =
                     wd.wait(bar_addr(bars, BAR_EMPTY + stage), phase ^ 1u, WAIT_EMPTY, t, kb);
-                    if (p.trace) empty_wait_ns += globaltimer_ns() - tw0;
-                    if (!wd.aborted) {
-                        const uint32_t fb_local = bar_addr(bars, BAR_FULL + stage);
-                        const uint32_t fb_leader = map_shared_rank(fb_local, 0);
-                        if (leader) {
-                            mbar_arrive_expect_tx(fb_local, pair_tx);
-                            ++armed;
-                        }
+                if (tr) empty_wait_ns += globaltimer_ns() - tw0;
+                if (lane == 0 && ok) {
+                    const uint32_t fb_local = bar_addr(bars, BAR_FULL + stage);
+                    const uint32_t fb_leader = map_shared_rank(fb_local, 0);
+                    if (leader) {
+                        mbar_arrive_expect_tx(fb_local, pair_tx);
+                        ++armed;
+                    }
 #pragma unroll
-                        for (int s = 0; s < KS; ++s) {
-                            const int slot = stage * KS + s;
-                            const int kx = (kb * KS + s) * BLK_K;
-                            if (p.l2_policy == 0) {
-                                tma_load_2d_pair(sA + slot * A_TILE_BYTES, &tmA, fb_leader, kx,
-                                                 m0);
-                                tma_load_2d_pair(sB + slot * b_tile_bytes(HALF_BN), &tmB,
-                                                 fb_leader, kx, nb);
-                            } else {
-                                tma_load_2d_pair_hint(sA + slot * A_TILE_BYTES, &tmA, fb_leader,
-                                                      kx, m0, pol_a);
-                                tma_load_2d_pair_hint(sB + slot * b_tile_bytes(HALF_BN), &tmB,
-                                                      fb_leader, kx, nb, pol_b);
-                            }
+                    for (int s = 0; s < KS; ++s) {
+                        const int slot = stage * KS + s;
+                        const int kx = (kb * KS + s) * BLK_K;
+                        if (p.l2_policy == 0) {
+                            tma_load_2d_pair(sA + slot * A_TILE_BYTES, &tmA, fb_leader, kx, m0);
+                            tma_load_2d_pair(sB + slot * b_tile_bytes(HALF_BN), &tmB, fb_leader,
+                                             kx, nb);
+                        } else {
+                            tma_load_2d_pair_hint(sA + slot * A_TILE_BYTES, &tmA, fb_leader, kx,
+                                                  m0, pol_a);
+                            tma_load_2d_pair_hint(sB + slot * b_tile_bytes(HALF_BN), &tmB,
+                                                  fb_leader, kx, nb, pol_b);
                         }
-                    }
-                    if (ki == 0) trace_unit(p, ui, TRACE_U_LOAD_FIRST, globaltimer_ns());
-                    if (ki == u.kb1 - u.kb0 - 1)
-                        trace_unit(p, ui, TRACE_U_LOAD_LAST, globaltimer_ns());
-                    if (++stage == D) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                    if (!wd.aborted) {
-                        end_stage = stage;
-                        end_phase = phase;
                     }
                 }
-                trace_unit(p, ui, TRACE_U_EMPTY_WAIT, empty_wait_ns);
-                ++ui;
+                if (tr && ki == 0) trace_unit(p, ui, TRACE_U_LOAD_FIRST, globaltimer_ns());
+                if (tr && ki == u.kb1 - u.kb0 - 1)
+                    trace_unit(p, ui, TRACE_U_LOAD_LAST, globaltimer_ns());
+                __syncwarp();
+                if (++stage == D) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                if (!wd.aborted) {
+                    end_stage = stage;
+                    end_phase = phase;
+                }
             }
-            if (wd.aborted) {
-                // Let copies already in flight land before the CTA can exit:
-                // the leader drains the phases it armed, the peer waits one
-                // budget-bounded grace period (its copies signal the leader).
-                if (leader) {
-                    int st = end_stage;
-                    uint32_t ph = end_phase;
-                    for (int i = 0; i < D && i < armed; ++i) {
-                        if (st == 0) {
-                            st = D - 1;
-                            ph ^= 1u;
-                        } else {
-                            --st;
-                        }
-                        wd.drain(bar_addr(bars, BAR_FULL + st), ph);
+            if (tr) trace_unit(p, ui, TRACE_U_EMPTY_WAIT, empty_wait_ns);
+            ++ui;
+        }
+        if (lane == 0 && wd.aborted) {
+            // Let copies already in flight land before the CTA can exit: the
+            // leader drains the phases it armed, the peer waits one
+            // budget-bounded grace period (its copies signal the leader).
+            if (leader) {
+                int st = end_stage;
+                uint32_t ph = end_phase;
+                for (int i = 0; i < D && i < armed; ++i) {
+                    if (st == 0) {
+                        st = D - 1;
+                        ph ^= 1u;
+                    } else {
+                        --st;
                     }
-                    if constexpr (DYN) {
-                        // the last cancellation request may still be in flight
-                        if (requests > 0) {
-                            const int r = requests - 1;
-                            wd.drain(bar_addr(bars, BAR_CLC_FULL + r % CLC_SLOTS),
-                                     static_cast<uint32_t>(r / CLC_SLOTS) & 1u);
-                        }
+                    wd.drain(bar_addr(bars, BAR_FULL + st), ph);
+                }
+                if constexpr (DYN) {
+                    // the last cancellation request may still be in flight
+                    if (requests > 0) {
+                        const int r = requests - 1;
+                        wd.drain(bar_addr(bars, BAR_CLC_FULL + r % CLC_SLOTS),
+                                 static_cast<uint32_t>(r / CLC_SLOTS) & 1u);
                     }
-                } else {
-                    const uint64_t t0 = globaltimer_ns();
-                    while (globaltimer_ns() - t0 < 200000ull) {
-                    }
+                }
+            } else {
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 200000ull) {
                 }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0 && leader) {
-            // ------------------------------------------- MMA issuer (leader)
+        if (leader) {
+            // ----------------------------------------------- MMA issuer (leader)
             constexpr uint32_t idesc = idesc_f16_f32(PAIR_BM, PAIR_BN);
+            const bool tr = p.trace && lane == 0;
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -379,23 +388,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
             int mui = 0;
             PairTiles<DYN> tiles = tiles0;
             WorkUnit u;
-            while (tiles.next(u, bars, wd, false)) {
+            while (tiles.next_warp(u, bars, wd, lane)) {
                 const int t = u.tile;
                 wd.wait(bar_addr(bars, BAR_TMEM_EMPTY + acc), acc_phase ^ 1u, WAIT_TMEM_EMPTY,
                         t, -1);
                 tc_fence_after_sync();
-                trace_unit(p, mui, TRACE_U_ACC_FREE, globaltimer_ns());
+                if (tr) trace_unit(p, mui, TRACE_U_ACC_FREE, globaltimer_ns());
                 unsigned long long full_wait_ns = 0;
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PAIR_BN);
                 for (int ki = 0; ki < u.kb1 - u.kb0; ++ki) {
                     const int kb = kblock_at(ki, DYN ? t / p.snake_span : mui, u.kb0, u.kb1,
                                              p.k_snake);
-                    const unsigned long long tw0 = p.trace ? globaltimer_ns() : 0ull;
-                    wd.wait(bar_addr(bars, BAR_FULL + stage), phase, WAIT_FULL, t, kb);
-                    if (p.trace) full_wait_ns += globaltimer_ns() - tw0;
-                    if (!wd.aborted) {
+                    const unsigned long long tw0 = tr ? globaltimer_ns() : 0ull;
+                    const bool ok =
+                        wd.wait(bar_addr(bars, BAR_FULL + stage), phase, WAIT_FULL, t, kb);
+                    if (tr) full_wait_ns += globaltimer_ns() - tw0;
+                    if (lane == 0 && ok) {
                         tc_fence_after_sync();
-                        if (ki == 0) trace_unit(p, mui, TRACE_U_MMA_FIRST, globaltimer_ns());
+                        if (tr && ki == 0) trace_unit(p, mui, TRACE_U_MMA_FIRST, globaltimer_ns());
 #pragma unroll
                         for (int s = 0; s < KS; ++s) {
                             // the second block of the last stage may lie past K
@@ -413,21 +423,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                         // frees stage `stage` in both CTAs once these MMAs have read it
                         mma_commit_pair_multicast(bar_addr(bars, BAR_EMPTY + stage), 0x3);
                     }
+                    __syncwarp();
                     if (++stage == D) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                if (!wd.aborted) mma_commit_pair_multicast(bar_addr(bars, BAR_TMEM_FULL + acc), 0x3);
-                trace_unit(p, mui, TRACE_U_MMA_LAST, globaltimer_ns());
-                trace_unit(p, mui, TRACE_U_FULL_WAIT, full_wait_ns);
+                if (lane == 0 && !wd.aborted)
+                    mma_commit_pair_multicast(bar_addr(bars, BAR_TMEM_FULL + acc), 0x3);
+                if (tr) {
+                    trace_unit(p, mui, TRACE_U_MMA_LAST, globaltimer_ns());
+                    trace_unit(p, mui, TRACE_U_FULL_WAIT, full_wait_ns);
+                }
+                __syncwarp();
                 ++mui;
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
             // every pair MMA has completed before TMEM is released
-            mma_commit_pair_multicast(bar_addr(bars, BAR_DRAIN), 0x1);
-            wd.drain(bar_addr(bars, BAR_DRAIN), 0);
+            if (lane == 0) {
+                mma_commit_pair_multicast(bar_addr(bars, BAR_DRAIN), 0x1);
+                wd.drain(bar_addr(bars, BAR_DRAIN), 0);
+            }
         }
         __syncwarp();
     } else {
