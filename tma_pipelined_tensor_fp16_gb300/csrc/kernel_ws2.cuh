@@ -93,7 +93,11 @@ __device__ __forceinline__ int clc_read(uint32_t bars, int use, Watchdog& wd, bo
     uint32_t cta_x = 0;
     const bool cancelled = clc_decode(clc_resp(bars, slot), cta_x);
     if (arm) mbar_arrive_expect_tx(full, CLC_RESP_BYTES);
-    mbar_arrive_cluster(map_shared_rank(bar_addr(bars, BAR_CLC_EMPTY + slot), 0));
+    // Relaxed: the slot's only access here is the load just decoded, whose
+    // value this thread has already consumed.  A release fence would also
+    // wait for the MMA issuer's queued tensor-core work at every tile start
+    // (measured 1.1 us per tile of drained MMA pipe at 8192^3).
+    mbar_arrive_cluster_relaxed(map_shared_rank(bar_addr(bars, BAR_CLC_EMPTY + slot), 0));
     return cancelled ? static_cast<int>(cta_x >> 1) : -1;
 }
 

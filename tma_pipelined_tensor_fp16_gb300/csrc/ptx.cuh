@@ -307,6 +307,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar)
                  : "memory");
 }
 
+// The same arrival with relaxed ordering: no fence before it.  Used where the
+// only access to protect is a load whose value the thread has already
+// consumed (in-order issue puts the arrival after that load has returned).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+                 : "memory");
+}
+
 // 2-D tile load into this CTA's shared memory whose completion bytes are
 // signalled to an mbarrier that may live in the peer CTA of the pair
 // (`cluster_bar` is a cluster-window address).
