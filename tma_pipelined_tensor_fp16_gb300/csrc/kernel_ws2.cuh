@@ -1,15 +1,16 @@
 // kernel_ws2.cuh -- the persistent, warp-specialised GEMM on CTA pairs: a
-// cluster of two CTAs on the two SMs of a TPC computes one 256 x 256 output
-// tile with tcgen05.mma.cta_group::2 issued by the pair's leader.
-// kernel_ws2.cu instantiates it with the static persistent schedule,
-// kernel_ws2_dyn.cu with the dynamic one (cluster launch control).
+// cluster of two CTAs on the two SMs of a TPC computes one 256 x PAIR_BN
+// output tile with tcgen05.mma.cta_group::2 issued by the pair's leader.
+// Template flags: DYN (tile schedule, below) and KS (K blocks of 64 per
+// pipeline stage: 1, or 2 for stages of K = 128).  Each (DYN, KS) pair is
+// instantiated by a translation unit of its own: kernel_ws2.cu,
+// kernel_ws2_k2.cu, kernel_ws2_dyn.cu, kernel_ws2_dyn_k2.cu.
 //
 // Why pairs: with one CTA per tile the 128 x 256 tile leaves room for only
-// four 48 KB stages beside the output staging, and the main loop is latency
-// bound at that depth (the PIPE_DEPTH sweep: 906 / 1441 / 1625 TFLOP/s at depth
-// 2 / 3 / 4 on 8192^3).  In a pair each CTA keeps its own 128 rows of A and
-// half of B (128 rows) per stage -- 32 KB -- so six stages fit, and every byte
-// of B fetched from L2 now feeds 256 rows of A instead of 128.
+// four 48 KB stages beside the output staging.  In a pair each CTA keeps its
+// own 128 rows of A and half of B (128 rows) per 64-wide K block -- 32 KB --
+// so six such stages fit (or three of K = 128), and every byte of B fetched
+// from L2 feeds 256 rows of A instead of 128.
 //
 // No TMA multicast is used: each CTA loads its own tiles into its own shared
 // memory.  Both CTAs' copies signal the LEADER's full[s] barrier (the
