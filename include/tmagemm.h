@@ -262,7 +262,9 @@ TMAGEMM_API int64_t gemm_sw128_offset(int64_t row, int64_t byte_in_row);
  * cannot pay the device synchronisation that cudaMalloc/cudaFree imply.  The
  * pages have no counterpart of this entry point.
  *
- * Runs the default (persistent, warp-specialised) kernel for C = A . B^T with
+ * Runs the kernel an automatic plan (gemm_create_plan) would run for
+ * C = A . B^T, with stream-K off -- the dynamic CTA-pair kernel for large
+ * problems, the single-CTA persistent kernel for small or skinny ones -- with
  * the same operands, layouts, preconditions and arithmetic as gemm_run, on
  * `cuda_stream`.  It allocates nothing: its only scratch memory, the kernel's
  * 32-byte watchdog status record, lives in a file-scope device array of 256

@@ -66,8 +66,12 @@ def _no_alloc(A, B, out, synchronous):
 
 
 def test_no_alloc_matches_gemm_run_on_two_calls_in_a_row():
+    # small shapes take the single-CTA kernel; the last two have enough pair
+    # tiles for the dynamic CTA-pair kernel (stages of K = 64 and of K = 128)
     cases = [((300, 264, 328), "f32", "uniform", 21, False),
-             ((520, 392, 1000), "f16", "normal", 22, True)]
+             ((520, 392, 1000), "f16", "normal", 22, True),
+             ((2560, 1024, 1000), "f16", "normal", 23, True),
+             ((2560, 1040, 512), "f32", "uniform", 24, False)]
     for (M, N, K), out, dist, seed, sync in cases:
         A, B = inputs.make_operands(M, N, K, dist, seed)
         want = _with_plan(A, B, out)

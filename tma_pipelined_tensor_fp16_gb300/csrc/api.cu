@@ -941,10 +941,11 @@ int64_t gemm_sw128_offset(int64_t row, int64_t byte_in_row)
 // (a foreign cudaMalloc either fails for lack of memory or is forbidden by
 // policy), and latency-critical serving loops that cannot afford the device
 // synchronisation cudaMalloc/cudaFree imply.  gemm_create_plan allocates the
-// plan's device status record, so those callers use gemm_run_noalloc instead:
-// the persistent kernel's only scratch memory, that status record, lives in
-// the file-scope array below, which every GPU that loads this library holds
-// until the process exits.
+// plan's device status record, so those callers use gemm_run_noalloc instead.
+// It runs the kernel an automatic plan would, without stream-K (the only
+// option that needs a workspace); the kernel's only scratch memory, the status
+// record, lives in the file-scope array below, which every GPU that loads this
+// library holds until the process exits.
 
 namespace {
 
@@ -1016,7 +1017,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
 
     gemm_options opts;
     std::memset(&opts, 0, sizeof(opts));
-    opts.variant = VAR_PERSISTENT;
+    opts.variant = VAR_AUTO;
     opts.stream_k = 1;  // no workspace: every tile whole
     gemm_config c;
     int r = select_config_impl(M, N, K, dtype_out, &opts, sms, smem_optin, &c);
@@ -1030,8 +1031,8 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     r = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, K * 2, BLK_K,
                   static_cast<uint32_t>(c.a_rows), "A");
     if (r == GEMM_OK)
-        r = encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, K * 2, BLK_K, c.block_n,
-                      "B");
+        r = encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, K * 2, BLK_K,
+                      static_cast<uint32_t>(is_pair(c.variant) ? c.block_n / 2 : c.block_n), "B");
     if (r == GEMM_OK) {
         if (dtype_out == GEMM_OUT_F16)
             r = encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, N, M, N * 2, 64, BLK_M, "C");
@@ -1083,7 +1084,10 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     p.sk_partials = nullptr;
     p.sk_tickets = nullptr;
     p.a_rows = c.a_rows;
-    e = launch_ws(s, stream);
+    p.k_snake = 1;
+    p.snake_span = std::max(1, std::min(sms / 2, c.num_tiles));
+    p.ksub = c.block_k / BLK_K;
+    e = is_pair(c.variant) ? launch_pair(s, stream) : launch_ws(s, stream);
     if (e != cudaSuccess) return cuda_fail("kernel launch", e);
 
     if (device_status) {
