@@ -150,3 +150,18 @@ def test_same_plan_launched_repeatedly(opts):
     assert_close(ref[rows, cols], oracle.gemm_entries(A, B, rows, cols), K, "f16", variant)
     for i, o in enumerate(outs[1:], 1):
         assert np.array_equal(o.view(np.uint16), ref.view(np.uint16)), "launch %d differs" % i
+
+
+@pytest.mark.parametrize("bk", [64, 128])
+def test_dynamic_many_tiles_per_cluster(bk):
+    # 4096 pair tiles over 76 resident clusters: about 54 cancellations per
+    # cluster, the response ring wrapping many times; a short K keeps it quick
+    M, N, K = 32768, 8192, 128
+    A, B = inputs.make_operands(M, N, K, "uniform", 77)
+    got, guard, desc = run(A, B, "f16", guard_rows=2, variant=V, block_k=bk)
+    assert np.isnan(guard.astype(np.float32)).all()
+    assert not np.isnan(got.astype(np.float32)).any(), desc
+    ref, _, _ = run(A, B, "f16", variant="persistent_2cta", block_k=bk)
+    assert np.array_equal(got.view(np.uint16), ref.view(np.uint16)), desc
+    rows, cols = _sample(M, N, 4000, 78)
+    assert_close(got[rows, cols], oracle.gemm_entries(A, B, rows, cols), K, "f16", desc)
