@@ -176,7 +176,15 @@ TMAGEMM_API gemm_plan* gemm_create_plan_ex(int64_t M, int64_t N, int64_t K, int 
  * Asynchronous: returns after the launch.  Argument and launch errors are
  * returned at once; an in-kernel timeout is reported by
  * gemm_get_device_status after the caller has synchronised the stream.  The
- * plan must be used on the device it was created on. */
+ * plan must be used on the device it was created on.
+ *
+ * CUDA graphs: the launch may be captured into a graph once the plan has run
+ * once outside the capture (that first run sets the kernel's shared-memory
+ * limit).  A replay repeats the captured run counter, so after a timeout in
+ * one replay the later replays of that graph end as aborted too: capture
+ * again.  Plans with stream-K tiles (stream_k = 2 and a partial last wave)
+ * refuse capture with GEMM_ERR_UNSUPPORTED: their fix-up tickets are keyed by
+ * the run counter and a replay would leave shared tiles unwritten. */
 TMAGEMM_API int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_stream);
 
 /* End-to-end variant of gemm_run for HOST buffers: copies A and B to device

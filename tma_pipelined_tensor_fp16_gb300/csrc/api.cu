@@ -588,6 +588,16 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
     if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
     if (dev != plan->device)
         return fail(GEMM_ERR_INVALID_ARG, "plan was created on another device");
+    if (plan->cfg.sk_tiles > 0) {
+        // Stream-K arrival tickets are keyed by the run counter, which a graph
+        // replay repeats: a replayed ticket word would never rank a last
+        // arrival, and the shared tiles would stay unwritten.
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(static_cast<cudaStream_t>(cuda_stream), &cs) == cudaSuccess &&
+            cs != cudaStreamCaptureStatusNone)
+            return fail(GEMM_ERR_UNSUPPORTED,
+                        "a plan with stream-K tiles cannot be captured into a CUDA graph");
+    }
 
     const gemm_config& c = plan->cfg;
     if (A != plan->mapA_ptr || B != plan->mapB_ptr || C != plan->mapC_ptr) {
