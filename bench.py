@@ -266,6 +266,9 @@ def main():
     ap.add_argument("--depth", type=int, default=0)
     ap.add_argument("--block-n", type=int, default=0)
     ap.add_argument("--block-k", type=int, default=0, choices=[0, 64, 128])
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the K timed launches into one CUDA graph and time its replay "
+                         "(launch overhead removed; per-launch times are the average)")
     ap.add_argument("--l2-flush", action="store_true",
                     help="cold L2: write a scratch buffer of twice the L2 size before every timed "
                          "launch; the rate is then taken from the launches' own events")
@@ -324,6 +327,16 @@ def main():
     if plan.device_status() != 0:
         raise SystemExit("warm-up failed: " + pkg.gemm_last_error())
 
+    if args.graph and args.l2_flush:
+        raise SystemExit("--graph and --l2-flush cannot be combined")
+    graph = None
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(args.steps):
+                plan.run(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), sh)
+        graph.replay()  # one untimed replay
+        torch.cuda.synchronize()
     scratch = None
     if args.l2_flush:
         l2 = torch.cuda.get_device_properties(local_rank).L2_cache_size
@@ -339,7 +352,9 @@ def main():
     sampler.mark_start()
     with torch.cuda.stream(stream):
         t_start.record(stream)
-        for i in range(args.steps):
+        if graph is not None:
+            graph.replay()
+        for i in range(args.steps if graph is None else 0):
             if scratch is not None:
                 scratch.fill_(i)  # evicts A, B and C from L2 (outside the launch's events)
             ev[i][0].record(stream)
@@ -353,7 +368,10 @@ def main():
     if plan.device_status() != 0:
         raise SystemExit("timed run failed: " + pkg.gemm_last_error())
     total_ms = t_start.elapsed_time(t_end)
-    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if graph is not None:
+        launch_ms = [total_ms / args.steps] * args.steps
+    else:
+        launch_ms = [a.elapsed_time(b) for a, b in ev]
     if scratch is not None:
         # the timed region also holds the flushes: the step time is the
         # launches' own time
@@ -451,6 +469,8 @@ def main():
                           if args.l2_flush else
                           "no flush: A+B+C exceed the L2" if M * K * 2 + N * K * 2 > 130e6
                           else "operands fit in L2 (warm)"),
+                   "launch": "one CUDA graph of the K launches" if args.graph
+                   else "K host launches",
                    "plan": plan_desc},
         "roofline": roof,
         "cpu_baseline": cpu,
