@@ -123,12 +123,12 @@ typedef struct {
                            ("05 Async Data Movement - TMA", Using 3D TMA to Move
                            Multiple Swizzle Atoms), loaded as two boxes and
                            consumed by 8 MMAs behind one barrier round trip
-                           (CTA-pair variants only, not with stream_k = 2;
-                           pipe_depth then counts 128-wide stages).  A second
-                           block past K arrives zero-filled and is skipped.
-                           0 = auto: 128 for the CTA-pair variants when K is a
-                           multiple of 64 (128-byte aligned operand rows) and
-                           neither stream_k = 2 nor pipe_depth is set, else 64 */
+                           (CTA-pair variants only; pipe_depth then counts
+                           128-wide stages, and stream-K splits K in such
+                           stages).  A second block past K arrives zero-filled
+                           and is skipped.  0 = auto: 128 for the CTA-pair
+                           variants when K is a multiple of 64 (128-byte aligned
+                           operand rows) and pipe_depth is not set, else 64 */
 } gemm_options;
 
 /* Resolved configuration of a plan (also returned by gemm_select_config). */
@@ -145,7 +145,8 @@ typedef struct {
     int tx_bytes;       /* bytes one stage's barrier expects (A + B tile) */
     int dp_tiles;       /* tiles computed whole */
     int sk_tiles;       /* tiles of the stream-K part (0: none) */
-    int sk_kb_per_worker; /* K blocks of the stream-K part per CTA / pair */
+    int sk_kb_per_worker; /* pipeline stages (of block_k) of the stream-K part
+                             per CTA / pair */
     int sk_max_contrib; /* most CTAs / pairs that share one stream-K tile */
     long long workspace_bytes; /* device workspace the plan allocates for stream-K */
     int a_rows;         /* rows of A per stage: 128, or 64 when M <= 64 (single-CTA

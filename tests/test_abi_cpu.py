@@ -185,8 +185,14 @@ def test_block_k_128_stages(b):
     assert st == b.GEMM_ERR_INVALID_ARG
     st, _ = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(block_k=96))
     assert st == b.GEMM_ERR_INVALID_ARG
-    st, _ = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(
+    # stream-K (static pair schedule) splits K in 128-wide stages: the 36-tile
+    # partial last wave over 76 pairs, 64 stages per tile
+    st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(
         variant="persistent_2cta", block_k=128, stream_k="on"))
+    assert st == 0 and c.block_k == 128 and c.sk_tiles == 1024 % 76
+    assert c.sk_kb_per_worker == -(-(c.sk_tiles * 64) // 76)
+    st, _ = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(
+        variant="dynamic_2cta", block_k=128, stream_k="on"))
     assert st == b.GEMM_ERR_UNSUPPORTED
     st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(block_k=64))
     assert st == 0 and c.block_k == 64 and c.pipe_depth == 6
@@ -310,14 +316,20 @@ def test_work_units_cover_every_k_block_once(b, M, N, K, opts):
         assert all(a[2] == b_[1] for a, b_ in zip(lst, lst[1:]))     # ranks follow K order
     if c.sk_tiles:
         # equal shares: every worker's K-block count within one range of the others
-        assert max(work) - min(work) <= c.sk_kb_per_worker
+        # shares are counted in pipeline stages of block_k / 64 K blocks
+        assert max(work) - min(work) <= c.sk_kb_per_worker * (c.block_k // 64)
 
 
 def test_stream_k_choice(b):
     on = b.make_options(stream_k="on")
     st, c = b.gemm_select_config(8192, 8192, 8192, 1, on)
-    assert (c.dp_tiles, c.sk_tiles, c.sk_kb_per_worker) == (988, 36, 61)
+    # the static pair schedule with 128-wide stages: 36 tail tiles x 64 stages
+    # over 76 pairs
+    assert c.variant == b.GEMM_VAR_PERSISTENT_2CTA and c.block_k == 128
+    assert (c.dp_tiles, c.sk_tiles, c.sk_kb_per_worker) == (988, 36, 31)
     assert c.dp_tiles % (c.grid // 2) == 0
+    st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(stream_k="on", block_k=64))
+    assert (c.dp_tiles, c.sk_tiles, c.sk_kb_per_worker) == (988, 36, 61)
     for opts in (None, b.make_options(stream_k="off")):  # auto = off
         st, c = b.gemm_select_config(8192, 8192, 8192, 1, opts)
         assert (c.dp_tiles, c.sk_tiles, c.workspace_bytes) == (1024, 0, 0)

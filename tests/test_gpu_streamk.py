@@ -38,6 +38,14 @@ CASES = [
     ("persistent_2cta", 520, 1000, 776, 8, 224),     # fp16: 32-column remainder stored directly
 ]
 
+# the CTA-pair kernel with stages of K = 128: stream-K ranges are counted in
+# such stages, and an odd block count leaves the last stage half past K
+CASES_K128 = [
+    ("persistent_2cta", 700, 1000, 520, 10, 256),
+    ("persistent_2cta", 1280, 1024, 328, 14, 224),
+    ("persistent_2cta", 300, 264, 2048, 6, 256),     # 4 tiles over 3 pairs
+]
+
 
 @pytest.mark.parametrize("variant,M,N,K,grid,bn", CASES)
 @pytest.mark.parametrize("out", ["f32", "f16"])
@@ -48,6 +56,21 @@ def test_stream_k_matches_oracle(variant, M, N, K, grid, bn, out):
     assert "stream_k=0/" not in desc, desc
     assert_close(got, oracle.gemm(A, B), K, out, desc)
     assert np.isnan(guard.astype(np.float32)).all()
+
+
+@pytest.mark.parametrize("variant,M,N,K,grid,bn", CASES_K128)
+@pytest.mark.parametrize("out", ["f32", "f16"])
+def test_stream_k_with_128_wide_stages(variant, M, N, K, grid, bn, out):
+    A, B = inputs.make_operands(M, N, K, "normal", 700 + M + K)
+    got, guard, desc = run(A, B, out, guard_rows=2, variant=variant, grid=grid, block_n=bn,
+                           stream_k="on", block_k=128)
+    assert "stream_k=0/" not in desc and "x128 " in desc, desc
+    assert_close(got, oracle.gemm(A, B), K, out, desc)
+    assert np.isnan(guard.astype(np.float32)).all()
+    Ai, Bi = inputs.make_operands(M, N, K, "int", 19)
+    goti, _, _ = run(Ai, Bi, out, variant=variant, grid=grid, block_n=bn, stream_k="on",
+                     block_k=128)
+    assert_exact(goti, oracle.gemm(Ai, Bi), out, desc)
 
 
 @pytest.mark.parametrize("variant,M,N,K,grid,bn", CASES[:2] + CASES[3:5])

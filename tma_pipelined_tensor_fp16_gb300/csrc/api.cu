@@ -239,18 +239,17 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
                     "dynamic_2cta schedules whole tiles: stream-K needs a static variant");
     if (opts.block_k == 128 && !is_pair(variant))
         return fail(GEMM_ERR_INVALID_ARG, "block_k = 128 is built for the CTA-pair variants");
-    if (opts.block_k == 128 && opts.stream_k == 2)
-        return fail(GEMM_ERR_UNSUPPORTED, "block_k = 128 schedules whole tiles: no stream-K");
     // K blocks of 64 per stage (two 128-byte swizzle atoms at block_k = 128).
     // Automatic for CTA pairs whose operand rows are 128-byte aligned (K a
-    // multiple of 64), unless stream-K or an explicit ring depth is asked for
-    // (a depth sweep is a sweep of 64-wide stages).  Measured on GB300, 3
+    // multiple of 64), unless an explicit ring depth is asked for (a depth
+    // sweep is a sweep of 64-wide stages).  Stream-K then splits K in units
+    // of these stages.  Measured on GB300, 3
     // stages of 64 KB against 6 of 32 KB: 8192^3 1808 vs 1690 TFLOP/s, 4096^3
     // 1600 vs 1357, 4000x3000x4992 1484 vs 1296 (dynamic schedule).  With
     // rows that start off a 128-byte line (K = 5000, 5064) every box row
     // straddles two lines and the wider stages lose: 1128-1143 vs 1162-1178.
-    const bool auto_k128 = opts.block_k == 0 && is_pair(variant) && opts.stream_k != 2 &&
-                           opts.pipe_depth == 0 && K % 64 == 0;
+    const bool auto_k128 =
+        opts.block_k == 0 && is_pair(variant) && opts.pipe_depth == 0 && K % 64 == 0;
     const int ksub = (opts.block_k == 128 || auto_k128) ? 2 : 1;
     if (is_pair(variant) && opts.block_n != 0 && !pair_width_ok(opts.block_n, dtype))
         return fail(GEMM_ERR_INVALID_ARG,
@@ -318,7 +317,8 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     c->k_blocks = static_cast<int>(ceil_div(K, BLK_K));
     // Stream-K (persistent warp-specialised variants) decides whether a grid
     // larger than the tile count pays: the extra workers share the K blocks.
-    const int64_t KBLK = ceil_div(K, BLK_K);
+    // stream-K splits K in units of pipeline stages (ksub K blocks of 64)
+    const int64_t KBLK = ceil_div(ceil_div(K, BLK_K), ksub);
     auto stream_k_worth = [&](int64_t T, int64_t workers) {
         const int64_t rem = T % workers;
         if (rem == 0 || opts.stream_k == 1) return false;
@@ -368,7 +368,7 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     c->dp_tiles = c->num_tiles;
     if (sk_capable) {
         const int64_t workers = is_pair(variant) ? c->grid / 2 : c->grid;
-        const int64_t T = c->num_tiles, KB = c->k_blocks;
+        const int64_t T = c->num_tiles, KB = KBLK;  // stages per tile
         if (stream_k_worth(T, workers)) {
             const int64_t sk = T >= workers ? T % workers : T;
             const int64_t L = ceil_div(sk * KB, workers);
@@ -916,14 +916,17 @@ int gemm_schedule_unit(const gemm_config* cfg, int worker, int index, int* tile,
         return fail(GEMM_ERR_INVALID_ARG, "NULL argument or negative index");
     const int workers = is_pair(cfg->variant) ? cfg->grid / 2 : cfg->grid;
     if (worker < 0 || worker >= workers) return fail(GEMM_ERR_INVALID_ARG, "worker out of range");
+    // the kernels count K in pipeline stages of `ks` K blocks; report blocks
+    const int ks = cfg->block_k > BLK_K ? cfg->block_k / BLK_K : 1;
+    const int stages = (cfg->k_blocks + ks - 1) / ks;
     WorkIter it;
-    it.init(worker, workers, cfg->dp_tiles, cfg->sk_tiles, cfg->k_blocks, cfg->sk_kb_per_worker);
+    it.init(worker, workers, cfg->dp_tiles, cfg->sk_tiles, stages, cfg->sk_kb_per_worker);
     WorkUnit u;
     for (int i = 0; it.next(u); ++i) {
         if (i == index) {
             *tile = u.tile;
-            *kb0 = u.kb0;
-            *kb1 = u.kb1;
+            *kb0 = u.kb0 * ks;
+            *kb1 = u.kb1 * ks < cfg->k_blocks ? u.kb1 * ks : cfg->k_blocks;
             *contrib = u.contrib;
             *ncontrib = u.ncontrib;
             ok();
