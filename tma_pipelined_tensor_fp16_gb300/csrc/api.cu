@@ -610,10 +610,10 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
         if (r == GEMM_OK) {
             if (plan->dtype == GEMM_OUT_F16)
                 r = encode_2d(&plan->tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, plan->N, plan->M,
-                              plan->N * 2, 64, BLK_M, "C");
+                              plan->N * 2, 64, 32, "C");
             else
                 r = encode_2d(&plan->tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, plan->N, plan->M,
-                              plan->N * 4, 32, BLK_M, "C");
+                              plan->N * 4, 32, 32, "C");
         }
         if (r != GEMM_OK) {
             plan->mapA_ptr = plan->mapB_ptr = plan->mapC_ptr = nullptr;
@@ -1048,9 +1048,9 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
                       static_cast<uint32_t>(is_pair(c.variant) ? c.block_n / 2 : c.block_n), "B");
     if (r == GEMM_OK) {
         if (dtype_out == GEMM_OUT_F16)
-            r = encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, N, M, N * 2, 64, BLK_M, "C");
+            r = encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, N, M, N * 2, 64, 32, "C");
         else
-            r = encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, N * 4, 32, BLK_M, "C");
+            r = encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, N * 4, 32, 32, "C");
     }
     if (r != GEMM_OK) return r;
 

@@ -126,11 +126,12 @@ __device__ __forceinline__ void trace_header(const Params& p, int word, unsigned
 // A 128-thread group (4 warps) drains one 128 x BLOCK_N fp32 accumulator.
 // Warp q of the group (q = warp index mod 4) may only reach TMEM lanes
 // 32q..32q+31, so thread `lane` of warp q owns output row 32q + lane.  The
-// tile leaves in sub-tiles of 128 rows x 128 bytes (64 fp16 or 32 fp32
-// columns), written into a 128-byte-swizzled staging buffer: the 16-byte
-// chunk c of row r lands at chunk c ^ (r mod 8), which is the layout the
-// C tensor map's SWIZZLE_128B expects and spreads each 8-thread phase of the
-// st.shared.v4 over all 32 banks.
+// tile leaves in sub-tiles of 128 bytes per row (64 fp16 or 32 fp32
+// columns); each warp writes its 32 rows of a sub-tile into its own
+// 128-byte-swizzled staging buffer and stores them with a 32-row TMA box (the
+// C tensor map's box is 32 rows high).  The 16-byte chunk c of row r lands at
+// chunk c ^ (r mod 8), the layout SWIZZLE_128B expects, which spreads each
+// 8-thread phase of the st.shared.v4 over all 32 banks.
 
 template <int BLOCK_N, bool F16OUT>
 struct EpilogueShape {
@@ -153,29 +154,37 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }
 
 // Stage one output sub-tile held in registers (`v`: SUB_COLS fp32 values of
-// output row `row`, as raw bits) and TMA-store it at (col0, m0).
-// `staging`: shared address of NUM_STAGING buffers of STAGING_BYTES, 1024-B
-// aligned.  `sub_count` counts the sub-tiles this group has staged so far (it
-// carries across tiles and selects the staging buffer).  `bar_id` is a named
-// barrier reserved for the 128 threads.  `issuer` is exactly one thread of the
-// group.  The store is skipped (but every barrier is still executed) when
-// `do_store` is false.
+// output row `row` of the 128-row group, as raw bits) and TMA-store it at
+// (col0, m0).  Each warp stages and stores its own 32 rows (row / 32 is the
+// warp's quarter): it writes them into its own pair of 4 KB buffers (32 rows
+// x 128 bytes, 128-byte swizzled) at `staging` + quarter * 8 KB, reconverges,
+// and its lane 0 issues a 32-row TMA store and commits it as a bulk group.
+// No thread outside the warp takes part, so the four warps of the group drain
+// and store independently (one 128-row store behind a group barrier per
+// sub-tile measured slower).  `sub_count` counts the sub-tiles this thread's
+// warp has staged so far (it carries across tiles and selects the buffer); a
+// buffer is rewritten only after the store issued from it two sub-tiles ago
+// has finished reading it.  The store is skipped when `do_store` is false or
+// the warp's rows start at or past M.
 template <bool F16OUT>
-__device__ __forceinline__ void stage_and_store(const uint32_t* v, uint32_t row, bool issuer,
+__device__ __forceinline__ void stage_and_store(const uint32_t* v, uint32_t row,
                                                 uint32_t staging, const CUtensorMap* tmap_c,
-                                                int col0, int m0, uint32_t& sub_count,
-                                                uint32_t bar_id, bool do_store)
+                                                int col0, int m0, int M, uint32_t& sub_count,
+                                                bool do_store)
 {
-    const uint32_t buf = staging + (sub_count & 1u) * STAGING_BYTES;
+    const uint32_t quarter = row >> 5;
+    const uint32_t r = row & 31u;
+    const uint32_t buf = staging + quarter * (2u * WARP_STAGING_BYTES) +
+                         (sub_count & 1u) * WARP_STAGING_BYTES;
     if (sub_count >= 2) {
         // the store issued two sub-tiles ago read this buffer
-        if (issuer) bulk_wait_group_read<1>();
-        named_bar_sync(bar_id, 128);
+        if (r == 0) bulk_wait_group_read<1>();
+        __syncwarp();
     }
-    const uint32_t row_base = buf + row * 128u;
+    const uint32_t row_base = buf + r * 128u;
 #pragma unroll
     for (uint32_t c = 0; c < 8; ++c) {
-        const uint32_t dst = row_base + ((c ^ (row & 7u)) << 4);
+        const uint32_t dst = row_base + ((c ^ (r & 7u)) << 4);
         if constexpr (F16OUT) {
             st_shared_v4(dst, pack_half2(v[8 * c + 0], v[8 * c + 1]),
                          pack_half2(v[8 * c + 2], v[8 * c + 3]),
@@ -186,9 +195,10 @@ __device__ __forceinline__ void stage_and_store(const uint32_t* v, uint32_t row,
         }
     }
     fence_proxy_async_smem();
-    named_bar_sync(bar_id, 128);
-    if (issuer && do_store) {
-        tma_store_2d(tmap_c, buf, col0, m0);
+    __syncwarp();
+    const int wm0 = m0 + static_cast<int>(quarter * 32u);
+    if (r == 0 && do_store && wm0 < M) {
+        tma_store_2d(tmap_c, buf, col0, wm0);
         bulk_commit_group();
     }
     ++sub_count;
@@ -222,10 +232,10 @@ __device__ __forceinline__ void direct_store_row32_f16(const uint32_t* v, void* 
 // sub-tile: TMEM -> registers -> staging -> TMA store.
 template <int BLOCK_N, bool F16OUT>
 __device__ __forceinline__ void epilogue_tma_store(uint32_t tmem_acc, int q, uint32_t lane,
-                                                   bool issuer, uint32_t staging,
-                                                   const CUtensorMap* tmap_c, int m0, int n0,
-                                                   int N, uint32_t& sub_count, uint32_t bar_id,
-                                                   bool do_store, void* C = nullptr, int M = 0)
+                                                   uint32_t staging, const CUtensorMap* tmap_c,
+                                                   int m0, int n0, int M, int N,
+                                                   uint32_t& sub_count, bool do_store,
+                                                   void* C = nullptr)
 {
     using S = EpilogueShape<BLOCK_N, F16OUT>;
     const uint32_t row = static_cast<uint32_t>(q) * 32u + lane;
@@ -250,8 +260,7 @@ __device__ __forceinline__ void epilogue_tma_store(uint32_t tmem_acc, int q, uin
         } else {
             tmem_load_32cols(taddr + j * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
         }
-        stage_and_store<F16OUT>(v, row, issuer, staging, tmap_c, col0, m0, sub_count, bar_id,
-                                do_store);
+        stage_and_store<F16OUT>(v, row, staging, tmap_c, col0, m0, M, sub_count, do_store);
     }
 }
 
@@ -311,11 +320,11 @@ __device__ __forceinline__ void sk_write_partial(uint32_t tmem_acc, int q, uint3
 // one contributor's worth.
 template <int BLOCK_N, bool F16OUT>
 __device__ __forceinline__ void sk_reduce_store(const float* slot0, size_t slot_stride,
-                                                int ncontrib, int q, uint32_t lane, bool issuer,
+                                                int ncontrib, int q, uint32_t lane,
                                                 uint32_t staging, const CUtensorMap* tmap_c,
-                                                int m0, int n0, int N, uint32_t& sub_count,
-                                                uint32_t bar_id, bool do_store, bool row_valid,
-                                                void* C = nullptr, int M = 0)
+                                                int m0, int n0, int M, int N,
+                                                uint32_t& sub_count, bool do_store,
+                                                bool row_valid, void* C = nullptr)
 {
     using S = EpilogueShape<BLOCK_N, F16OUT>;
     const uint32_t row = static_cast<uint32_t>(q) * 32u + lane;
@@ -378,8 +387,8 @@ __device__ __forceinline__ void sk_reduce_store(const float* slot0, size_t slot_
                 }
             }
         }
-        stage_and_store<F16OUT>(reinterpret_cast<const uint32_t*>(acc), row, issuer, staging,
-                                tmap_c, col0, m0, sub_count, bar_id, do_store);
+        stage_and_store<F16OUT>(reinterpret_cast<const uint32_t*>(acc), row, staging, tmap_c,
+                                col0, m0, M, sub_count, do_store);
     }
 }
 
@@ -415,9 +424,8 @@ __device__ __forceinline__ void sk_epilogue(uint32_t tmem_acc, int q, uint32_t l
     named_bar_sync(bar_id, 128);  // everyone has read the slot before it is reused
     if (ticket == static_cast<uint32_t>(ncontrib - 1)) {
         __threadfence();
-        sk_reduce_store<BLOCK_N, F16OUT>(slot0, slot_stride, ncontrib, q, lane, issuer, staging,
-                                         tmap_c, m0, n0, N, sub_count, bar_id, !aborted,
-                                         row_valid, C, M);
+        sk_reduce_store<BLOCK_N, F16OUT>(slot0, slot_stride, ncontrib, q, lane, staging, tmap_c,
+                                         m0, n0, M, N, sub_count, !aborted, row_valid, C);
     }
 }
 

@@ -27,6 +27,11 @@ constexpr int MAX_STAGES = 8;
 constexpr int CLC_SLOTS = 4;
 constexpr int STAGING_BYTES = 128 * 128;  // one 128-row x 128-byte output sub-tile
 constexpr int NUM_STAGING = 2;            // double-buffered output staging
+// Each epilogue warp stages its own 32 rows: two buffers of 32 x 128 bytes per
+// warp, the four warps' pairs side by side in the NUM_STAGING x STAGING_BYTES
+// staging area.
+constexpr uint32_t WARP_STAGING_BYTES = 32 * 128;
+static_assert(4 * 2 * WARP_STAGING_BYTES == NUM_STAGING * STAGING_BYTES, "staging area");
 
 // Bytes one pipeline stage receives: the A tile plus the B tile, in fp16
 // ("GEMM II -- pipelining with TMA", Step 4, the byte_count formula).  The TMA

@@ -281,9 +281,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
             const uint32_t tmem_acc = tmem_base + static_cast<uint32_t>(acc * BN);
             const uint32_t empty_bar = bar_addr(bars, BAR_TMEM_EMPTY + acc);
             if (u.ncontrib == 1) {
-                epilogue_tma_store<BN, F16OUT>(tmem_acc, q, lane, issuer, staging, &tmC,
-                                               mt * BLK_M, nt * BN, p.N, sub_count, EPI_BAR_ID,
-                                               !wd.aborted);
+                epilogue_tma_store<BN, F16OUT>(tmem_acc, q, lane, staging, &tmC, mt * BLK_M,
+                                               nt * BN, p.M, p.N, sub_count, !wd.aborted);
                 tc_fence_before_sync();
                 mbar_arrive(empty_bar);
             } else {
@@ -307,7 +306,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
                 acc_phase ^= 1u;
             }
         }
-        if (issuer) bulk_wait_group<0>();
+        // each warp's stores have read their staging before the CTA exits
+        if (lane == 0) bulk_wait_group<0>();
         if (issuer) trace_header(p, TRACE_H_UNITS, static_cast<unsigned long long>(eui));
     }
 

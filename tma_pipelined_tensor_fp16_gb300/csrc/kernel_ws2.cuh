@@ -481,10 +481,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                 if (lane == 0) mbar_arrive_cluster(empty_leader);
             };
             if (u.ncontrib == 1) {
-                epilogue_tma_store<PAIR_BN, F16OUT>(tmem_acc, q, lane, issuer, staging, &tmC, m0,
-                                                    nt * PAIR_BN, p.N, sub_count,
-                                                    PAIR_EPI_BAR_ID, !wd.aborted && m0 < p.M,
-                                                    p.C, p.M);
+                epilogue_tma_store<PAIR_BN, F16OUT>(tmem_acc, q, lane, staging, &tmC, m0,
+                                                    nt * PAIR_BN, p.M, p.N, sub_count,
+                                                    !wd.aborted, p.C);
                 release();
             } else {
                 // each CTA fixes up its own 128 rows of the pair tile
@@ -503,7 +502,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
-        if (issuer) bulk_wait_group<0>();
+        // each warp's stores have read their staging before the CTA exits
+        if (lane == 0) bulk_wait_group<0>();
         if (issuer) trace_header(p, TRACE_H_UNITS, static_cast<unsigned long long>(eui));
         __syncwarp();
     }

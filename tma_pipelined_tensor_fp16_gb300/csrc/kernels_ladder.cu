@@ -238,14 +238,15 @@ __global__ void __launch_bounds__(128) k_tma_serial(const __grid_constant__ CUte
 
     tc_fence_after_sync();
     uint32_t sub_count = 0;
-    epilogue_tma_store<BN, F16OUT>(tmem, warp, lane, tid == 0, staging, &tmC, m0, n0, p.N,
-                                   sub_count, 1, !wd.aborted);
+    epilogue_tma_store<BN, F16OUT>(tmem, warp, lane, staging, &tmC, m0, n0, p.M, p.N,
+                                   sub_count, !wd.aborted);
 
     if (tid == 0) {
         if (load_pending) wd.drain(tma_bar, pending_parity);
         drain_mmas(wd, drain_bar);
-        bulk_wait_group<0>();
     }
+    // each warp's stores have read their staging before the CTA exits
+    if (lane == 0) bulk_wait_group<0>();
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) {
@@ -347,8 +348,8 @@ __global__ void __launch_bounds__(128) k_pipelined(const __grid_constant__ CUten
         }
 
         tc_fence_after_sync();
-        epilogue_tma_store<BN, F16OUT>(tmem, warp, lane, tid == 0, staging, &tmC, m0, n0, p.N,
-                                       sub_count, 1, !wd.aborted);
+        epilogue_tma_store<BN, F16OUT>(tmem, warp, lane, staging, &tmC, m0, n0, p.M, p.N,
+                                       sub_count, !wd.aborted);
         // every TMEM read is done before the next tile's first MMA overwrites it
         tc_fence_before_sync();
         __syncthreads();
@@ -359,8 +360,9 @@ __global__ void __launch_bounds__(128) k_pipelined(const __grid_constant__ CUten
             if (pending & (1u << s))
                 wd.drain(bar_addr(bars, BAR_FULL + s), (pending_parity >> s) & 1u);
         drain_mmas(wd, drain_bar);
-        bulk_wait_group<0>();
     }
+    // each warp's stores have read their staging before the CTA exits
+    if (lane == 0) bulk_wait_group<0>();
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) {
