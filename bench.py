@@ -9,9 +9,10 @@ operands resident in device memory.  Prints one JSON line (rank 0).
                   [--variant V] [--depth D] [--block-n BN] [--impl ours|reference]
 
 Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
-and a device synchronise on both sides, timed with CUDA events on the launch
-stream; max over ranks.  The operands (A + B = 256 MiB at 8192^3) and the
-output (128 MiB) are larger than the 126 MiB L2, so no flush is inserted.
+and a device synchronise on both sides, timed with two CUDA events on the
+launch stream around the K back-to-back launches; max over ranks.  The
+operands (A + B = 256 MiB at 8192^3) and the output (128 MiB) are larger than
+the 126 MiB L2, so no flush is inserted.
 
 ``--impl reference`` times the CPU oracle (the only other implementation of
 this computation) on a bounded sample of the same workload on the host cores.
@@ -32,7 +33,8 @@ sys.path.insert(0, ROOT)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["csrc/ptx.cuh", "csrc/gemm_common.h", "csrc/device_common.cuh",
                   "csrc/kernel_ws.cu", "csrc/kernel_ws2.cuh", "csrc/kernel_ws2.cu",
-                  "csrc/kernel_ws2_dyn.cu", "csrc/kernels_ladder.cu", "csrc/api.cu"]
+                  "csrc/kernel_ws2_dyn.cu", "csrc/kernels_ladder.cu", "csrc/api.cu",
+                  "csrc/launch.h", "csrc/kernel_ws2_k2.cu", "csrc/kernel_ws2_dyn_k2.cu"]
 
 
 def kernel_source_hash():
@@ -350,16 +352,24 @@ def main():
     barrier()
     torch.cuda.synchronize()
     sampler.mark_start()
+    # The K launches run back to back between two events: an event recorded
+    # between two launches would serialise them and hide the overlap of one
+    # launch's set-up with the previous launch's tail (programmatic dependent
+    # launch).  Only the L2-flush mode brackets each launch with events, to
+    # leave the flushes out of the launches' time.
     with torch.cuda.stream(stream):
         t_start.record(stream)
         if graph is not None:
             graph.replay()
-        for i in range(args.steps if graph is None else 0):
-            if scratch is not None:
+        elif scratch is None:
+            for _ in range(args.steps):
+                plan.run(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), sh)
+        else:
+            for i in range(args.steps):
                 scratch.fill_(i)  # evicts A, B and C from L2 (outside the launch's events)
-            ev[i][0].record(stream)
-            plan.run(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), sh)
-            ev[i][1].record(stream)
+                ev[i][0].record(stream)
+                plan.run(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), sh)
+                ev[i][1].record(stream)
         t_end.record(stream)
     torch.cuda.synchronize()
     sampler.mark_end()
@@ -368,15 +378,30 @@ def main():
     if plan.device_status() != 0:
         raise SystemExit("timed run failed: " + pkg.gemm_last_error())
     total_ms = t_start.elapsed_time(t_end)
-    if graph is not None:
-        launch_ms = [total_ms / args.steps] * args.steps
-    else:
-        launch_ms = [a.elapsed_time(b) for a, b in ev]
     if scratch is not None:
         # the timed region also holds the flushes: the step time is the
         # launches' own time
+        launch_ms = [a.elapsed_time(b) for a, b in ev]
         total_ms = sum(launch_ms)
+    else:
+        launch_ms = [total_ms / args.steps] * args.steps
     total_ms = max_over_ranks(total_ms, dist, "cuda")
+
+    # Outside the timed region: each launch alone between its own two events
+    # (informational; such launches cannot overlap their neighbours).
+    single_ms = []
+    if graph is None and scratch is None:
+        n1 = min(args.steps, 20)
+        ev1 = ev[:n1]
+        with torch.cuda.stream(stream):
+            for a, b in ev1:
+                a.record(stream)
+                plan.run(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), sh)
+                b.record(stream)
+        torch.cuda.synchronize()
+        if plan.device_status() != 0:
+            raise SystemExit("per-launch pass failed: " + pkg.gemm_last_error())
+        single_ms = [a.elapsed_time(b) for a, b in ev1]
 
     flops, nbytes = algorithmic(cfg)
     ms_per_step = total_ms / args.steps
@@ -470,15 +495,20 @@ def main():
                           "no flush: A+B+C exceed the L2" if M * K * 2 + N * K * 2 > 130e6
                           else "operands fit in L2 (warm)"),
                    "launch": "one CUDA graph of the K launches" if args.graph
-                   else "K host launches",
+                   else "K host launches, each bracketed by events" if args.l2_flush
+                   else "K host launches back to back",
                    "plan": plan_desc},
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks,
-        "tflops_per_launch_median": flops / (statistics.median(launch_ms) * 1e-3) / 1e12,
     }
+    if single_ms:
+        line["single_launch_median"] = {
+            "value": flops / (statistics.median(single_ms) * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "launches": len(single_ms),
+            "note": "each launch between its own two events, outside the timed region"}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

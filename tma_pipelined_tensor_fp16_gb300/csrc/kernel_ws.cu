@@ -109,6 +109,9 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    // global memory only after the work before this launch has completed
+    griddep_wait();
+    griddep_launch_dependents();
     const uint32_t tmem_base = *tmem_slot;
     if (tid == 0) {
         trace_header(p, TRACE_H_START, globaltimer_ns());
@@ -327,8 +330,7 @@ cudaError_t launch_kernel(KernelT kernel, const LaunchSpec& s, cudaStream_t stre
 {
     cudaError_t e = ensure_smem_limit(kernel, s.smem_bytes);
     if (e != cudaSuccess) return e;
-    kernel<<<s.grid, WS_THREADS, s.smem_bytes, stream>>>(*s.tmA, *s.tmB, *s.tmC, s.p);
-    return cudaGetLastError();
+    return launch_programmatic(kernel, s, WS_THREADS, stream);
 }
 
 template <int BN, bool F16OUT>

@@ -249,6 +249,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
     tc_fence_before_sync();
     cluster_sync_all();
     tc_fence_after_sync();
+    // Everything above touches only shared memory, TMEM and the kernel's
+    // parameters; global memory (A, B, C, the status record, the trace) is
+    // accessed only after the work before this launch has completed.
+    griddep_wait();
+    griddep_launch_dependents();
     const uint32_t tmem_base = *tmem_slot;
     if (tid == 0) {
         trace_header(p, TRACE_H_START, globaltimer_ns());
@@ -523,8 +528,7 @@ cudaError_t launch_pair_kernel(KernelT kernel, const LaunchSpec& s, cudaStream_t
 {
     cudaError_t e = ensure_smem_limit(kernel, s.smem_bytes);
     if (e != cudaSuccess) return e;
-    kernel<<<s.grid, PAIR_THREADS, s.smem_bytes, stream>>>(*s.tmA, *s.tmB, *s.tmC, s.p);
-    return cudaGetLastError();
+    return launch_programmatic(kernel, s, PAIR_THREADS, stream);
 }
 
 // Launch k_ws2<block_n, f16out, DYN, KS> for one of the built pair tile

@@ -63,4 +63,27 @@ cudaError_t ensure_smem_limit(KernelT kernel, unsigned bytes)
     return e;
 }
 
+// Launch a warp-specialised GEMM kernel as a programmatic dependent of the
+// work before it on `stream`: its CTAs may be scheduled while that work drains
+// and run their set-up (barriers, TMEM allocation) meanwhile.  The kernel
+// executes griddep_wait() before its first global-memory access, so it still
+// reads A and B and writes C only after everything earlier on the stream has
+// completed; it calls griddep_launch_dependents() after its set-up.
+template <typename KernelT>
+cudaError_t launch_programmatic(KernelT kernel, const LaunchSpec& s, int threads,
+                                cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(s.grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = s.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, *s.tmA, *s.tmB, *s.tmC, s.p);
+}
+
 }  // namespace tg

@@ -292,6 +292,21 @@ __device__ __forceinline__ uint32_t map_shared_rank(uint32_t local, uint32_t ran
     return r;
 }
 
+// Programmatic dependent launch (PTX griddepcontrol).  wait: block until
+// every grid this launch depends on has completed and its memory operations
+// are visible.  launch_dependents: let the next launch on the stream, if it
+// was launched as a programmatic dependent, be scheduled before this grid
+// completes (its CTAs still wait for resources and for its own `wait`).
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // All threads of every CTA in the cluster.
 __device__ __forceinline__ void cluster_sync_all()
 {
