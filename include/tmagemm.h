@@ -179,6 +179,16 @@ TMAGEMM_API gemm_plan* gemm_create_plan_ex(int64_t M, int64_t N, int64_t K, int 
  * gemm_get_device_status after the caller has synchronised the stream.  The
  * plan must be used on the device it was created on.
  *
+ * Dependent launch: the warp-specialised variants (everything but the
+ * lock-step ladder) are launched as programmatic dependents of the work before
+ * them on the stream.  Their CTAs may become resident and set up shared memory
+ * and TMEM while the previous kernel drains, but they read A and B and write C
+ * only after all earlier work on the stream has completed (griddepcontrol.wait
+ * before the first global-memory access), so stream order is kept.  After
+ * set-up they allow the next launch on the stream to be scheduled early; a
+ * kernel launched after this one as a programmatic dependent must itself wait
+ * (griddepcontrol.wait) before reading C.
+ *
  * CUDA graphs: the launch may be captured into a graph once the plan has run
  * once outside the capture (that first run sets the kernel's shared-memory
  * limit).  A replay repeats the captured run counter, so after a timeout in
