@@ -74,7 +74,7 @@ typedef enum {
                                        its own half of the operands; block_n 128,
                                        160, 192, 224 or 256, chosen by wave
                                        efficiency */
-    GEMM_VAR_DYNAMIC_2CTA = 8       /* the CTA-pair kernel with a dynamic tile
+    GEMM_VAR_DYNAMIC_2CTA = 8,      /* the CTA-pair kernel with a dynamic tile
                                        schedule ("GEMM II -- pipelining with
                                        TMA", Step 6: cluster launch control as
                                        the upgrade of the static assignment):
@@ -87,6 +87,21 @@ typedef enum {
                                        gemm_schedule_unit reports only each
                                        cluster's own tile, the rest being
                                        assigned at run time */
+    GEMM_VAR_DYNAMIC_2X2 = 9        /* GEMM_VAR_DYNAMIC_2CTA with two CTA pairs
+                                       per cluster (4 CTAs) on two side-by-side
+                                       tiles of the same 256 rows: the CTAs of
+                                       equal rank in the two pairs need the same
+                                       128 rows of A, and each loads one 64-row
+                                       half and multicasts it to both, so A
+                                       leaves L2 once per cluster.  block_n 192,
+                                       224 or 256; with an odd number of tile
+                                       columns the last cluster's second tile
+                                       lies past N and is not stored.  grid must
+                                       be 0; no stream-K.  gemm_schedule_unit
+                                       reports each cluster's own unit u: tile
+                                       row and unit column from the grouped
+                                       raster over tiles_m x ceil(tiles_n / 2),
+                                       tiles 2 x column and 2 x column + 1 */
 } gemm_variant;
 
 /* Plan options; a zero field means "choose automatically". */

@@ -167,6 +167,36 @@ def test_dynamic_pair_configuration(b):
         assert b.gemm_worker_units(c, w) == [(w, 0, c.k_blocks, 0, 1)]
 
 
+def test_two_pair_cluster_configuration(b):
+    # Two CTA pairs per cluster on side-by-side tiles, one cluster (4 CTAs)
+    # per unit of two tile columns; an odd column count leaves the last
+    # unit's second tile past N.
+    st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(variant="dynamic_2x2"))
+    assert st == 0, b.last_error()
+    assert c.variant == b.GEMM_VAR_DYNAMIC_2X2
+    assert (c.block_m, c.block_n, c.block_k, c.pipe_depth, c.threads) == (256, 256, 128, 3, 192)
+    assert (c.tiles_m, c.tiles_n, c.num_tiles) == (32, 32, 1024)
+    assert c.grid == 4 * 32 * 16
+    st, c = b.gemm_select_config(600, 776, 328, 0, b.make_options(variant="dynamic_2x2"))
+    assert st == 0 and c.block_n == 192 and c.tiles_n == 5
+    assert c.grid == 4 * c.tiles_m * 3
+    st, c = b.gemm_select_config(4000, 3000, 5000, 0,
+                                 b.make_options(variant="dynamic_2x2", block_n=224))
+    assert st == 0 and (c.tiles_m, c.tiles_n, c.grid) == (16, 14, 4 * 16 * 7)
+    for bad in (dict(block_n=128), dict(block_n=160), dict(grid=144)):
+        st, _ = b.gemm_select_config(8192, 8192, 8192, 1,
+                                     b.make_options(variant="dynamic_2x2", **bad))
+        assert st == b.GEMM_ERR_INVALID_ARG, bad
+    st, _ = b.gemm_select_config(8192, 8192, 8192, 1,
+                                 b.make_options(variant="dynamic_2x2", stream_k="on"))
+    assert st == b.GEMM_ERR_UNSUPPORTED
+    # each cluster's own unit; the rest is decided while the kernel runs
+    st, c = b.gemm_select_config(1000, 1000, 520, 1, b.make_options(variant="dynamic_2x2"))
+    assert st == 0 and c.grid == 4 * c.tiles_m * ((c.tiles_n + 1) // 2)
+    for w in range(c.grid // 4):
+        assert b.gemm_worker_units(c, w) == [(w, 0, c.k_blocks, 0, 1)]
+
+
 def test_block_k_128_stages(b):
     # a stage of K = 128 as two 128-byte swizzle groups of 64 fp16 ("05 Async
     # Data Movement - TMA", Using 3D TMA to Move Multiple Swizzle Atoms): twice

@@ -83,6 +83,7 @@ const char* variant_name(int v)
     case VAR_PERSISTENT_LOCKSTEP: return "persistent_lockstep";
     case VAR_PERSISTENT_2CTA: return "persistent_2cta";
     case VAR_DYNAMIC_2CTA: return "dynamic_2cta";
+    case VAR_DYNAMIC_2X2: return "dynamic_2x2";
     default: return "?";
     }
 }
@@ -90,19 +91,51 @@ const char* variant_name(int v)
 bool is_ws(int v)
 {
     return v == VAR_WS_PIPELINED || v == VAR_PERSISTENT || v == VAR_PERSISTENT_2CTA ||
-           v == VAR_DYNAMIC_2CTA;
+           v == VAR_DYNAMIC_2CTA || v == VAR_DYNAMIC_2X2;
 }
 // One resident CTA per SM that takes tile after tile (statically or by
 // cancelling clusters that have not started).
 bool is_persistent(int v)
 {
     return v == VAR_PERSISTENT || v == VAR_PERSISTENT_LOCKSTEP || v == VAR_PERSISTENT_2CTA ||
-           v == VAR_DYNAMIC_2CTA;
+           v == VAR_DYNAMIC_2CTA || v == VAR_DYNAMIC_2X2;
 }
-bool is_pair(int v) { return v == VAR_PERSISTENT_2CTA || v == VAR_DYNAMIC_2CTA; }
+// 256-row tiles computed by CTA pairs (cta_group::2).
+bool is_pair(int v)
+{
+    return v == VAR_PERSISTENT_2CTA || v == VAR_DYNAMIC_2CTA || v == VAR_DYNAMIC_2X2;
+}
+// One cluster per work unit, clusters cancelling those not started yet.
+bool is_dynamic(int v) { return v == VAR_DYNAMIC_2CTA || v == VAR_DYNAMIC_2X2; }
+// Pair tiles in the cluster's work unit: two side-by-side tiles sharing A.
+int unit_pairs(int v) { return v == VAR_DYNAMIC_2X2 ? 2 : 1; }
 bool has_ring(int v) { return v != VAR_SYNC_TILED && v != VAR_TMA_SERIAL; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// The kernel's view of the tile grid: its work units are pair tiles, or (two
+// pairs per cluster) side-by-side pairs of them, so Params::tiles_n counts
+// unit columns; snake_span is the number of work units one full set of
+// clusters takes at a time.
+struct UnitGrid {
+    int tiles_n, units, snake_span;
+};
+UnitGrid unit_grid(const gemm_config& c, int sms)
+{
+    const int np = unit_pairs(c.variant);
+    UnitGrid g;
+    g.tiles_n = static_cast<int>(ceil_div(c.tiles_n, np));
+    g.units = c.tiles_m * g.tiles_n;
+    g.snake_span = std::max(1, std::min(sms / (2 * np), g.units));
+    return g;
+}
+
+// Rows of A per TMA box: two pairs per cluster load half of each 128-row
+// block each and multicast it to both pairs.
+uint32_t a_box_rows(const gemm_config& c)
+{
+    return static_cast<uint32_t>(c.variant == VAR_DYNAMIC_2X2 ? BLK_M / 2 : c.a_rows);
+}
 
 // Fraction of launched tile slots that do work when `tiles` tiles run in
 // waves over `sms` SMs.
@@ -136,9 +169,10 @@ int choose_block_n(int variant, int64_t M, int64_t N, int sms)
 // Pair tile widths the CTA-pair kernel is built for: multiples of 32 (fp32
 // output stores 32-column sub-tiles; fp16 output 64-column sub-tiles plus a
 // directly stored 32-column remainder for widths 160 and 224).
-bool pair_width_ok(int bn, int dtype)
+bool pair_width_ok(int bn, int dtype, int variant)
 {
     (void)dtype;  // fp16 widths of 160 / 224 store their last 32 columns directly
+    if (variant == VAR_DYNAMIC_2X2) return bn == 192 || bn == 224 || bn == 256;
     return bn == 128 || bn == 160 || bn == 192 || bn == 224 || bn == 256;
 }
 
@@ -149,22 +183,26 @@ bool pair_width_ok(int bn, int dtype)
 // wave and overhang losses divided out (narrower tiles issue more barrier
 // round trips and load more operand bytes per FLOP).  Stages of two K blocks
 // (ksub = 2) halve the round trips, and narrow tiles lose less.
-int choose_pair_bn(int64_t M, int64_t N, int sms, int dtype, int ksub)
+int choose_pair_bn(int64_t M, int64_t N, int sms, int dtype, int ksub, int variant)
 {
     const int widths[5] = {256, 224, 192, 160, 128};
     const double eff_k64[5] = {1.0, 0.92, 0.79, 0.73, 0.54};
     const double eff_k128[5] = {1.0, 0.94, 0.89, 0.81, 0.70};
     const double* tile_eff = ksub == 2 ? eff_k128 : eff_k64;
-    const int64_t pairs = sms / 2;
+    // A work unit of the two-pair variant is two side-by-side tiles; with an
+    // odd number of tile columns the last unit's second tile lies past N.
+    const int np = unit_pairs(variant);
+    const int64_t slots = sms / (2 * np);
     const int64_t tm = ceil_div(M, 2 * BLK_M);
     int best = 256;
     double best_score = -1.0;
     for (int i = 0; i < 5; ++i) {
         const int bn = widths[i];
-        if (!pair_width_ok(bn, dtype)) continue;
+        if (!pair_width_ok(bn, dtype, variant)) continue;
         const int64_t tn = ceil_div(N, bn);
-        const double cols = static_cast<double>(N) / static_cast<double>(tn * bn);
-        const double score = wave_efficiency(tm * tn, static_cast<int>(pairs)) * cols * tile_eff[i];
+        const int64_t un = ceil_div(tn, np);
+        const double cols = static_cast<double>(N) / static_cast<double>(un * np * bn);
+        const double score = wave_efficiency(tm * un, static_cast<int>(slots)) * cols * tile_eff[i];
         if (score > best_score + 1e-9) {
             best_score = score;
             best = bn;
@@ -208,7 +246,7 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     if ((N * elt) % 16 != 0)
         return fail(GEMM_ERR_UNSUPPORTED,
                     "N * sizeof(output) must be a multiple of 16 bytes (TMA row stride of C)");
-    if (opts.variant < 0 || opts.variant > VAR_DYNAMIC_2CTA)
+    if (opts.variant < 0 || opts.variant > VAR_DYNAMIC_2X2)
         return fail(GEMM_ERR_INVALID_ARG, "unknown variant");
     if (opts.pipe_depth < 0 || opts.pipe_depth > MAX_STAGES)
         return fail(GEMM_ERR_INVALID_ARG, "pipe_depth must be 0 (auto) or 1..8");
@@ -231,12 +269,12 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     const int variant = opts.variant == VAR_AUTO ? auto_variant(M, N, sms, opts) : opts.variant;
     if (opts.debug_stall && !is_ws(variant))
         return fail(GEMM_ERR_INVALID_ARG, "debug_stall needs a warp-specialised variant");
-    if (variant == VAR_DYNAMIC_2CTA && opts.grid != 0)
+    if (is_dynamic(variant) && opts.grid != 0)
         return fail(GEMM_ERR_INVALID_ARG,
-                    "dynamic_2cta launches one cluster per tile: grid must be 0 (auto)");
-    if (variant == VAR_DYNAMIC_2CTA && opts.stream_k == 2)
+                    "the dynamic variants launch one cluster per work unit: grid must be 0 (auto)");
+    if (is_dynamic(variant) && opts.stream_k == 2)
         return fail(GEMM_ERR_UNSUPPORTED,
-                    "dynamic_2cta schedules whole tiles: stream-K needs a static variant");
+                    "the dynamic variants schedule whole tiles: stream-K needs a static variant");
     if (opts.block_k == 128 && !is_pair(variant))
         return fail(GEMM_ERR_INVALID_ARG, "block_k = 128 is built for the CTA-pair variants");
     // K blocks of 64 per stage (two 128-byte swizzle atoms at block_k = 128).
@@ -251,11 +289,13 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     const bool auto_k128 =
         opts.block_k == 0 && is_pair(variant) && opts.pipe_depth == 0 && K % 64 == 0;
     const int ksub = (opts.block_k == 128 || auto_k128) ? 2 : 1;
-    if (is_pair(variant) && opts.block_n != 0 && !pair_width_ok(opts.block_n, dtype))
+    if (is_pair(variant) && opts.block_n != 0 && !pair_width_ok(opts.block_n, dtype, variant))
         return fail(GEMM_ERR_INVALID_ARG,
-                    "CTA-pair tile width (block_n) must be 128, 160, 192, 224 or 256");
+                    variant == VAR_DYNAMIC_2X2
+                        ? "dynamic_2x2 tile width (block_n) must be 192, 224 or 256"
+                        : "CTA-pair tile width (block_n) must be 128, 160, 192, 224 or 256");
     const int bn = opts.block_n   ? opts.block_n
-                   : is_pair(variant) ? choose_pair_bn(M, N, sms, dtype, ksub)
+                   : is_pair(variant) ? choose_pair_bn(M, N, sms, dtype, ksub, variant)
                                       : choose_block_n(variant, M, N, sms);
     // Shared memory per CTA holds B tiles of `bn_cta` rows: a CTA of a pair
     // keeps half of the pair tile's B rows.
@@ -334,10 +374,13 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
         return opts.stream_k == 2;
     };
     const bool sk_capable = variant == VAR_PERSISTENT || variant == VAR_PERSISTENT_2CTA;
-    if (variant == VAR_DYNAMIC_2CTA) {
-        // one cluster per pair tile; running clusters cancel the rest
-        if (2 * tiles > LIM) return fail(GEMM_ERR_UNSUPPORTED, "too many output tiles");
-        c->grid = static_cast<int>(2 * tiles);
+    if (is_dynamic(variant)) {
+        // one cluster per work unit (pair tile, or two side-by-side pair
+        // tiles); running clusters cancel the rest
+        const int np = unit_pairs(variant);
+        const int64_t units = tm * ceil_div(tn, np);
+        if (2 * np * units > LIM) return fail(GEMM_ERR_UNSUPPORTED, "too many output tiles");
+        c->grid = static_cast<int>(2 * np * units);
     } else if (is_pair(variant)) {
         // clusters of two CTAs, one pair tile per cluster at a time
         int64_t pairs = (opts.grid ? opts.grid : sms) / 2;
@@ -542,7 +585,7 @@ gemm_plan* gemm_create_plan_ex(int64_t M, int64_t N, int64_t K, int dtype_out,
     p->k_snake = (opts && opts->k_order == 1) ? 0 : 1;
     // The dynamic schedule takes each tile's K direction from the tile index,
     // as the static schedule of a full grid (SM count / 2 clusters) would.
-    p->snake_span = std::max(1, std::min(sms / 2, p->cfg.num_tiles));
+    p->snake_span = unit_grid(p->cfg, sms).snake_span;
     e = cudaMalloc(&p->d_status, sizeof(DevStatus));
     if (e == cudaSuccess) e = cudaMemset(p->d_status, 0, sizeof(DevStatus));
     if (e == cudaSuccess && p->cfg.workspace_bytes > 0) {
@@ -602,7 +645,7 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
     const gemm_config& c = plan->cfg;
     if (A != plan->mapA_ptr || B != plan->mapB_ptr || C != plan->mapC_ptr) {
         int r = encode_2d(&plan->tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, plan->K, plan->M,
-                          plan->K * 2, BLK_K, static_cast<uint32_t>(c.a_rows), "A");
+                          plan->K * 2, BLK_K, a_box_rows(c), "A");
         if (r == GEMM_OK)
             r = encode_2d(&plan->tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, plan->K, plan->N,
                           plan->K * 2, BLK_K, is_pair(c.variant) ? c.block_n / 2 : c.block_n,
@@ -639,8 +682,11 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
     p.N = static_cast<int>(plan->N);
     p.K = static_cast<int>(plan->K);
     p.tiles_m = c.tiles_m;
-    p.tiles_n = c.tiles_n;
-    p.num_tiles = c.num_tiles;
+    {
+        const UnitGrid ug = unit_grid(c, 2);  // (snake_span comes from the plan)
+        p.tiles_n = ug.tiles_n;
+        p.num_tiles = ug.units;
+    }
     p.k_blocks = c.k_blocks;
     p.group_m = c.group_m;
     p.pipe_depth = c.pipe_depth;
@@ -657,7 +703,7 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
     p.snake_span = plan->snake_span;
     p.ksub = c.block_k / BLK_K;
     p.a_rows = c.a_rows;
-    p.dp_tiles = c.dp_tiles;
+    p.dp_tiles = unit_pairs(c.variant) == 1 ? c.dp_tiles : p.num_tiles;
     p.sk_tiles = c.sk_tiles;
     p.sk_kb_per_worker = c.sk_kb_per_worker;
     p.sk_max_contrib = c.sk_max_contrib;
@@ -914,13 +960,17 @@ int gemm_schedule_unit(const gemm_config* cfg, int worker, int index, int* tile,
 {
     if (!cfg || !tile || !kb0 || !kb1 || !contrib || !ncontrib || index < 0)
         return fail(GEMM_ERR_INVALID_ARG, "NULL argument or negative index");
-    const int workers = is_pair(cfg->variant) ? cfg->grid / 2 : cfg->grid;
+    // workers: clusters (of NP CTA pairs) or CTAs; two pairs per cluster take
+    // units of two side-by-side tiles
+    const int np = unit_pairs(cfg->variant);
+    const int workers = is_pair(cfg->variant) ? cfg->grid / (2 * np) : cfg->grid;
     if (worker < 0 || worker >= workers) return fail(GEMM_ERR_INVALID_ARG, "worker out of range");
     // the kernels count K in pipeline stages of `ks` K blocks; report blocks
     const int ks = cfg->block_k > BLK_K ? cfg->block_k / BLK_K : 1;
     const int stages = (cfg->k_blocks + ks - 1) / ks;
+    const int dp = np == 1 ? cfg->dp_tiles : unit_grid(*cfg, 2).units;
     WorkIter it;
-    it.init(worker, workers, cfg->dp_tiles, cfg->sk_tiles, stages, cfg->sk_kb_per_worker);
+    it.init(worker, workers, dp, cfg->sk_tiles, stages, cfg->sk_kb_per_worker);
     WorkUnit u;
     for (int i = 0; it.next(u); ++i) {
         if (i == index) {
@@ -1041,8 +1091,8 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     if (r != GEMM_OK) return r;
 
     CUtensorMap tmA, tmB, tmC;
-    r = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, K * 2, BLK_K,
-                  static_cast<uint32_t>(c.a_rows), "A");
+    r = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, K * 2, BLK_K, a_box_rows(c),
+                  "A");
     if (r == GEMM_OK)
         r = encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, K * 2, BLK_K,
                       static_cast<uint32_t>(is_pair(c.variant) ? c.block_n / 2 : c.block_n), "B");
@@ -1074,8 +1124,9 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
     p.tiles_m = c.tiles_m;
-    p.tiles_n = c.tiles_n;
-    p.num_tiles = c.num_tiles;
+    const UnitGrid ug = unit_grid(c, sms);
+    p.tiles_n = ug.tiles_n;
+    p.num_tiles = ug.units;
     p.k_blocks = c.k_blocks;
     p.group_m = c.group_m;
     p.pipe_depth = c.pipe_depth;
@@ -1090,7 +1141,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     }
     p.budget_ns = 2000ull * 1000000ull;
     p.debug_stall = 0;
-    p.dp_tiles = c.num_tiles;
+    p.dp_tiles = ug.units;
     p.sk_tiles = 0;
     p.sk_kb_per_worker = 0;
     p.sk_max_contrib = 0;
@@ -1098,7 +1149,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     p.sk_tickets = nullptr;
     p.a_rows = c.a_rows;
     p.k_snake = 1;
-    p.snake_span = std::max(1, std::min(sms / 2, c.num_tiles));
+    p.snake_span = ug.snake_span;
     p.ksub = c.block_k / BLK_K;
     e = is_pair(c.variant) ? launch_pair(s, stream) : launch_ws(s, stream);
     if (e != cudaSuccess) return cuda_fail("kernel launch", e);
