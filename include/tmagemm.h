@@ -83,10 +83,10 @@ typedef enum {
                                        have not started
                                        (clusterlaunchcontrol.try_cancel) and
                                        computes their tiles.  grid must be 0;
-                                       stream_k = 2 is GEMM_ERR_UNSUPPORTED;
-                                       gemm_schedule_unit reports only each
-                                       cluster's own tile, the rest being
-                                       assigned at run time */
+                                       stream_k = 2 splits the tail instead
+                                       (see stream_k); gemm_schedule_unit
+                                       reports only each cluster's own unit,
+                                       the rest being assigned at run time */
     GEMM_VAR_DYNAMIC_2X2 = 9        /* GEMM_VAR_DYNAMIC_2CTA with two CTA pairs
                                        per cluster (4 CTAs) on two side-by-side
                                        tiles of the same 256 rows: the CTAs of
@@ -122,7 +122,14 @@ typedef struct {
                            partial last wave are split into K-block ranges
                            shared evenly by all CTAs (or pairs); partial sums go
                            through a workspace the plan owns and are added in a
-                           fixed order, so results do not vary from run to run. */
+                           fixed order, so results do not vary from run to run.
+                           GEMM_VAR_DYNAMIC_2CTA with stream_k = 2: the tiles of
+                           the partial last wave (all tiles when there are fewer
+                           than SM count / 2) are each split into S = 2..4 equal
+                           K ranges, S = (SM count / 2) / those tiles, each
+                           range at least 4 stages, run as separate units;
+                           gemm_config.sk_max_contrib is S.  Not with
+                           GEMM_VAR_DYNAMIC_2X2. */
     int l2_policy;      /* L2 eviction priority of the operand loads (warp-specialised
                            variants): 0 = default, 1 = A evict_last and B
                            evict_first, 2 = A evict_first and B evict_last,
@@ -209,8 +216,10 @@ TMAGEMM_API gemm_plan* gemm_create_plan_ex(int64_t M, int64_t N, int64_t K, int 
  * limit).  A replay repeats the captured run counter, so after a timeout in
  * one replay the later replays of that graph end as aborted too: capture
  * again.  Plans with stream-K tiles (stream_k = 2 and a partial last wave)
- * refuse capture with GEMM_ERR_UNSUPPORTED: their fix-up tickets are keyed by
- * the run counter and a replay would leave shared tiles unwritten. */
+ * have fix-up tickets keyed by the run counter, which a replay would repeat
+ * and so leave shared tiles unwritten: the static schedule refuses capture
+ * with GEMM_ERR_UNSUPPORTED, and a captured launch of the dynamic schedule
+ * runs every tile whole. */
 TMAGEMM_API int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_stream);
 
 /* End-to-end variant of gemm_run for HOST buffers: copies A and B to device

@@ -92,6 +92,7 @@ def test_headline_configuration(b):
     assert (c.block_m, c.block_n, c.block_k) == (256, 256, 128)
     assert c.pipe_depth == 3 and c.grid == 2048 and c.threads == 192
     assert c.num_tiles == 1024 and c.k_blocks == 128 and c.tmem_cols == 512
+    assert (c.dp_tiles, c.sk_tiles, c.workspace_bytes) == (1024, 0, 0)
     # both CTAs' A and half-B tiles, two 64-wide K blocks each
     assert c.tx_bytes == 2 * 2 * (128 * 64 + 128 * 64) * 2
     # an explicit ring depth keeps stages of one 64-wide block
@@ -141,7 +142,8 @@ def test_pair_variant_constraints(b):
 def test_dynamic_pair_configuration(b):
     # One cluster per pair tile; the clusters that run cancel the others
     # ("GEMM II -- pipelining with TMA", Step 6: cluster launch control).
-    st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(variant="dynamic_2cta"))
+    st, c = b.gemm_select_config(8192, 8192, 8192, 1,
+                                 b.make_options(variant="dynamic_2cta", stream_k="off"))
     assert st == 0, b.last_error()
     assert c.variant == b.GEMM_VAR_DYNAMIC_2CTA
     assert (c.block_m, c.block_n, c.pipe_depth, c.threads, c.tmem_cols) == (256, 256, 3, 192, 512)
@@ -153,15 +155,16 @@ def test_dynamic_pair_configuration(b):
     st, _ = b.gemm_select_config(8192, 8192, 8192, 1,
                                  b.make_options(variant="dynamic_2cta", grid=152))
     assert st == b.GEMM_ERR_INVALID_ARG and "grid" in b.last_error()
-    st, _ = b.gemm_select_config(8192, 8192, 8192, 1,
+    st, c = b.gemm_select_config(8192, 8192, 8192, 1,
                                  b.make_options(variant="dynamic_2cta", stream_k="on"))
-    assert st == b.GEMM_ERR_UNSUPPORTED and "stream-K" in b.last_error()
+    assert st == 0 and (c.dp_tiles, c.sk_tiles, c.sk_max_contrib) == (988, 36, 2)
     st, _ = b.gemm_select_config(8192, 8192, 8192, 1,
                                  b.make_options(variant="dynamic_2cta", block_n=64))
     assert st == b.GEMM_ERR_INVALID_ARG
     # the schedule query reports each cluster's own tile; the rest is decided
     # while the kernel runs
-    st, c = b.gemm_select_config(1000, 1000, 520, 1, b.make_options(variant="dynamic_2cta"))
+    st, c = b.gemm_select_config(1000, 1000, 520, 1,
+                                 b.make_options(variant="dynamic_2cta", stream_k="off"))
     assert st == 0
     for w in range(c.grid // 2):
         assert b.gemm_worker_units(c, w) == [(w, 0, c.k_blocks, 0, 1)]
@@ -197,6 +200,38 @@ def test_two_pair_cluster_configuration(b):
         assert b.gemm_worker_units(c, w) == [(w, 0, c.k_blocks, 0, 1)]
 
 
+def test_dynamic_split_tail(b):
+    # With stream_k = 2 the dynamic schedule splits the tiles of a partial last
+    # wave into S equal K ranges, S = clusters // leftover tiles (at most 4, at
+    # least 4 stages each); none when the waves are whole or S would be 1.
+    def cfg(M, N, K, **o):
+        o.setdefault("stream_k", "on")
+        st, c = b.gemm_select_config(M, N, K, 1, b.make_options(variant="dynamic_2cta", **o))
+        assert st == 0, b.last_error()
+        return c
+    c = cfg(8192, 8192, 8192)
+    assert (c.dp_tiles, c.sk_tiles, c.sk_max_contrib, c.grid) == (988, 36, 2, 2 * 1060)
+    c = cfg(1024, 1024, 4096, block_n=256)   # 16 tiles < 76 clusters: 4 ranges each
+    assert (c.num_tiles, c.dp_tiles, c.sk_tiles, c.sk_max_contrib) == (16, 0, 16, 4)
+    assert c.grid == 2 * 64
+    c = cfg(1024, 1024, 256, block_n=256)    # 2 stages: too short to split
+    assert c.sk_tiles == 0 and c.grid == 2 * 16
+    c = cfg(1024, 1024, 1024, block_n=256)   # 8 stages: two ranges of 4
+    assert (c.sk_tiles, c.sk_max_contrib) == (16, 2)
+    c = cfg(4096, 4096, 4096, block_n=224)   # 304 tiles = 4 whole waves
+    assert c.sk_tiles == 0 and c.grid == 608
+    c = cfg(8192, 8192, 8192, stream_k="off")
+    assert c.sk_tiles == 0 and c.grid == 2048
+    # the schedule query follows the split: each cluster's own unit
+    c = cfg(1024, 1024, 4096, block_n=256)
+    ks = c.block_k // 64
+    stages = (c.k_blocks + ks - 1) // ks
+    for w in range(c.grid // 2):
+        tile, part = divmod(w, 4)
+        kb0, kb1 = part * stages // 4 * ks, min((part + 1) * stages // 4 * ks, c.k_blocks)
+        assert b.gemm_worker_units(c, w) == [(tile, kb0, kb1, part, 4)]
+
+
 def test_block_k_128_stages(b):
     # a stage of K = 128 as two 128-byte swizzle groups of 64 fp16 ("05 Async
     # Data Movement - TMA", Using 3D TMA to Move Multiple Swizzle Atoms): twice
@@ -221,9 +256,9 @@ def test_block_k_128_stages(b):
         variant="persistent_2cta", block_k=128, stream_k="on"))
     assert st == 0 and c.block_k == 128 and c.sk_tiles == 1024 % 76
     assert c.sk_kb_per_worker == -(-(c.sk_tiles * 64) // 76)
-    st, _ = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(
+    st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(
         variant="dynamic_2cta", block_k=128, stream_k="on"))
-    assert st == b.GEMM_ERR_UNSUPPORTED
+    assert st == 0 and (c.block_k, c.sk_tiles, c.sk_max_contrib) == (128, 36, 2)  # split tail
     st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(block_k=64))
     assert st == 0 and c.block_k == 64 and c.pipe_depth == 6
     # automatic: 128-wide stages only over 128-byte aligned rows (K % 64 == 0)
@@ -317,7 +352,10 @@ def test_swizzle_map_matches_page_rule_and_bank_analysis(b):
     (64, 16384, 16384, {"stream_k": "on"}),                   # every tile shared
     (1000, 1000, 520, {"variant": "persistent", "grid": 7, "stream_k": "on"}),
     (1000, 1000, 520, {"variant": "persistent_2cta", "grid": 10, "stream_k": "on"}),
-    (1000, 1000, 520, {"variant": "dynamic_2cta"}),           # own tile per cluster
+    (1000, 1000, 520, {"variant": "dynamic_2cta"}),           # own whole tile per cluster
+    (1000, 1000, 520, {"variant": "dynamic_2cta", "stream_k": "on"}),  # 28 tiles split in 2
+    (8192, 8192, 8192, {"variant": "dynamic_2cta", "stream_k": "on"}),  # 36-tile split tail
+    (1024, 1024, 4096, {"variant": "dynamic_2cta", "block_n": 256, "stream_k": "on"}),
     (300, 520, 64, {"variant": "persistent", "stream_k": "on"}),   # one K block per tile
 ])
 def test_work_units_cover_every_k_block_once(b, M, N, K, opts):
@@ -344,7 +382,12 @@ def test_work_units_cover_every_k_block_once(b, M, N, K, opts):
         lst.sort()
         assert [j for j, _, _, _ in lst] == list(range(lst[0][3]))  # ranks 0..n-1, once each
         assert all(a[2] == b_[1] for a, b_ in zip(lst, lst[1:]))     # ranks follow K order
-    if c.sk_tiles:
+    if c.sk_tiles and c.variant == b.GEMM_VAR_DYNAMIC_2CTA:
+        # a split tile's ranges differ by at most one stage
+        for lst in contribs.values():
+            sizes = [kb1 - kb0 for _, kb0, kb1, _ in lst]
+            assert max(sizes) - min(sizes) <= c.block_k // 64
+    elif c.sk_tiles:
         # equal shares: every worker's K-block count within one range of the others
         # shares are counted in pipeline stages of block_k / 64 K blocks
         assert max(work) - min(work) <= c.sk_kb_per_worker * (c.block_k // 64)

@@ -272,9 +272,9 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     if (is_dynamic(variant) && opts.grid != 0)
         return fail(GEMM_ERR_INVALID_ARG,
                     "the dynamic variants launch one cluster per work unit: grid must be 0 (auto)");
-    if (is_dynamic(variant) && opts.stream_k == 2)
+    if (variant == VAR_DYNAMIC_2X2 && opts.stream_k == 2)
         return fail(GEMM_ERR_UNSUPPORTED,
-                    "the dynamic variants schedule whole tiles: stream-K needs a static variant");
+                    "dynamic_2x2 schedules whole tiles: stream-K needs another pair variant");
     if (opts.block_k == 128 && !is_pair(variant))
         return fail(GEMM_ERR_INVALID_ARG, "block_k = 128 is built for the CTA-pair variants");
     // K blocks of 64 per stage (two 128-byte swizzle atoms at block_k = 128).
@@ -428,6 +428,34 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
                     sk * maxc * halves * static_cast<long long>(BLK_M) * bn * 4 +
                     ((sk * halves * 4 + 255) / 256) * 256;
             }
+        }
+    }
+    // Split tail of the dynamic pair schedule (stream_k = 2).  The tiles of a
+    // partial last wave -- all of them when there are fewer tiles than
+    // resident clusters -- are each cut into S equal K ranges, S =
+    // floor(clusters / those tiles) up to 4, so the clusters that would idle
+    // share them; every range keeps at least 4 stages.  The two to four
+    // partial tiles meet in the workspace and the last one to arrive sums them
+    // in K order and stores the tile.  Opt-in: measured on GB300 the fp32
+    // partial round trip through the workspace (latency-bound with four
+    // warps per CTA) costs what the shorter wave saves, or more.
+    if (variant == VAR_DYNAMIC_2CTA && opts.stream_k == 2) {
+        const int64_t cl = sms / 2;
+        const int64_t T = c->num_tiles;
+        const int64_t rem = T % cl;
+        int64_t S = rem ? cl / rem : 0;
+        if (S > 4) S = 4;
+        while (S >= 2 && KBLK / S < 4) --S;
+        if (S >= 2) {
+            const int64_t units = T - rem + S * rem;
+            if (2 * units > LIM) return fail(GEMM_ERR_UNSUPPORTED, "too many output tiles");
+            c->grid = static_cast<int>(2 * units);
+            c->dp_tiles = static_cast<int>(T - rem);
+            c->sk_tiles = static_cast<int>(rem);
+            c->sk_kb_per_worker = 0;
+            c->sk_max_contrib = static_cast<int>(S);
+            c->workspace_bytes = rem * S * 2 * static_cast<long long>(BLK_M) * bn * 4 +
+                                 ((rem * 2 * 4 + 255) / 256) * 256;
         }
     }
     return ok();
@@ -631,15 +659,21 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
     if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
     if (dev != plan->device)
         return fail(GEMM_ERR_INVALID_ARG, "plan was created on another device");
+    // Arrival tickets of split tiles are keyed by the run counter, which a
+    // graph replay repeats: a replayed ticket word would never rank a last
+    // arrival, and the shared tiles would stay unwritten.  A captured launch
+    // of the dynamic schedule therefore runs every tile whole; a static
+    // stream-K plan refuses capture.
+    bool whole_tiles = false;
     if (plan->cfg.sk_tiles > 0) {
-        // Stream-K arrival tickets are keyed by the run counter, which a graph
-        // replay repeats: a replayed ticket word would never rank a last
-        // arrival, and the shared tiles would stay unwritten.
         cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
         if (cudaStreamIsCapturing(static_cast<cudaStream_t>(cuda_stream), &cs) == cudaSuccess &&
-            cs != cudaStreamCaptureStatusNone)
-            return fail(GEMM_ERR_UNSUPPORTED,
-                        "a plan with stream-K tiles cannot be captured into a CUDA graph");
+            cs != cudaStreamCaptureStatusNone) {
+            if (!is_dynamic(plan->cfg.variant))
+                return fail(GEMM_ERR_UNSUPPORTED,
+                            "a plan with stream-K tiles cannot be captured into a CUDA graph");
+            whole_tiles = true;
+        }
     }
 
     const gemm_config& c = plan->cfg;
@@ -709,7 +743,13 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
     p.sk_max_contrib = c.sk_max_contrib;
     p.trace = plan->trace;
     p.trace_units = plan->trace_units;
-    if (c.sk_tiles > 0) {
+    if (whole_tiles) {
+        s.grid = 2 * c.num_tiles;
+        p.dp_tiles = c.num_tiles;
+        p.sk_tiles = 0;
+        p.sk_max_contrib = 1;
+    }
+    if (p.sk_tiles > 0) {
         const int halves = is_pair(c.variant) ? 2 : 1;
         const size_t partial_bytes = static_cast<size_t>(c.sk_tiles) * c.sk_max_contrib * halves *
                                      BLK_M * c.block_n * 4;
@@ -969,6 +1009,22 @@ int gemm_schedule_unit(const gemm_config* cfg, int worker, int index, int* tile,
     const int ks = cfg->block_k > BLK_K ? cfg->block_k / BLK_K : 1;
     const int stages = (cfg->k_blocks + ks - 1) / ks;
     const int dp = np == 1 ? cfg->dp_tiles : unit_grid(*cfg, 2).units;
+    if (is_dynamic(cfg->variant)) {
+        // the cluster's own unit; the rest is decided while the kernel runs
+        if (index > 0) {
+            ok();
+            return 0;
+        }
+        WorkUnit u;
+        dynamic_unit(worker, dp, cfg->sk_tiles > 0 ? cfg->sk_max_contrib : 1, stages, u);
+        *tile = u.tile;
+        *kb0 = u.kb0 * ks;
+        *kb1 = u.kb1 * ks < cfg->k_blocks ? u.kb1 * ks : cfg->k_blocks;
+        *contrib = u.contrib;
+        *ncontrib = u.ncontrib;
+        ok();
+        return 1;
+    }
     WorkIter it;
     it.init(worker, workers, dp, cfg->sk_tiles, stages, cfg->sk_kb_per_worker);
     WorkUnit u;

@@ -83,14 +83,17 @@ struct Params {
     int epoch;                  // run counter, > 0
     unsigned long long budget_ns;  // bound on any single wait
     int debug_stall;            // 1: producer first waits on a barrier nothing completes
-    // Stream-K tail (persistent kernels).  The first dp_tiles tiles of the
+    // Stream-K tail (static persistent kernels).  The first dp_tiles tiles of the
     // raster order (a multiple of the worker count) are whole tiles; the last
     // sk_tiles tiles are cut into K-block ranges of sk_kb_per_worker blocks,
     // one range per worker.  sk_tiles = 0: every tile is whole.
     int dp_tiles;
     int sk_tiles;
     int sk_kb_per_worker;
-    int sk_max_contrib;         // most workers that can share one tile
+    int sk_max_contrib;         // most workers that can share one tile; the
+                                // dynamic pair schedule splits each of its
+                                // sk_tiles last tiles into exactly this many
+                                // K ranges (a split tail, see dynamic_unit)
     float* sk_partials;         // [sk_tiles][sk_max_contrib][halves][tile rows x cols] fp32
     unsigned* sk_tickets;       // [sk_tiles][halves] arrival tickets (epoch << 8 | count)
     // Optional timeline (warp-specialised kernels): per CTA a header record
@@ -162,6 +165,33 @@ struct WorkUnit {
     int sk_index;
     int contrib, ncontrib;
 };
+
+// Work unit number u of the dynamic pair schedule (one cluster per unit).
+// Units below dp are the whole tiles 0..dp-1.  With a split tail, the tiles
+// dp, dp+1, ... of the partial last wave are each split into `splits` K
+// ranges of the tile's KB stages, one unit per range (units dp + splits * i
+// + c, c = 0..splits-1, for tile dp + i), so that the last wave has
+// splits times as many, shorter units for the clusters it would leave idle.
+TG_HD void dynamic_unit(int u, int dp, int splits, int KB, WorkUnit& w)
+{
+    if (u < dp || splits < 2) {
+        w.tile = u;
+        w.kb0 = 0;
+        w.kb1 = KB;
+        w.sk_index = -1;
+        w.contrib = 0;
+        w.ncontrib = 1;
+        return;
+    }
+    const int v = u - dp;
+    const int c = v % splits;
+    w.tile = dp + v / splits;
+    w.kb0 = (c * KB) / splits;
+    w.kb1 = ((c + 1) * KB) / splits;
+    w.sk_index = v / splits;
+    w.contrib = c;
+    w.ncontrib = splits;
+}
 
 // The sequence of work units of worker `w` out of `workers`: first the whole
 // tiles w, w + workers, ... below dp_tiles, then the worker's contiguous range

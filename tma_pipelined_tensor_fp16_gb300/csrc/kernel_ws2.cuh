@@ -125,9 +125,11 @@ __device__ __forceinline__ int clc_read(uint32_t bars, int use, Watchdog& wd, bo
 template <bool DYN, int NP>
 struct PairTiles {
     WorkIter it;  // static schedule
-    int own;      // dynamic: this cluster's own tile
-    int use;      // dynamic: responses read so far; -1 before the own tile
+    int own;      // dynamic: this cluster's own unit
+    int use;      // dynamic: responses read so far; -1 before the own unit
     int KB;
+    int dp;       // dynamic: units below dp are whole tiles
+    int splits;   // dynamic: K ranges per tile of the split tail (< 2: none)
 
     // Next unit for a single-thread reader (`arm` as in clc_read).
     __device__ __forceinline__ bool next(WorkUnit& u, uint32_t bars, Watchdog& wd, bool arm)
@@ -163,12 +165,7 @@ struct PairTiles {
     __device__ __forceinline__ bool take(WorkUnit& u, int t) const
     {
         if (t < 0) return false;
-        u.tile = t;
-        u.kb0 = 0;
-        u.kb1 = KB;
-        u.sk_index = -1;
-        u.contrib = 0;
-        u.ncontrib = 1;
+        dynamic_unit(t, dp, splits, KB, u);
         return true;
     }
 };
@@ -238,6 +235,8 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
     tiles0.own = cluster;
     tiles0.use = -1;
     tiles0.KB = KB;
+    tiles0.dp = DYN && p.sk_tiles > 0 ? p.dp_tiles : 0x7FFFFFFF;
+    tiles0.splits = DYN && p.sk_tiles > 0 ? p.sk_max_contrib : 1;
 
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
