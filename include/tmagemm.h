@@ -174,6 +174,13 @@ typedef struct {
     int a_rows;         /* rows of A per stage: 128, or 64 when M <= 64 (single-CTA
                            warp-specialised variants; the MMA still computes 128
                            rows and rows past M are never stored) */
+    int tail_halves;    /* GEMM_VAR_DYNAMIC_2CTA, automatic (stream_k = 0) with
+                           256-column tiles and stages of K = 128: when all the
+                           tiles fit in at most half the resident clusters (SM
+                           count / 4), each is computed as two 256 x 128 tiles
+                           by two clusters (no partial sums to combine); this
+                           is the number of tiles so split, 0 = none.  The grid
+                           is 2 x (num_tiles + tail_halves) CTAs */
 } gemm_config;
 
 /* Create a plan for C[M x N] = A[M x K] . B[N x K]^T on the current CUDA

@@ -232,6 +232,23 @@ def test_dynamic_split_tail(b):
         assert b.gemm_worker_units(c, w) == [(tile, kb0, kb1, part, 4)]
 
 
+def test_narrow_tiles_for_a_single_partial_wave(b):
+    # all tiles within half the clusters: each 256 x 256 tile runs as two
+    # 256 x 128 tiles on two clusters
+    st, c = b.gemm_select_config(1024, 1024, 4096, 1,
+                                 b.make_options(variant="dynamic_2cta", block_n=256))
+    assert st == 0 and (c.num_tiles, c.tail_halves, c.grid) == (16, 16, 64)
+    for w in range(c.grid // 2):
+        assert b.gemm_worker_units(c, w) == [(w // 2, 0, c.k_blocks, 0, 1)]
+    for M, N, K, opts in [(8192, 8192, 8192, {}),                      # many waves
+                          (1024, 1024, 4096, {"stream_k": "off"}),
+                          (1024, 1024, 4096, {"block_k": 64}),         # K = 64 stages
+                          (2560, 2560, 4096, {"block_n": 256}),        # 100 tiles
+                          (1024, 1024, 4096, {"block_n": 192})]:
+        st, c = b.gemm_select_config(M, N, K, 1, b.make_options(variant="dynamic_2cta", **opts))
+        assert st == 0 and c.tail_halves == 0, (M, N, K, opts)
+
+
 def test_block_k_128_stages(b):
     # a stage of K = 128 as two 128-byte swizzle groups of 64 fp16 ("05 Async
     # Data Movement - TMA", Using 3D TMA to Move Multiple Swizzle Atoms): twice

@@ -44,7 +44,8 @@ class gemm_config(ctypes.Structure):
                  "threads", "tiles_m", "tiles_n", "num_tiles", "k_blocks", "smem_bytes",
                  "tmem_cols", "tx_bytes", "dp_tiles", "sk_tiles", "sk_kb_per_worker",
                  "sk_max_contrib")] + [("workspace_bytes", ctypes.c_longlong),
-                                       ("a_rows", ctypes.c_int)]
+                                       ("a_rows", ctypes.c_int),
+                                       ("tail_halves", ctypes.c_int)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -123,6 +123,11 @@ struct Params {
     // stage of K = 128 as two 128-byte swizzle atoms, one barrier round trip
     // per 8 MMAs).  The single-CTA kernels use 1.
     int ksub;
+    // Dynamic pair schedule, narrow tail: the last `tail_halves` tiles are
+    // each computed as two half-width tiles (see dynamic_unit); 0 = none.
+    // Their B rows come through the kernel's second B tensor map, whose box
+    // is half as high.
+    int tail_halves;
 };
 
 // The i-th K block (i = 0, 1, ...) processed for work unit number `unit` of a
@@ -164,6 +169,7 @@ struct WorkUnit {
     int kb0, kb1;
     int sk_index;
     int contrib, ncontrib;
+    int half;  // 0: the whole tile; 1, 2: its left or right half-width tile
 };
 
 // Work unit number u of the dynamic pair schedule (one cluster per unit).
@@ -172,8 +178,24 @@ struct WorkUnit {
 // ranges of the tile's KB stages, one unit per range (units dp + splits * i
 // + c, c = 0..splits-1, for tile dp + i), so that the last wave has
 // splits times as many, shorter units for the clusters it would leave idle.
+//
+// A narrow tail (splits == 0, tail tiles dp, dp+1, ...) computes each tail
+// tile as two half-width tiles over the whole K instead: units dp + 2 * i + h
+// are tile dp + i's left (h = 0) and right (h = 1) halves, so no partial sums
+// need combining.
 TG_HD void dynamic_unit(int u, int dp, int splits, int KB, WorkUnit& w)
 {
+    w.half = 0;
+    if (u >= dp && splits == 0) {
+        w.tile = dp + (u - dp) / 2;
+        w.kb0 = 0;
+        w.kb1 = KB;
+        w.sk_index = -1;
+        w.contrib = 0;
+        w.ncontrib = 1;
+        w.half = 1 + (u - dp) % 2;
+        return;
+    }
     if (u < dp || splits < 2) {
         w.tile = u;
         w.kb0 = 0;
@@ -226,6 +248,7 @@ struct WorkIter {
             u.sk_index = -1;
             u.contrib = 0;
             u.ncontrib = 1;
+            u.half = 0;
             dp_next += workers;
             return true;
         }
@@ -242,6 +265,7 @@ struct WorkIter {
             u.sk_index = t;
             u.contrib = (sk_pos / L) - first;
             u.ncontrib = last - first + 1;
+            u.half = 0;
             sk_pos += kb1 - kb0;
             return true;
         }

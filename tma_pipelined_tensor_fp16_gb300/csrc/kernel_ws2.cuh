@@ -189,12 +189,20 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t x)
 template <int PAIR_BN, bool F16OUT, bool DYN, int KS, int NP = 1>
 __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
     k_ws2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-          const __grid_constant__ CUtensorMap tmC, const Params p)
+          const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB2,
+          const Params p)
 {
     static_assert(PAIR_BN % 32 == 0 && PAIR_BN >= 64 && PAIR_BN <= 256, "pair tile width");
     static_assert(!F16OUT || PAIR_BN % 64 == 0 || PAIR_BN % 64 == 32,
                   "fp16 output: 64-column sub-tiles plus at most one 32-column remainder");
     constexpr int HALF_BN = PAIR_BN / 2;  // B rows held by each CTA
+    // Half-width tiles of a narrow tail: PAIR_BN / 2 columns, HALF_BN / 2 rows
+    // of B per CTA (through tmB2), for the widths whose half the epilogue
+    // stores in whole sub-tiles.
+    constexpr int NARROW_BN = PAIR_BN / 2;
+    constexpr bool NARROW_OK =
+        NP == 1 && DYN && (F16OUT ? (NARROW_BN % 64 == 0 || NARROW_BN % 64 == 32)
+                                  : NARROW_BN % 32 == 0);
     constexpr int ACC = 2;
     // two accumulators of PAIR_BN columns, rounded up to a legal allocation
     constexpr uint32_t TMEM_COLS = pow2_at_least(ACC * PAIR_BN);
@@ -235,13 +243,18 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
     tiles0.own = cluster;
     tiles0.use = -1;
     tiles0.KB = KB;
-    tiles0.dp = DYN && p.sk_tiles > 0 ? p.dp_tiles : 0x7FFFFFFF;
-    tiles0.splits = DYN && p.sk_tiles > 0 ? p.sk_max_contrib : 1;
+    tiles0.dp = DYN && p.sk_tiles > 0      ? p.dp_tiles
+                : NARROW_OK && p.tail_halves > 0 ? p.num_tiles - p.tail_halves
+                                                 : 0x7FFFFFFF;
+    tiles0.splits = DYN && p.sk_tiles > 0 ? p.sk_max_contrib
+                    : NARROW_OK && p.tail_halves > 0 ? 0
+                                                     : 1;
 
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
         prefetch_tensormap(&tmC);
+        if (NARROW_OK && p.tail_halves > 0) prefetch_tensormap(&tmB2);
         for (int s = 0; s < D; ++s) {
             mbar_init(bar_addr(bars, BAR_FULL + s), 1);   // leader: its producer's expect_tx
             mbar_init(bar_addr(bars, BAR_EMPTY + s), NP);  // each leader's multicast commit
@@ -293,6 +306,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
         // ---------------------------------------------------- TMA producer
         // both CTAs' A and B, all KS blocks (a block past K arrives zero-filled)
         const uint32_t pair_tx = 2u * stage_tx_bytes(HALF_BN) * static_cast<uint32_t>(KS);
+        const uint32_t narrow_tx = 2u * stage_tx_bytes(HALF_BN / 2) * static_cast<uint32_t>(KS);
         const uint64_t pol_a = (p.l2_policy == 2) ? policy_evict_first() : policy_evict_last();
         const uint64_t pol_b = (p.l2_policy == 1) ? policy_evict_first() : policy_evict_last();
         const bool tr = p.trace && lane == 0;
@@ -332,8 +346,12 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
             int mt, nt;
             raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
             nt = nt * NP + static_cast<int>(pp);
+            const bool narrow = NARROW_OK && u.half != 0;
             const int m0 = mt * PAIR_BM + static_cast<int>(pr) * BLK_M;
-            const int nb = nt * PAIR_BN + static_cast<int>(pr) * HALF_BN;
+            const int nb = narrow ? nt * PAIR_BN + (u.half - 1) * NARROW_BN +
+                                        static_cast<int>(pr) * (HALF_BN / 2)
+                                  : nt * PAIR_BN + static_cast<int>(pr) * HALF_BN;
+            const CUtensorMap* mapB = narrow ? &tmB2 : &tmB;
             for (int ki = 0; ki < u.kb1 - u.kb0; ++ki) {
                 const int kb = kblock_at(ki, DYN ? t / p.snake_span : ui, u.kb0, u.kb1,
                                          p.k_snake);
@@ -345,7 +363,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
                     const uint32_t fb_local = bar_addr(bars, BAR_FULL + stage);
                     const uint32_t fb_leader = map_shared_rank(fb_local, leader_rank);
                     if (leader) {
-                        mbar_arrive_expect_tx(fb_local, pair_tx);
+                        mbar_arrive_expect_tx(fb_local, narrow ? narrow_tx : pair_tx);
                         ++armed;
                     }
 #pragma unroll
@@ -362,19 +380,19 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
                                 sA + slot * A_TILE_BYTES + pp * (A_TILE_BYTES / 2), &tmA,
                                 fb_leader, kx, m0 + static_cast<int>(pp) * (BLK_M / 2), mask);
                             if (p.l2_policy == 0)
-                                tma_load_2d_pair(sB + slot * b_tile_bytes(HALF_BN), &tmB,
+                                tma_load_2d_pair(sB + slot * b_tile_bytes(HALF_BN), mapB,
                                                  fb_leader, kx, nb);
                             else
-                                tma_load_2d_pair_hint(sB + slot * b_tile_bytes(HALF_BN), &tmB,
+                                tma_load_2d_pair_hint(sB + slot * b_tile_bytes(HALF_BN), mapB,
                                                       fb_leader, kx, nb, pol_b);
                         } else if (p.l2_policy == 0) {
                             tma_load_2d_pair(sA + slot * A_TILE_BYTES, &tmA, fb_leader, kx, m0);
-                            tma_load_2d_pair(sB + slot * b_tile_bytes(HALF_BN), &tmB, fb_leader,
+                            tma_load_2d_pair(sB + slot * b_tile_bytes(HALF_BN), mapB, fb_leader,
                                              kx, nb);
                         } else {
                             tma_load_2d_pair_hint(sA + slot * A_TILE_BYTES, &tmA, fb_leader, kx,
                                                   m0, pol_a);
-                            tma_load_2d_pair_hint(sB + slot * b_tile_bytes(HALF_BN), &tmB,
+                            tma_load_2d_pair_hint(sB + slot * b_tile_bytes(HALF_BN), mapB,
                                                   fb_leader, kx, nb, pol_b);
                         }
                     }
@@ -429,7 +447,8 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
     } else if (warp == 1) {
         if (leader) {
             // ----------------------------------------------- MMA issuer (leader)
-            constexpr uint32_t idesc = idesc_f16_f32(PAIR_BM, PAIR_BN);
+            constexpr uint32_t idesc_full = idesc_f16_f32(PAIR_BM, PAIR_BN);
+            constexpr uint32_t idesc_narrow = idesc_f16_f32(PAIR_BM, NARROW_BN);
             const bool tr = p.trace && lane == 0;
             int stage = 0;
             uint32_t phase = 0;
@@ -446,6 +465,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
                 if (tr) trace_unit(p, mui, TRACE_U_ACC_FREE, globaltimer_ns());
                 unsigned long long full_wait_ns = 0;
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PAIR_BN);
+                const uint32_t idesc = (NARROW_OK && u.half != 0) ? idesc_narrow : idesc_full;
                 for (int ki = 0; ki < u.kb1 - u.kb0; ++ki) {
                     const int kb = kblock_at(ki, DYN ? t / p.snake_span : mui, u.kb0, u.kb1,
                                              p.k_snake);
@@ -531,7 +551,14 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(empty_leader);
             };
-            if (u.ncontrib == 1) {
+            if (NARROW_OK && u.half != 0) {
+                if constexpr (NARROW_OK)
+                    epilogue_tma_store<NARROW_BN, F16OUT>(
+                        tmem_acc, q, lane, staging, &tmC, m0,
+                        nt * PAIR_BN + (u.half - 1) * NARROW_BN, p.M, p.N, sub_count,
+                        !wd.aborted, p.C);
+                release();
+            } else if (u.ncontrib == 1) {
                 epilogue_tma_store<PAIR_BN, F16OUT>(tmem_acc, q, lane, staging, &tmC, m0,
                                                     nt * PAIR_BN, p.M, p.N, sub_count,
                                                     !wd.aborted, p.C);
@@ -574,7 +601,7 @@ cudaError_t launch_pair_kernel(KernelT kernel, const LaunchSpec& s, cudaStream_t
 {
     cudaError_t e = ensure_smem_limit(kernel, s.smem_bytes);
     if (e != cudaSuccess) return e;
-    return launch_programmatic(kernel, s, PAIR_THREADS, stream);
+    return launch_programmatic(kernel, s, PAIR_THREADS, stream, s.tmB2 ? *s.tmB2 : *s.tmB);
 }
 
 // Launch k_ws2<block_n, f16out, DYN, KS, NP> for one of the built pair tile

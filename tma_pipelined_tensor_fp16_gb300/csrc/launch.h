@@ -32,6 +32,8 @@ struct LaunchSpec {
     const CUtensorMap* tmA;
     const CUtensorMap* tmB;
     const CUtensorMap* tmC;
+    const CUtensorMap* tmB2;  // CTA-pair kernel: B with half-height boxes (narrow
+                              // tail tiles); nullptr = the same as tmB
     Params p;
 };
 
@@ -71,9 +73,9 @@ cudaError_t ensure_smem_limit(KernelT kernel, unsigned bytes)
 // executes griddep_wait() before its first global-memory access, so it still
 // reads A and B and writes C only after everything earlier on the stream has
 // completed; it calls griddep_launch_dependents() after its set-up.
-template <typename KernelT>
+template <typename KernelT, typename... Maps>
 cudaError_t launch_programmatic(KernelT kernel, const LaunchSpec& s, int threads,
-                                cudaStream_t stream)
+                                cudaStream_t stream, const Maps&... extra_maps)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(s.grid));
@@ -85,7 +87,7 @@ cudaError_t launch_programmatic(KernelT kernel, const LaunchSpec& s, int threads
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, *s.tmA, *s.tmB, *s.tmC, s.p);
+    return cudaLaunchKernelEx(&cfg, kernel, *s.tmA, *s.tmB, *s.tmC, extra_maps..., s.p);
 }
 
 }  // namespace tg
