@@ -58,7 +58,11 @@ typedef enum {
                                        GEMM_VAR_DYNAMIC_2CTA, or
                                        GEMM_VAR_PERSISTENT_2CTA when the options
                                        set grid or stream_k = 2 -- else
-                                       GEMM_VAR_PERSISTENT */
+                                       GEMM_VAR_PERSISTENT.  When K % 64 != 0
+                                       (rows off 128-byte lines) and no width,
+                                       depth, stage or stream-K option is set,
+                                       GEMM_VAR_DYNAMIC_2X2 if a makespan model
+                                       predicts it at least 5 % faster */
     GEMM_VAR_SYNC_TILED = 1,        /* Step 3: thread copies, one MMA at a time */
     GEMM_VAR_TMA_SERIAL = 2,        /* Step 4: TMA load + expect_tx, serial loop */
     GEMM_VAR_PIPELINED = 3,         /* Step 5: PIPE_DEPTH ring, lock-step prefetch */

@@ -109,12 +109,28 @@ def test_headline_configuration(b):
 @pytest.mark.parametrize("M,N,K,dt,variant,bn", [(256, 256, 256, 0, 5, 64),
                                                  (4096, 4096, 4096, 1, 8, 224),
                                                  (8192, 8192, 8192, 1, 8, 256),
-                                                 (4000, 3000, 5000, 0, 8, 224),
+                                                 (4000, 3000, 5000, 0, 9, 256),
+                                                 (4000, 3000, 4992, 0, 8, 224),
+                                                 (8192, 8192, 8200, 1, 9, 256),
                                                  (64, 16384, 16384, 1, 5, 128),
                                                  (128, 65536, 64, 1, 5, 256)])
 def test_auto_variant_choice(b, M, N, K, dt, variant, bn):
     st, c = b.gemm_select_config(M, N, K, dt)
     assert st == 0 and c.variant == variant and c.block_n == bn
+
+
+def test_two_pairs_for_misaligned_rows_only_when_shorter(b):
+    # rows off 128-byte lines (K % 64 != 0): two pairs per cluster when the
+    # makespan model (waves over 36 four-CTA clusters x tile cost x 0.87)
+    # beats one pair per cluster (waves over 76) by 5 %
+    st, c = b.gemm_select_config(4000, 3000, 5000, 0)
+    assert (c.variant, c.block_n, c.block_k, c.grid) == (b.GEMM_VAR_DYNAMIC_2X2, 256, 64,
+                                                         4 * 16 * 6)
+    # aligned rows, explicit options or stream-K keep one pair per cluster
+    for K, opts in [(4992, {}), (5000, {"block_n": 256}), (5000, {"pipe_depth": 4}),
+                    (5000, {"stream_k": "off"}), (5000, {"stream_k": "on"})]:
+        st, c = b.gemm_select_config(4000, 3000, K, 0, b.make_options(**opts))
+        assert st == 0 and c.variant != b.GEMM_VAR_DYNAMIC_2X2, (K, opts)
 
 
 def test_pair_variant_constraints(b):

@@ -227,6 +227,57 @@ int auto_variant(int64_t M, int64_t N, int sms, const gemm_options& opts)
     return VAR_PERSISTENT;
 }
 
+// Resident clusters of four CTAs at the pair kernels' shared-memory size:
+// cudaOccupancyMaxActiveClusters gives 36 on GB300's 152 SMs (144 SMs; the
+// GPCs' TPC counts leave 8 SMs over), against SM count / 2 = 76 clusters of
+// two.
+int four_cta_clusters(int sms) { return sms >= 16 ? (sms / 2 - 4) / 2 : 1; }
+
+// Relative time of one tile of a CTA pair, 256 rows x `bn` columns, against a
+// 256 x 256 tile (the per-width tables of choose_pair_bn).
+double pair_tile_cost(int bn, int ksub)
+{
+    const int widths[5] = {256, 224, 192, 160, 128};
+    const double eff_k64[5] = {1.0, 0.92, 0.79, 0.73, 0.54};
+    const double eff_k128[5] = {1.0, 0.94, 0.89, 0.81, 0.70};
+    for (int i = 0; i < 5; ++i)
+        if (widths[i] == bn) return (bn / 256.0) / (ksub == 2 ? eff_k128[i] : eff_k64[i]);
+    return 1.0;
+}
+
+// Automatic plans for rows of A and B that do not start on 128-byte lines
+// (K % 64 != 0): every box row then straddles two lines, the main loop waits
+// on operand loads, and two pairs per cluster sharing A (dynamic_2x2) run a
+// pair tile in 0.87 of the time (measured, 4000 x 3000 x 5000: a wave of
+// 224-wide tiles 26.4 us against 30.4).  Fewer clusters fit, so the choice
+// compares makespans: waves x tile cost, over the built widths of each
+// variant, and takes dynamic_2x2 when it is at least 5 % shorter.  Returns
+// the chosen width for dynamic_2x2, or 0 to keep one pair per cluster.
+int misaligned_two_pair_width(int64_t M, int64_t N, int sms, int dtype)
+{
+    const int64_t tm = ceil_div(M, 2 * BLK_M);
+    const int64_t cl2 = sms / 2, cl4 = four_cta_clusters(sms);
+    double pair_t = 1e300, quad_t = 1e300;
+    int quad_bn = 0;
+    const int widths[5] = {256, 224, 192, 160, 128};
+    for (int bn : widths) {
+        const int64_t tn = ceil_div(N, bn);
+        if (pair_width_ok(bn, dtype, VAR_DYNAMIC_2CTA)) {
+            const double t = static_cast<double>(ceil_div(tm * tn, cl2)) * pair_tile_cost(bn, 1);
+            if (t < pair_t) pair_t = t;
+        }
+        if (pair_width_ok(bn, dtype, VAR_DYNAMIC_2X2)) {
+            const double t =
+                static_cast<double>(ceil_div(tm * ceil_div(tn, 2), cl4)) * pair_tile_cost(bn, 1) * 0.87;
+            if (t < quad_t) {
+                quad_t = t;
+                quad_bn = bn;
+            }
+        }
+    }
+    return quad_t < 0.95 * pair_t ? quad_bn : 0;
+}
+
 int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_options* o,
                        int sms, int smem_optin, gemm_config* c)
 {
@@ -266,7 +317,15 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
         return fail(GEMM_ERR_INVALID_ARG, "k_order must be 0 (auto), 1 (ascending) or 2 (snake)");
     if (sms < 1 || smem_optin < 1) return fail(GEMM_ERR_INVALID_ARG, "bad device limits");
 
-    const int variant = opts.variant == VAR_AUTO ? auto_variant(M, N, sms, opts) : opts.variant;
+    int variant = opts.variant == VAR_AUTO ? auto_variant(M, N, sms, opts) : opts.variant;
+    if (opts.variant == VAR_AUTO && variant == VAR_DYNAMIC_2CTA && K % 64 != 0 &&
+        opts.block_n == 0 && opts.pipe_depth == 0 && opts.block_k != 128 && opts.stream_k == 0) {
+        const int qbn = misaligned_two_pair_width(M, N, sms, dtype);
+        if (qbn) {
+            variant = VAR_DYNAMIC_2X2;
+            opts.block_n = qbn;
+        }
+    }
     if (opts.debug_stall && !is_ws(variant))
         return fail(GEMM_ERR_INVALID_ARG, "debug_stall needs a warp-specialised variant");
     if (is_dynamic(variant) && opts.grid != 0)
