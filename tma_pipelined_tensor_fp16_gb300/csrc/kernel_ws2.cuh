@@ -196,9 +196,10 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
     static_assert(!F16OUT || PAIR_BN % 64 == 0 || PAIR_BN % 64 == 32,
                   "fp16 output: 64-column sub-tiles plus at most one 32-column remainder");
     constexpr int HALF_BN = PAIR_BN / 2;  // B rows held by each CTA
-    // Half-width tiles of a narrow tail: PAIR_BN / 2 columns, HALF_BN / 2 rows
-    // of B per CTA (through tmB2), for the widths whose half the epilogue
-    // stores in whole sub-tiles.
+    // Half-width tiles (the last p.tail_halves tiles of the dynamic schedule,
+    // each run as two units; see dynamic_unit): PAIR_BN / 2 columns,
+    // HALF_BN / 2 rows of B per CTA through tmB2, for the widths whose half
+    // the epilogue stores in whole sub-tiles.
     constexpr int NARROW_BN = PAIR_BN / 2;
     constexpr bool NARROW_OK =
         NP == 1 && DYN && (F16OUT ? (NARROW_BN % 64 == 0 || NARROW_BN % 64 == 32)
@@ -282,7 +283,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
         tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
         tmem_relinquish_alloc_permit_pair();
     }
-    // both CTAs' barriers exist before either touches the other's
+    // every CTA's barriers exist before any CTA of the cluster touches another's
     tc_fence_before_sync();
     cluster_sync_all();
     tc_fence_after_sync();
