@@ -10,7 +10,8 @@ NaN into C:
 
 * a torch kernel that writes A (an exact negation);
 * a GEMM whose fp16 output is the next GEMM's A operand (chained GEMMs), for
-  the CTA-pair kernel feeding the single-CTA kernel and the other way round.
+  the CTA-pair kernel feeding the single-CTA kernel, the two-pairs-per-cluster
+  kernel, and the other way round.
 """
 import numpy as np
 import pytest
@@ -32,7 +33,7 @@ def _built():
     __graft_entry__.build()
 
 
-@pytest.mark.parametrize("variant", ["dynamic_2cta", "persistent"])
+@pytest.mark.parametrize("variant", ["dynamic_2cta", "persistent", "dynamic_2x2"])
 def test_operand_written_by_the_previous_kernel(variant):
     import torch
 
@@ -59,7 +60,9 @@ def test_operand_written_by_the_previous_kernel(variant):
 
 
 @pytest.mark.parametrize("first,second", [("dynamic_2cta", "persistent"),
-                                          ("persistent", "dynamic_2cta")])
+                                          ("persistent", "dynamic_2cta"),
+                                          ("dynamic_2x2", "dynamic_2cta"),
+                                          ("dynamic_2cta", "dynamic_2x2")])
 def test_chained_gemms(first, second):
     import torch
 
