@@ -114,7 +114,8 @@ typedef struct {
     int pipe_depth;     /* shared-memory stages, 1..8 (ring variants) */
     int block_n;        /* output tile width: 64, 128 or 256 (tile height 128);
                            for the CTA-pair variant see GEMM_VAR_PERSISTENT_2CTA */
-    int group_m;        /* raster group height in M tiles (default 8) */
+    int group_m;        /* raster group height in M tiles (default 16 for CTA
+                           pairs, 8 otherwise) */
     int grid;           /* persistent variants: CTAs to launch (default: SM count) */
     int wait_budget_ms; /* bound on any single in-kernel wait (default 2000) */
     int debug_stall;    /* 1: the producer first waits on a barrier that nothing
