@@ -115,19 +115,25 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // The kernel's view of the tile grid: its work units are pair tiles, or (two
 // pairs per cluster) side-by-side pairs of them, so Params::tiles_n counts
-// unit columns; snake_span is the number of work units one full set of
-// clusters takes at a time.
+// unit columns and Params::num_tiles units.
 struct UnitGrid {
-    int tiles_n, units, snake_span;
+    int tiles_n, units;
 };
-UnitGrid unit_grid(const gemm_config& c, int sms)
+UnitGrid unit_grid(const gemm_config& c)
 {
     const int np = unit_pairs(c.variant);
     UnitGrid g;
     g.tiles_n = static_cast<int>(ceil_div(c.tiles_n, np));
     g.units = c.tiles_m * g.tiles_n;
-    g.snake_span = std::max(1, std::min(sms / (2 * np), g.units));
     return g;
+}
+
+// Work units one full set of resident clusters takes at a time: the dynamic
+// schedule flips a unit's K direction every snake_span units.
+int snake_span_of(const gemm_config& c, int sms)
+{
+    const int np = unit_pairs(c.variant);
+    return std::max(1, std::min(sms / (2 * np), unit_grid(c).units));
 }
 
 // Rows of A per TMA box: two pairs per cluster load half of each 128-row
@@ -506,11 +512,9 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     if (variant == VAR_DYNAMIC_2CTA && opts.stream_k == 0 && bn == 256 && ksub == 2) {
         const int64_t cl = sms / 2;
         const int64_t T = c->num_tiles;
-        const int64_t rem = T;
-        if (2 * rem <= cl) {
-            if (2 * (T + rem) > LIM) return fail(GEMM_ERR_UNSUPPORTED, "too many output tiles");
-            c->tail_halves = static_cast<int>(rem);
-            c->grid = static_cast<int>(2 * (T + rem));
+        if (2 * T <= cl) {  // every tile as two units: 2 T clusters of 2 CTAs
+            c->tail_halves = static_cast<int>(T);
+            c->grid = static_cast<int>(4 * T);
         }
     }
     // Split tail of the dynamic pair schedule (stream_k = 2).  The tiles of a
@@ -697,7 +701,7 @@ gemm_plan* gemm_create_plan_ex(int64_t M, int64_t N, int64_t K, int dtype_out,
     p->k_snake = (opts && opts->k_order == 1) ? 0 : 1;
     // The dynamic schedule takes each tile's K direction from the tile index,
     // as the static schedule of a full grid (SM count / 2 clusters) would.
-    p->snake_span = unit_grid(p->cfg, sms).snake_span;
+    p->snake_span = snake_span_of(p->cfg, sms);
     e = cudaMalloc(&p->d_status, sizeof(DevStatus));
     if (e == cudaSuccess) e = cudaMemset(p->d_status, 0, sizeof(DevStatus));
     if (e == cudaSuccess && p->cfg.workspace_bytes > 0) {
@@ -805,7 +809,7 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
     p.K = static_cast<int>(plan->K);
     p.tiles_m = c.tiles_m;
     {
-        const UnitGrid ug = unit_grid(c, 2);  // (snake_span comes from the plan)
+        const UnitGrid ug = unit_grid(c);
         p.tiles_n = ug.tiles_n;
         p.num_tiles = ug.units;
     }
@@ -1097,7 +1101,7 @@ int gemm_schedule_unit(const gemm_config* cfg, int worker, int index, int* tile,
     // the kernels count K in pipeline stages of `ks` K blocks; report blocks
     const int ks = cfg->block_k > BLK_K ? cfg->block_k / BLK_K : 1;
     const int stages = (cfg->k_blocks + ks - 1) / ks;
-    const int dp = np == 1 ? cfg->dp_tiles : unit_grid(*cfg, 2).units;
+    const int dp = np == 1 ? cfg->dp_tiles : unit_grid(*cfg).units;
     if (is_dynamic(cfg->variant)) {
         // the cluster's own unit; the rest is decided while the kernel runs
         if (index > 0) {
@@ -1272,7 +1276,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
     p.tiles_m = c.tiles_m;
-    const UnitGrid ug = unit_grid(c, sms);
+    const UnitGrid ug = unit_grid(c);
     p.tiles_n = ug.tiles_n;
     p.num_tiles = ug.units;
     p.k_blocks = c.k_blocks;
@@ -1297,7 +1301,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     p.sk_tickets = nullptr;
     p.a_rows = c.a_rows;
     p.k_snake = 1;
-    p.snake_span = ug.snake_span;
+    p.snake_span = snake_span_of(c, sms);
     p.ksub = c.block_k / BLK_K;
     e = is_pair(c.variant) ? launch_pair(s, stream) : launch_ws(s, stream);
     if (e != cudaSuccess) return cuda_fail("kernel launch", e);
