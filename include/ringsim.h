@@ -1,0 +1,119 @@
+/* ringsim.h -- host-side model of the stage-ring protocols (C ABI).
+ *
+ * A discrete-event model of the load/compute handshake that the GEMM kernels
+ * implement with mbarriers, TMA copies and tcgen05 MMAs.  It serves two
+ * purposes:
+ *
+ * 1. Protocol checking.  mbarriers are modelled with an arrival count, a
+ *    pending transaction-byte count and a completed-phase counter ("05 Async
+ *    Data Movement - TMA", How to Wait for a TMA Load: a phase completes only
+ *    after both the arrivals and the pending bytes reach zero; a wait on
+ *    parity p returns once the phase of parity p has completed).  Stage slots
+ *    and accumulators carry the identity and landed byte count of what they
+ *    hold, so that a read of bytes that have not landed or of a stale round,
+ *    and a write over data still being read, are detected.  Faults of the
+ *    kinds the pages warn about can be injected: a wrong byte budget, a budget
+ *    announced several times, a missed phase flip, phases reset to 0 at every
+ *    persistent tile, a refill issued before the MMA reading the slot is done,
+ *    an epilogue that does not wait for its accumulator.  The model reports
+ *    deadlock (nothing can progress and nothing is in flight) or the first
+ *    hazard.
+ *
+ * 2. Timing.  With a fixed load time per copy and a fixed MMA time per stage
+ *    ("GEMM II -- pipelining with TMA", the interactive pipeline Gantt: serial
+ *    vs prefetch, PIPE_DEPTH, K tiles, load : MMA cost) it reports the
+ *    makespan, the tensor-pipe idle fraction, whether the MMAs run back to
+ *    back and the most loads in flight.
+ *
+ * Protocols:
+ *   RINGSIM_LOCKSTEP   one thread per CTA: prologue loads of the first
+ *                      PIPE_DEPTH stages, then per K block wait(tma_bar[s]),
+ *                      MMA, wait(mma_bar), refill slot s with block k + D
+ *                      ("GEMM II", Step 5; depth 1 is Step 4's serial loop),
+ *                      per-stage TMA barriers and one MMA barrier, the TMA
+ *                      phase flipped when the ring wraps and the MMA phase
+ *                      every iteration.
+ *   RINGSIM_WARP_SPEC  the warp-specialised kernels of this library: a
+ *                      producer (wait empty[s], arrive.expect_tx(full[s]),
+ *                      two copies), an MMA issuer (wait full[s], MMA,
+ *                      commit -> empty[s]; at the end of a tile commit ->
+ *                      tmem_full[a]) and an epilogue (wait tmem_full[a], read,
+ *                      arrive tmem_empty[a]) with `accumulators` TMEM buffers;
+ *                      ring position and phases run on across tiles.
+ *
+ * No GPU is involved; results are deterministic. */
+#ifndef RINGSIM_H
+#define RINGSIM_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(_WIN32)
+#define RINGSIM_API __declspec(dllexport)
+#else
+#define RINGSIM_API __attribute__((visibility("default")))
+#endif
+
+enum { RINGSIM_LOCKSTEP = 0, RINGSIM_WARP_SPEC = 1 };
+
+enum {
+    RINGSIM_OK = 0,
+    RINGSIM_DEADLOCK = 1,      /* no role can progress and nothing is in flight */
+    RINGSIM_EARLY_READ = 2,    /* a stage or accumulator read before its data was complete */
+    RINGSIM_OVERWRITE = 3,     /* a stage or accumulator written while still being read */
+    RINGSIM_EXTRA_ARRIVAL = 4, /* more arrivals on a barrier phase than it expects */
+    RINGSIM_BAD_ARG = 5
+};
+
+typedef struct {
+    int protocol;          /* RINGSIM_LOCKSTEP or RINGSIM_WARP_SPEC */
+    int depth;             /* PIPE_DEPTH, 1..64 */
+    int k_tiles;           /* K blocks per output tile, >= 1 */
+    int tiles;             /* output tiles processed in sequence by one CTA, >= 1 */
+    int accumulators;      /* warp-specialised: TMEM accumulator buffers, 1 or 2 */
+    double load_time;      /* time from a copy's issue to its bytes landing */
+    double mma_time;       /* tensor-pipe time of one stage's MMAs */
+    double epilogue_time;  /* time to drain one accumulator */
+    double issue_latency;  /* time a role spends between a completed wait and its issue */
+    long long stage_bytes; /* bytes of one stage (two copies of half each) */
+    int chunks;            /* each copy's bytes land in this many equal parts (>= 1) */
+    /* fault injection (0 = off) */
+    long long bytes_delta;     /* the announced byte budget is stage_bytes + bytes_delta */
+    int announce_times;        /* the budget is announced this many times (1 = correct; 0 = 1) */
+    int skip_phase_flip;       /* the issuing side never flips its ring phase */
+    int reset_phase_per_tile;  /* ring position and phases restart at 0 at every tile */
+    int refill_before_mma;     /* lock-step: refill a slot before waiting for its MMA */
+    int epilogue_no_wait;      /* warp-specialised: the epilogue skips its accumulator wait */
+} ringsim_config;
+
+typedef struct {
+    int status;                /* RINGSIM_* */
+    double makespan;           /* end of the last activity */
+    double mma_busy;           /* total tensor-pipe busy time */
+    double idle_fraction;      /* 1 - mma_busy / makespan */
+    int mma_back_to_back;      /* 1 if every MMA after the first started as the previous ended */
+    int max_loads_in_flight;   /* most copies issued and not yet landed at once */
+    int stages_consumed;       /* stages whose MMAs were issued */
+    int tiles_stored;          /* accumulators drained by the epilogue */
+    int roles_unique;          /* 1 if every barrier had one arriving and one waiting role */
+    char detail[256];          /* the hazard or deadlock, in words */
+} ringsim_result;
+
+/* Run one configuration.  Returns the result's status (RINGSIM_BAD_ARG, with
+ * a message in `detail`, for an invalid configuration). */
+RINGSIM_API int ringsim_run(const ringsim_config* cfg, ringsim_result* out);
+
+/* The byte-count handshake of one barrier phase ("05 Async Data Movement -
+ * TMA", How to Wait for a TMA Load): a barrier expecting one arrival, one
+ * arrive.expect_tx(bytes_a + bytes_b), then the two copies' complete-tx.
+ * Writes three states (after expect_tx, after the first copy, after the
+ * second), each as {pending arrivals, pending bytes, phase completed 0/1},
+ * into `states` (9 values). */
+RINGSIM_API void ringsim_byte_trace(long long bytes_a, long long bytes_b, long long* states);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RINGSIM_H */
