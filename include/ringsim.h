@@ -40,6 +40,15 @@
  *                      tmem_full[a]) and an epilogue (wait tmem_full[a], read,
  *                      arrive tmem_empty[a]) with `accumulators` TMEM buffers;
  *                      ring position and phases run on across tiles.
+ *   RINGSIM_PAIR       the CTA-pair kernel with `pairs` pairs per cluster: a
+ *                      producer in every CTA, the MMA issuer and its barriers
+ *                      in each pair's leader.  Both CTAs' copies of a stage
+ *                      signal the leader's full[s] (armed once with the pair's
+ *                      bytes); the leader's commit frees empty[s] in every CTA
+ *                      whose stage it read from or whose producer writes into
+ *                      it.  With two pairs, the CTAs of equal rank share A: each
+ *                      loads one half into both, so empty[s] counts an arrival
+ *                      from each leader.
  *
  * No GPU is involved; results are deterministic. */
 #ifndef RINGSIM_H
@@ -55,7 +64,7 @@ extern "C" {
 #define RINGSIM_API __attribute__((visibility("default")))
 #endif
 
-enum { RINGSIM_LOCKSTEP = 0, RINGSIM_WARP_SPEC = 1 };
+enum { RINGSIM_LOCKSTEP = 0, RINGSIM_WARP_SPEC = 1, RINGSIM_PAIR = 2 };
 
 enum {
     RINGSIM_OK = 0,
@@ -67,16 +76,16 @@ enum {
 };
 
 typedef struct {
-    int protocol;          /* RINGSIM_LOCKSTEP or RINGSIM_WARP_SPEC */
+    int protocol;          /* RINGSIM_LOCKSTEP, RINGSIM_WARP_SPEC or RINGSIM_PAIR */
     int depth;             /* PIPE_DEPTH, 1..64 */
     int k_tiles;           /* K blocks per output tile, >= 1 */
     int tiles;             /* output tiles processed in sequence by one CTA, >= 1 */
-    int accumulators;      /* warp-specialised: TMEM accumulator buffers, 1 or 2 */
+    int accumulators;      /* warp-specialised and pair: TMEM accumulator buffers, 1 or 2 */
     double load_time;      /* time from a copy's issue to its bytes landing */
     double mma_time;       /* tensor-pipe time of one stage's MMAs */
     double epilogue_time;  /* time to drain one accumulator */
     double issue_latency;  /* time a role spends between a completed wait and its issue */
-    long long stage_bytes; /* bytes of one stage (two copies of half each) */
+    long long stage_bytes; /* bytes of one stage of one CTA (two copies of half each: A and B) */
     int chunks;            /* each copy's bytes land in this many equal parts (>= 1) */
     /* fault injection (0 = off) */
     long long bytes_delta;     /* the announced byte budget is stage_bytes + bytes_delta */
@@ -85,6 +94,9 @@ typedef struct {
     int reset_phase_per_tile;  /* ring position and phases restart at 0 at every tile */
     int refill_before_mma;     /* lock-step: refill a slot before waiting for its MMA */
     int epilogue_no_wait;      /* warp-specialised: the epilogue skips its accumulator wait */
+    int pairs;                 /* RINGSIM_PAIR: CTA pairs per cluster, 1 or 2 (0 = 1) */
+    int commit_own_pair_only;  /* RINGSIM_PAIR fault: a leader frees only its own pair's stages */
+    int empty_count_one;       /* RINGSIM_PAIR fault: empty[s] expects one arrival with two pairs */
 } ringsim_config;
 
 typedef struct {

@@ -14,6 +14,11 @@
   fail when a stage completes an odd number of phases per tile, a refill
   before the MMA is done overwrites, an epilogue that does not wait reads an
   incomplete accumulator.
+* The CTA-pair protocol (one or two pairs per cluster) runs clean over the
+  same sweep; with two pairs sharing A, a leader that frees only its own
+  pair's stages deadlocks (empty[s] waits for the other leader), and an
+  empty[s] that counts one arrival lets a producer overwrite a stage the
+  other pair is still reading.
 """
 import os
 import re
@@ -196,3 +201,61 @@ def test_bad_arguments(rs):
         assert rs.run(**kw)["status_name"] == "bad argument", kw
     with pytest.raises(TypeError):
         rs.run(no_such_option=1)
+
+
+@pytest.mark.parametrize("pairs", [1, 2])
+@pytest.mark.parametrize("D", [1, 2, 3, 4, 6])
+def test_pair_protocol_runs_clean(rs, pairs, D):
+    for K in sorted({1, max(1, D - 1), D, D + 1, 2 * D + 1}):
+        for tiles in (1, 3):
+            for acc in (1, 2):
+                r = rs.run(protocol="pair", pairs=pairs, depth=D, k_tiles=K, tiles=tiles,
+                           accumulators=acc, chunks=3, epilogue_time=0.7, load_time=1.3,
+                           mma_time=1.0, issue_latency=0.1)
+                where = (pairs, D, K, tiles, acc, r["detail"])
+                assert r["status_name"] == "ok", where
+                assert r["stages_consumed"] == pairs * tiles * K, where
+                assert r["tiles_stored"] == pairs * tiles, where
+                assert r["roles_unique"] == 1, where
+
+
+def test_pairs_in_step_cost_nothing_over_one_pair(rs):
+    # when both pairs run in step, waiting for the other leader's commit
+    # before a refill adds no time
+    kw = dict(protocol="pair", depth=4, k_tiles=16, tiles=3, load_time=2.5, epilogue_time=2.0)
+    one, two = rs.run(pairs=1, **kw), rs.run(pairs=2, **kw)
+    assert one["status_name"] == two["status_name"] == "ok"
+    assert two["makespan"] == pytest.approx(one["makespan"])
+    assert two["mma_busy"] == pytest.approx(2 * one["mma_busy"])
+    assert two["idle_fraction"] == pytest.approx(one["idle_fraction"])
+
+
+def test_two_pairs_need_both_leaders_commits(rs):
+    kw = dict(protocol="pair", depth=4, k_tiles=8, tiles=2)
+    assert rs.run(pairs=2, **kw)["status_name"] == "ok"
+    own = rs.run(pairs=2, commit_own_pair_only=1, **kw)
+    assert own["status_name"] == "deadlock", own
+    one = rs.run(pairs=2, empty_count_one=1, **kw)
+    assert one["status_name"] == "overwrite", one
+    both = rs.run(pairs=2, commit_own_pair_only=1, empty_count_one=1, **kw)
+    assert both["status_name"] == "overwrite", both
+    # with one pair there is no other leader: both faults are no-ops
+    for fault in (dict(commit_own_pair_only=1), dict(empty_count_one=1)):
+        assert rs.run(pairs=1, **fault, **kw)["status_name"] == "ok", fault
+
+
+@pytest.mark.parametrize("pairs", [1, 2])
+def test_pair_byte_budget_faults(rs, pairs):
+    kw = dict(protocol="pair", pairs=pairs, depth=4, k_tiles=8, tiles=2)
+    big = rs.run(bytes_delta=16, **kw)
+    assert big["status_name"] == "deadlock" and "16 bytes pending" in big["detail"], big
+    # the leader arms its full[s] with one CTA's bytes instead of the pair's
+    small = rs.run(bytes_delta=-(128 * 64 + 128 * 64) * 2, chunks=2, **kw)
+    assert small["status_name"] == "early read", small
+    assert rs.run(epilogue_no_wait=1, **kw)["status_name"] == "early read"
+    assert rs.run(skip_phase_flip=1, **kw)["status_name"] != "ok"
+
+
+def test_pair_bad_arguments(rs):
+    for kw in (dict(pairs=3), dict(pairs=-1), dict(stage_bytes=6), dict(accumulators=0)):
+        assert rs.run(protocol="pair", **kw)["status_name"] == "bad argument", kw

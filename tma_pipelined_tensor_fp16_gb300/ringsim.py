@@ -6,7 +6,9 @@ uses:
 
 * protocol checking, with faults injected on the host (a wrong byte budget,
   a budget announced several times, a missed phase flip, phases reset per
-  persistent tile, an early refill, an epilogue that does not wait): the model
+  persistent tile, an early refill, an epilogue that does not wait, and for
+  the CTA-pair kernel a leader that frees only its own pair's stages or an
+  empty barrier that counts one arrival where two leaders commit): the model
   reports the deadlock or the first read of incomplete data;
 * the timing model of "GEMM II -- pipelining with TMA" (the interactive
   pipeline Gantt: serial vs prefetch, PIPE_DEPTH, K tiles, load : MMA cost),
@@ -26,7 +28,7 @@ SRC = os.path.join(HERE, "sim", "ringsim.cpp")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "ringsim.h")
 LIB_PATH = os.path.join(HERE, "libringsim.so")
 
-LOCKSTEP, WARP_SPEC = 0, 1
+LOCKSTEP, WARP_SPEC, PAIR = 0, 1, 2
 (OK, DEADLOCK, EARLY_READ, OVERWRITE, EXTRA_ARRIVAL, BAD_ARG) = range(6)
 STATUS_NAMES = {OK: "ok", DEADLOCK: "deadlock", EARLY_READ: "early read", OVERWRITE: "overwrite",
                 EXTRA_ARRIVAL: "extra arrival", BAD_ARG: "bad argument"}
@@ -40,7 +42,9 @@ class RingsimConfig(ctypes.Structure):
                 ("stage_bytes", ctypes.c_longlong), ("chunks", ctypes.c_int),
                 ("bytes_delta", ctypes.c_longlong), ("announce_times", ctypes.c_int),
                 ("skip_phase_flip", ctypes.c_int), ("reset_phase_per_tile", ctypes.c_int),
-                ("refill_before_mma", ctypes.c_int), ("epilogue_no_wait", ctypes.c_int)]
+                ("refill_before_mma", ctypes.c_int), ("epilogue_no_wait", ctypes.c_int),
+                ("pairs", ctypes.c_int), ("commit_own_pair_only", ctypes.c_int),
+                ("empty_count_one", ctypes.c_int)]
 
 
 class RingsimResult(ctypes.Structure):
@@ -91,19 +95,21 @@ DEFAULTS = dict(protocol=WARP_SPEC, depth=4, k_tiles=8, tiles=1, accumulators=2,
                 mma_time=1.0, epilogue_time=0.0, issue_latency=0.0,
                 stage_bytes=(128 * 64 + 128 * 64) * 2, chunks=2, bytes_delta=0,
                 announce_times=1, skip_phase_flip=0, reset_phase_per_tile=0,
-                refill_before_mma=0, epilogue_no_wait=0)
+                refill_before_mma=0, epilogue_no_wait=0, pairs=1, commit_own_pair_only=0,
+                empty_count_one=0)
 
 
 def run(**kw):
     """Run one configuration (keyword arguments as in ringsim_config; the
-    protocol may be given as "lockstep" or "warp_spec"); returns a dict."""
+    protocol may be given as "lockstep", "warp_spec" or "pair"); returns a dict."""
     args = dict(DEFAULTS)
     unknown = set(kw) - set(args)
     if unknown:
         raise TypeError("unknown ringsim option(s): %s" % sorted(unknown))
     args.update(kw)
     if isinstance(args["protocol"], str):
-        args["protocol"] = {"lockstep": LOCKSTEP, "warp_spec": WARP_SPEC}[args["protocol"]]
+        args["protocol"] = {"lockstep": LOCKSTEP, "warp_spec": WARP_SPEC,
+                            "pair": PAIR}[args["protocol"]]
     cfg = RingsimConfig(**args)
     res = RingsimResult()
     lib().ringsim_run(ctypes.byref(cfg), ctypes.byref(res))

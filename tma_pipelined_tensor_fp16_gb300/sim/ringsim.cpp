@@ -531,6 +531,427 @@ const char* role_name(int role)
 
 }  // namespace
 
+namespace {
+
+// The CTA-pair kernel (RINGSIM_PAIR): `pairs` pairs per cluster, CTAs 2p and
+// 2p + 1 forming pair p with its leader 2p.  Every CTA has a producer and
+// stage slots; each leader has the MMA issuer, full[s] and the accumulators;
+// every CTA has empty[s].  One epilogue role per pair stands for its eight
+// epilogue warps.  Role identities are counted by kind (producer, MMA issuer,
+// epilogue) for the unique-role check, since with two pairs both leaders'
+// commits free a stage by design.
+struct PairSim {
+    ringsim_config c{};
+    ringsim_result* r = nullptr;
+    int NP = 1, C = 2, D = 1, A = 2;
+    double now = 0.0;
+    long long seq = 0;
+    std::priority_queue<Event, std::vector<Event>, std::greater<Event>> events;
+    std::vector<Slot> slots;                  // [cta * D + s]
+    std::vector<Barrier> full, empty;         // [cta * D + s]
+    std::vector<Barrier> tmem_full, tmem_empty;  // [pair * A + a]
+    std::vector<Accum> accs;                  // [pair * A + a]
+    std::vector<double> pipe_free, last_end;  // per pair
+    std::vector<char> first;                  // per pair
+    int loads_in_flight = 0;
+    bool fault = false;
+
+    void fail(int status, const char* what)
+    {
+        if (fault) return;
+        fault = true;
+        r->status = status;
+        std::snprintf(r->detail, sizeof(r->detail), "t=%.3f: %s", now, what);
+    }
+    void push(Event e)
+    {
+        e.seq = seq++;
+        events.push(e);
+    }
+    void wake(RoleState& s, double t)
+    {
+        s.ready_at = t;
+        Event e{};
+        e.t = t;
+        e.kind = EV_WAKE;
+        push(e);
+    }
+
+    // A copy of `bytes` of round (tile, k) into CTA d's slot s, signalling
+    // the leader of d's pair.
+    void copy_into(int d, int s, int tile, int k, long long bytes)
+    {
+        Slot& sl = slots[d * D + s];
+        const bool same = sl.tile == tile && sl.k == k;
+        if (sl.readers > 0 || (!same && sl.copies > 0)) {
+            char m[200];
+            std::snprintf(m, sizeof(m),
+                          "CTA %d slot %d written with (tile %d, k %d) while (tile %d, k %d) is still %s",
+                          d, s, tile, k, sl.tile, sl.k, sl.readers ? "read by an MMA" : "landing");
+            fail(RINGSIM_OVERWRITE, m);
+            return;
+        }
+        if (!same) {
+            sl.tile = tile;
+            sl.k = k;
+            sl.landed = 0;
+        }
+        ++sl.copies;
+        ++loads_in_flight;
+        r->max_loads_in_flight = std::max(r->max_loads_in_flight, loads_in_flight);
+        const int parts = c.chunks < 1 ? 1 : c.chunks;
+        Barrier* bar = &full[(d & ~1) * D + s];
+        for (int i = 0; i < parts; ++i) {
+            Event e{};
+            e.t = now + c.load_time * static_cast<double>(i + 1) / parts;
+            e.kind = EV_BYTES;
+            e.slot = d * D + s;
+            e.tile = tile;
+            e.k = k;
+            e.bytes = bytes / parts + (i == parts - 1 ? bytes % parts : 0);
+            e.last = i == parts - 1;
+            e.bar = bar;
+            push(e);
+        }
+    }
+
+    void apply(const Event& e)
+    {
+        if (e.kind == EV_BYTES) {
+            Slot& sl = slots[e.slot];
+            if (sl.tile == e.tile && sl.k == e.k) sl.landed += e.bytes;
+            e.bar->complete_tx(e.bytes);
+            if (e.last) {
+                --sl.copies;
+                --loads_in_flight;
+            }
+        } else if (e.kind == EV_MMA_DONE) {
+            // e.slot: the pair's leader CTA * D + stage; both CTAs' slots were read
+            --slots[e.slot].readers;
+            --slots[e.slot + D].readers;
+            if (accs[e.acc].tile == e.tile) ++accs[e.acc].mmas_done;
+        } else if (e.kind == EV_COMMIT) {
+            if (!e.bar->arrive(ROLE_MMA))
+                fail(RINGSIM_EXTRA_ARRIVAL, "a commit arrived on a completed phase");
+        }
+    }
+
+    bool step_producer(RoleState& s, int cta)
+    {
+        const int K = c.k_tiles;
+        const int pr = cta & 1, pp = cta >> 1;
+        switch (s.pc) {
+        case 0:
+            if (s.tile == c.tiles) {
+                s.done = true;
+                return true;
+            }
+            s.k = 0;
+            s.pc = 1;
+            return true;
+        case 1:
+            if (!empty[cta * D + s.stage].passed(ROLE_PRODUCER, s.phase ^ 1u)) return false;
+            s.pc = 2;
+            wake(s, now + c.issue_latency);
+            return true;
+        case 2: {
+            if (now < s.ready_at) return false;
+            if (pr == 0) {
+                const int times = c.announce_times > 0 ? c.announce_times : 1;
+                const long long budget = (2 * c.stage_bytes + c.bytes_delta) * times;
+                if (!full[cta * D + s.stage].arrive_expect_tx(ROLE_PRODUCER, budget)) {
+                    fail(RINGSIM_EXTRA_ARRIVAL, "a second arrival on a full barrier phase");
+                    return true;
+                }
+            }
+            const long long half = c.stage_bytes / 2;  // A rows, and this CTA's half of B
+            copy_into(cta, s.stage, s.tile, s.k, c.stage_bytes - half);  // B
+            if (NP == 1) {
+                copy_into(cta, s.stage, s.tile, s.k, half);  // A
+            } else {
+                // this CTA's 64-row half of A, into both CTAs of its rank
+                const long long quarter = half / 2 + (pp == 1 ? half % 2 : 0);
+                copy_into(pr, s.stage, s.tile, s.k, quarter);
+                copy_into(2 + pr, s.stage, s.tile, s.k, quarter);
+            }
+            if (++s.stage == D) {
+                s.stage = 0;
+                if (!c.skip_phase_flip) s.phase ^= 1u;
+            }
+            if (++s.k == K) {
+                ++s.tile;
+                s.pc = 0;
+            } else {
+                s.pc = 1;
+            }
+            return true;
+        }
+        }
+        return false;
+    }
+
+    bool step_mma(RoleState& s, int pair)
+    {
+        const int K = c.k_tiles, L = 2 * pair;
+        switch (s.pc) {
+        case 0:
+            if (s.tile == c.tiles) {
+                s.done = true;
+                return true;
+            }
+            s.k = 0;
+            s.pc = 1;
+            return true;
+        case 1: {
+            if (!tmem_empty[pair * A + s.acc].passed(ROLE_MMA, s.phase2 ^ 1u)) return false;
+            Accum& a = accs[pair * A + s.acc];
+            if (!a.drained || a.draining) {
+                fail(RINGSIM_OVERWRITE, "MMA starts into an accumulator not yet drained");
+                return true;
+            }
+            a.tile = s.tile;
+            a.mmas_done = 0;
+            a.drained = false;
+            s.pc = 2;
+            return true;
+        }
+        case 2:
+            if (!full[L * D + s.stage].passed(ROLE_MMA, s.phase)) return false;
+            s.pc = 3;
+            wake(s, now + c.issue_latency);
+            return true;
+        case 3: {
+            if (now < s.ready_at) return false;
+            for (int d = L; d < L + 2; ++d) {
+                const Slot& sl = slots[d * D + s.stage];
+                if (sl.tile != s.tile || sl.k != s.k || sl.landed != c.stage_bytes) {
+                    char m[220];
+                    std::snprintf(m, sizeof(m),
+                                  "pair %d MMA of (tile %d, k %d) reads CTA %d slot %d holding (tile %d, k %d) "
+                                  "with %lld of %lld bytes landed",
+                                  pair, s.tile, s.k, d, s.stage, sl.tile, sl.k, sl.landed, c.stage_bytes);
+                    fail(RINGSIM_EARLY_READ, m);
+                    return true;
+                }
+            }
+            ++slots[L * D + s.stage].readers;
+            ++slots[(L + 1) * D + s.stage].readers;
+            const double start = std::max(pipe_free[pair], now);
+            if (!first[pair] && start > last_end[pair] + 1e-9) r->mma_back_to_back = 0;
+            first[pair] = 0;
+            pipe_free[pair] = start + c.mma_time;
+            last_end[pair] = pipe_free[pair];
+            r->mma_busy += c.mma_time;
+            ++r->stages_consumed;
+            Event done{};
+            done.t = pipe_free[pair];
+            done.kind = EV_MMA_DONE;
+            done.slot = L * D + s.stage;
+            done.tile = s.tile;
+            done.acc = pair * A + s.acc;
+            push(done);
+            // the commit frees the stage in both CTAs of the pair, and with
+            // two pairs in the other pair's CTAs too (their producers write
+            // their half of A into this pair's slots)
+            const int lo = (NP == 2 && !c.commit_own_pair_only) ? 0 : L;
+            const int hi = (NP == 2 && !c.commit_own_pair_only) ? C : L + 2;
+            for (int d = lo; d < hi; ++d) {
+                Event cm{};
+                cm.t = pipe_free[pair];
+                cm.kind = EV_COMMIT;
+                cm.bar = &empty[d * D + s.stage];
+                push(cm);
+            }
+            if (++s.stage == D) {
+                s.stage = 0;
+                if (!c.skip_phase_flip) s.phase ^= 1u;
+            }
+            if (++s.k == K) {
+                Event cm{};
+                cm.t = pipe_free[pair];
+                cm.kind = EV_COMMIT;
+                cm.bar = &tmem_full[pair * A + s.acc];
+                push(cm);
+                if (++s.acc == A) {
+                    s.acc = 0;
+                    s.phase2 ^= 1u;
+                }
+                ++s.tile;
+                s.pc = 0;
+            } else {
+                s.pc = 2;
+            }
+            return true;
+        }
+        }
+        return false;
+    }
+
+    bool step_epilogue(RoleState& s, int pair)
+    {
+        const int K = c.k_tiles;
+        switch (s.pc) {
+        case 0:
+            if (s.tile == c.tiles) {
+                s.done = true;
+                return true;
+            }
+            s.pc = 1;
+            return true;
+        case 1: {
+            if (!c.epilogue_no_wait &&
+                !tmem_full[pair * A + s.acc].passed(ROLE_EPILOGUE, s.phase2))
+                return false;
+            Accum& a = accs[pair * A + s.acc];
+            if (a.tile != s.tile || a.mmas_done != K) {
+                fail(RINGSIM_EARLY_READ, "the epilogue reads an accumulator before its MMAs are done");
+                return true;
+            }
+            a.draining = true;
+            s.pc = 2;
+            wake(s, now + c.epilogue_time);
+            return true;
+        }
+        case 2: {
+            if (now < s.ready_at) return false;
+            Accum& a = accs[pair * A + s.acc];
+            a.draining = false;
+            a.drained = true;
+            if (!tmem_empty[pair * A + s.acc].arrive(ROLE_EPILOGUE)) {
+                fail(RINGSIM_EXTRA_ARRIVAL, "a second arrival on an accumulator's empty barrier");
+                return true;
+            }
+            ++r->tiles_stored;
+            if (++s.acc == A) {
+                s.acc = 0;
+                s.phase2 ^= 1u;
+            }
+            ++s.tile;
+            s.pc = 0;
+            return true;
+        }
+        }
+        return false;
+    }
+
+    int run()
+    {
+        NP = c.pairs > 0 ? c.pairs : 1;
+        C = 2 * NP;
+        D = c.depth;
+        A = c.accumulators;
+        slots.resize(C * D);
+        full.resize(C * D);
+        empty.resize(C * D);
+        const int empty_expected = (NP == 2 && !c.empty_count_one) ? 2 : 1;
+        for (Barrier& b : empty) b.expected = b.pending = empty_expected;
+        tmem_full.resize(NP * A);
+        tmem_empty.resize(NP * A);
+        accs.resize(NP * A);
+        pipe_free.assign(NP, 0.0);
+        last_end.assign(NP, 0.0);
+        first.assign(NP, 1);
+        r->mma_back_to_back = 1;
+        // roles: producers 0..C-1, MMA issuers C..C+NP-1, epilogues after
+        std::vector<RoleState> roles(C + 2 * NP);
+        auto step = [&](int i) {
+            RoleState& s = roles[i];
+            if (s.done || fault) return false;
+            if (i < C) return step_producer(s, i);
+            if (i < C + NP) return step_mma(s, i - C);
+            return step_epilogue(s, i - C - NP);
+        };
+        long long budget_steps =
+            400LL * (c.tiles * static_cast<long long>(c.k_tiles) + 16) * C + 1000000;
+        while (!fault) {
+            bool progressed = true;
+            while (progressed && !fault && budget_steps >= 0) {
+                progressed = false;
+                for (int i = 0; i < static_cast<int>(roles.size()); ++i)
+                    while (step(i)) {
+                        progressed = true;
+                        if (--budget_steps < 0) break;
+                    }
+            }
+            if (fault) break;
+            if (budget_steps < 0) {
+                fail(RINGSIM_DEADLOCK, "step limit reached");
+                break;
+            }
+            bool all_done = true;
+            for (const RoleState& s : roles) all_done = all_done && s.done;
+            if (events.empty()) {
+                if (!all_done) {
+                    // MMA issuers first: their waits name the cause within the detail's length
+                    std::string stuck = "deadlock:";
+                    const int nroles = static_cast<int>(roles.size());
+                    for (int j = 0; j < nroles; ++j) {
+                        const int i = (j + C) % nroles;
+                        const RoleState& s = roles[i];
+                        if (s.done) continue;
+                        const Barrier* b;
+                        const char* who;
+                        const char* which;
+                        int idx, owner;
+                        unsigned parity;
+                        if (i < C) {
+                            who = "producer";
+                            idx = owner = i;
+                            b = &empty[i * D + s.stage];
+                            which = "empty";
+                            parity = s.phase ^ 1u;
+                        } else if (i < C + NP) {
+                            who = "MMA issuer";
+                            idx = i - C;
+                            owner = 2 * idx;
+                            if (s.pc == 1) {
+                                b = &tmem_empty[idx * A + s.acc];
+                                which = "tmem_empty";
+                                parity = s.phase2 ^ 1u;
+                            } else {
+                                b = &full[owner * D + s.stage];
+                                which = "full";
+                                parity = s.phase;
+                            }
+                        } else {
+                            who = "epilogue";
+                            idx = i - C - NP;
+                            owner = 2 * idx;
+                            b = &tmem_full[idx * A + s.acc];
+                            which = "tmem_full";
+                            parity = s.phase2;
+                        }
+                        char m[200];
+                        std::snprintf(m, sizeof(m),
+                                      " %s %d (tile %d, k %d) waits on CTA %d's %s parity %u "
+                                      "(%u done, %d arrivals, %lld bytes pending);",
+                                      who, idx, s.tile, s.k, owner, which, parity, b->completed,
+                                      b->pending, b->tx);
+                        stuck += m;
+                    }
+                    fail(RINGSIM_DEADLOCK, stuck.c_str());
+                }
+                break;
+            }
+            const Event e = events.top();
+            events.pop();
+            now = std::max(now, e.t);
+            apply(e);
+        }
+        r->makespan = now;
+        r->idle_fraction = now > 0 ? 1.0 - r->mma_busy / (now * NP) : 0.0;
+        bool unique = true;
+        for (const Barrier& b : full) unique = unique && b.roles_ok;
+        for (const Barrier& b : empty) unique = unique && b.roles_ok;
+        for (const Barrier& b : tmem_full) unique = unique && b.roles_ok;
+        for (const Barrier& b : tmem_empty) unique = unique && b.roles_ok;
+        r->roles_unique = unique ? 1 : 0;
+        return r->status;
+    }
+};
+
+}  // namespace
+
 extern "C" {
 
 RINGSIM_API int ringsim_run(const ringsim_config* cfg, ringsim_result* out)
@@ -544,18 +965,29 @@ RINGSIM_API int ringsim_run(const ringsim_config* cfg, ringsim_result* out)
     };
     if (!cfg) return bad("config is NULL");
     const ringsim_config& c = *cfg;
-    if (c.protocol != RINGSIM_LOCKSTEP && c.protocol != RINGSIM_WARP_SPEC)
-        return bad("protocol must be RINGSIM_LOCKSTEP or RINGSIM_WARP_SPEC");
+    if (c.protocol != RINGSIM_LOCKSTEP && c.protocol != RINGSIM_WARP_SPEC && c.protocol != RINGSIM_PAIR)
+        return bad("protocol must be RINGSIM_LOCKSTEP, RINGSIM_WARP_SPEC or RINGSIM_PAIR");
     if (c.depth < 1 || c.depth > 64) return bad("depth must be 1..64");
     if (c.k_tiles < 1 || c.k_tiles > 65535) return bad("k_tiles must be 1..65535");
     if (c.tiles < 1 || c.tiles > 100000) return bad("tiles must be 1..100000");
-    if (c.protocol == RINGSIM_WARP_SPEC && (c.accumulators < 1 || c.accumulators > 2))
+    if (c.protocol != RINGSIM_LOCKSTEP && (c.accumulators < 1 || c.accumulators > 2))
         return bad("accumulators must be 1 or 2");
+    if (c.protocol == RINGSIM_PAIR && (c.pairs < 0 || c.pairs > 2))
+        return bad("pairs must be 1 or 2");
+    if (c.protocol == RINGSIM_PAIR && c.stage_bytes % 4 != 0)
+        return bad("stage_bytes must be a multiple of 4 for CTA pairs");
     if (c.stage_bytes < 2 || c.load_time < 0 || c.mma_time < 0 || c.epilogue_time < 0 ||
         c.issue_latency < 0)
         return bad("stage_bytes >= 2 and non-negative times required");
-    if (c.stage_bytes + c.bytes_delta <= 0) return bad("the announced byte budget must be positive");
+    if ((c.protocol == RINGSIM_PAIR ? 2 : 1) * c.stage_bytes + c.bytes_delta <= 0)
+        return bad("the announced byte budget must be positive");
 
+    if (c.protocol == RINGSIM_PAIR) {
+        PairSim ps;
+        ps.c = c;
+        ps.r = out;
+        return ps.run();
+    }
     Sim sim;
     sim.c = c;
     sim.r = out;
