@@ -461,7 +461,7 @@ def main():
                 "peak_source": "%s hbm_gbs (copy)" % peak_kind}
     else:
         achieved = flops / avg_launch_s / 1e12
-        # A long timed region (or one the power limiter throttled) is judged
+        # A long timed region (or one the power limiter throttled) is measured
         # against the sustained figure, a short one against the burst figure.
         sustained = total_ms > 200.0 or "sw_power_cap" in clocks.get("reasons", [])
         key = "bf16_tflops_sustained" if sustained else "bf16_tflops"

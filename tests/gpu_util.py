@@ -5,7 +5,7 @@ Tolerances (written out here and used by every parity test):
 * fp32 output: max |C_gpu - C_ref| <= 1e-3 * sqrt(K).
 * fp16 output: per element |C_gpu - C_ref| <= 1e-2 * |C_ref| + 1e-3 * sqrt(K)
   (relative 1e-2, with an absolute floor so entries whose exact value is near
-  zero are not judged by a relative test they cannot meet).
+  zero are not held to a relative test they cannot meet).
 * small-integer inputs: bit-exact -- the exact integer result in fp32, or its
   round-to-nearest-even fp16 encoding as computed by the oracle's own encoder.
 """
