@@ -147,6 +147,14 @@ class ClockSampler:
             except OSError:
                 pass
         inside = [r for ts, r in rows if self.t0 is not None and self.t0 <= ts <= self.t1]
+        window = "inside the timed region"
+        if not inside and self.t0 is not None:
+            # A timed region shorter than the sampling period: take the
+            # samples closest to it (the warm-up just before, the tail just
+            # after), within 100 ms, and say so.
+            near = sorted(rows, key=lambda tr: max(self.t0 - tr[0], tr[0] - self.t1, 0.0))
+            inside = [r for ts, r in near[:3] if max(self.t0 - ts, ts - self.t1) <= 0.1]
+            window = "nearest samples within 100 ms of a timed region shorter than the sampling period"
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0,
                     "reasons": ["no nvidia-smi sample inside the timed region"]}
@@ -161,7 +169,7 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm),
                 "sm_max_mhz": float(inside[0][2]),
                 "power_w_max": max(power) if power else None,
-                "samples": len(inside), "reasons": sorted(reasons)}
+                "samples": len(inside), "window": window, "reasons": sorted(reasons)}
 
 
 # --------------------------------------------------------------- oracle timing
