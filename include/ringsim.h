@@ -49,6 +49,27 @@
  *                      it.  With two pairs, the CTAs of equal rank share A: each
  *                      loads one half into both, so empty[s] counts an arrival
  *                      from each leader.
+ *   RINGSIM_CLC        the response ring of the dynamic tile schedule
+ *                      (cluster launch control, which "GEMM II" Step 6 names
+ *                      as the successor of its precomputed tile assignment).
+ *                      One cluster of `pairs` CTA pairs takes `tiles` tiles:
+ *                      its own, then one per cancellation response.  The
+ *                      rank-0 producer requests at the start of each tile
+ *                      (wait clc_empty[j], try_cancel multicast into every
+ *                      CTA's slot j, landing `clc_latency` later and
+ *                      completing 16 bytes on that CTA's clc_full[j]).  Every
+ *                      reader -- each CTA's producer and four epilogue warps,
+ *                      each leader's MMA issuer: 11 per pair -- reads the
+ *                      next response after its tile (wait clc_full[j],
+ *                      decode; the producer re-arms its CTA's clc_full[j]
+ *                      with 16 bytes for the slot's next use) and arrives on
+ *                      the rank-0 CTA's clc_empty[j].  The last response
+ *                      cancels nothing and ends every reader.  Role timing:
+ *                      a tile's MMAs take k_tiles * mma_time, start
+ *                      load_time after its first loads, and may run D =
+ *                      depth stages behind the producer; an epilogue warp
+ *                      drains a tile in epilogue_time once its MMAs are done;
+ *                      `accumulators` tiles may be in flight between them.
  *
  * No GPU is involved; results are deterministic. */
 #ifndef RINGSIM_H
@@ -64,7 +85,7 @@ extern "C" {
 #define RINGSIM_API __attribute__((visibility("default")))
 #endif
 
-enum { RINGSIM_LOCKSTEP = 0, RINGSIM_WARP_SPEC = 1, RINGSIM_PAIR = 2 };
+enum { RINGSIM_LOCKSTEP = 0, RINGSIM_WARP_SPEC = 1, RINGSIM_PAIR = 2, RINGSIM_CLC = 3 };
 
 enum {
     RINGSIM_OK = 0,
@@ -76,11 +97,11 @@ enum {
 };
 
 typedef struct {
-    int protocol;          /* RINGSIM_LOCKSTEP, RINGSIM_WARP_SPEC or RINGSIM_PAIR */
+    int protocol;          /* RINGSIM_LOCKSTEP, RINGSIM_WARP_SPEC, RINGSIM_PAIR or RINGSIM_CLC */
     int depth;             /* PIPE_DEPTH, 1..64 */
     int k_tiles;           /* K blocks per output tile, >= 1 */
     int tiles;             /* output tiles processed in sequence by one CTA, >= 1 */
-    int accumulators;      /* warp-specialised and pair: TMEM accumulator buffers, 1 or 2 */
+    int accumulators;      /* warp-specialised, pair, CLC: TMEM accumulator buffers, 1 or 2 */
     double load_time;      /* time from a copy's issue to its bytes landing */
     double mma_time;       /* tensor-pipe time of one stage's MMAs */
     double epilogue_time;  /* time to drain one accumulator */
@@ -94,9 +115,15 @@ typedef struct {
     int reset_phase_per_tile;  /* ring position and phases restart at 0 at every tile */
     int refill_before_mma;     /* lock-step: refill a slot before waiting for its MMA */
     int epilogue_no_wait;      /* warp-specialised: the epilogue skips its accumulator wait */
-    int pairs;                 /* RINGSIM_PAIR: CTA pairs per cluster, 1 or 2 (0 = 1) */
+    int pairs;                 /* RINGSIM_PAIR, RINGSIM_CLC: CTA pairs per cluster, 1 or 2 (0 = 1) */
     int commit_own_pair_only;  /* RINGSIM_PAIR fault: a leader frees only its own pair's stages */
     int empty_count_one;       /* RINGSIM_PAIR fault: empty[s] expects one arrival with two pairs */
+    int clc_slots;             /* RINGSIM_CLC: response slots, 1..16 (0 = 4) */
+    double clc_latency;        /* RINGSIM_CLC: time from a request to its response landing */
+    int clc_readers_delta;     /* RINGSIM_CLC fault: clc_empty expects 11 * pairs + this arrivals */
+    int clc_no_rearm;          /* RINGSIM_CLC fault: the producer never re-arms clc_full */
+    int clc_rearm_after_release; /* RINGSIM_CLC: the producer re-arms after its release, issue_latency later */
+    int clc_request_late;      /* RINGSIM_CLC: the next request is issued at the end of a tile */
 } ringsim_config;
 
 typedef struct {
@@ -108,8 +135,12 @@ typedef struct {
     int max_loads_in_flight;   /* most copies issued and not yet landed at once */
     int stages_consumed;       /* stages whose MMAs were issued */
     int tiles_stored;          /* accumulators drained by the epilogue */
-    int roles_unique;          /* 1 if every barrier had one arriving and one waiting role */
+    int roles_unique;          /* 1 if every barrier had one arriving and one waiting role
+                                  (RINGSIM_CLC: always 1; its responses have many readers) */
     char detail[256];          /* the hazard or deadlock, in words */
+    double response_wait;      /* RINGSIM_CLC: time the requesting producer waited for responses */
+    double request_wait;       /* RINGSIM_CLC: time the requester waited for a free response slot */
+    int responses_read;        /* RINGSIM_CLC: responses read, summed over the readers */
 } ringsim_result;
 
 /* Run one configuration.  Returns the result's status (RINGSIM_BAD_ARG, with

@@ -10,8 +10,9 @@ schedule is the dynamic one (cluster launch control) over such units.
 
 Covers shapes with an odd number of tile columns (the last unit's second
 tile lies past N and must not be stored), one unit, units above the number
-of resident clusters, the three tile widths and both stage widths, integer
-inputs bit-exact, identity with the one-pair kernel when both walk K in the
+of resident clusters, some 114 units per resident cluster (the response
+ring wrapping many times), the three tile widths and both stage widths,
+integer inputs bit-exact, identity with the one-pair kernel when both walk K in the
 same order, the workload shapes, repeated launches, the unit sequence seen
 by the device timeline, and the watchdog.
 """
@@ -92,6 +93,23 @@ def test_2x2_equals_one_pair_kernel(bk):
                         k_order="up")
     assert np.array_equal(got.view(np.uint16), ref.view(np.uint16)), (desc, desc1)
     rows, cols = _sample(M, N, 2000, 88)
+    assert_close(got[rows, cols], oracle.gemm_entries(A, B, rows, cols), K, "f16", desc)
+
+
+def test_2x2_many_units_per_cluster():
+    # 4096 units (two 256-wide pair tiles each) over 36 resident clusters of
+    # four: about 114 cancellations per cluster, the four-slot response ring
+    # wrapping some 28 times.  The host model of that ring shows a reader
+    # miscount only after about 85 units per cluster with two pairs, so
+    # shorter runs could not catch one; a short K keeps this quick.
+    M, N, K = 65536, 8192, 128
+    A, B = inputs.make_operands(M, N, K, "uniform", 79)
+    got, guard, desc = run(A, B, "f16", guard_rows=2, variant=V, block_n=256, k_order="up")
+    assert np.isnan(guard.astype(np.float32)).all()
+    assert not np.isnan(got.astype(np.float32)).any(), desc
+    ref, _, desc1 = run(A, B, "f16", variant="dynamic_2cta", block_n=256, k_order="up")
+    assert np.array_equal(got.view(np.uint16), ref.view(np.uint16)), (desc, desc1)
+    rows, cols = _sample(M, N, 4000, 79)
     assert_close(got[rows, cols], oracle.gemm_entries(A, B, rows, cols), K, "f16", desc)
 
 

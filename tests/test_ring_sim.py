@@ -19,6 +19,15 @@
   pair's stages deadlocks (empty[s] waits for the other leader), and an
   empty[s] that counts one arrival lets a producer overwrite a stage the
   other pair is still reading.
+* The response ring of the dynamic tile schedule (cluster launch control)
+  runs clean for one to eight slots, one or two pairs, any response latency
+  and epilogue time; a reader count too high deadlocks; one reader too few
+  overwrites a response still unread, or deadlocks, only after a number of
+  tiles per cluster that grows with the slot count (beyond what one cluster
+  takes at 8192^3 with four slots); a producer that never re-arms its slot
+  deadlocks at the slot's second use; re-arming after the release is
+  benign.  Requesting at the
+  start of a tile hides a response latency shorter than the tile.
 """
 import os
 import re
@@ -259,3 +268,101 @@ def test_pair_byte_budget_faults(rs, pairs):
 def test_pair_bad_arguments(rs):
     for kw in (dict(pairs=3), dict(pairs=-1), dict(stage_bytes=6), dict(accumulators=0)):
         assert rs.run(protocol="pair", **kw)["status_name"] == "bad argument", kw
+
+
+CLC = dict(protocol="clc", depth=4, k_tiles=8, load_time=1.2, mma_time=1.0, tiles=9)
+
+
+@pytest.mark.parametrize("pairs", [1, 2])
+@pytest.mark.parametrize("slots", [1, 2, 4, 8])
+def test_clc_ring_runs_clean(rs, pairs, slots):
+    for tiles in (1, 2, 5, 17):
+        for latency in (0.0, 0.5, 3.0, 20.0):
+            for epi in (0.0, 2.0, 12.0):
+                for acc in (1, 2):
+                    r = rs.run(**dict(CLC, pairs=pairs, clc_slots=slots, tiles=tiles,
+                                      clc_latency=latency, epilogue_time=epi, accumulators=acc))
+                    where = (pairs, slots, tiles, latency, epi, acc, r["detail"])
+                    assert r["status_name"] == "ok", where
+                    assert r["tiles_stored"] == tiles, where
+                    # every reader (11 per pair) reads every response, the last
+                    # one included (it cancels nothing and ends the loop)
+                    assert r["responses_read"] == 11 * pairs * tiles, where
+                    assert r["stages_consumed"] == pairs * tiles * 8, where
+
+
+def test_clc_reader_count_too_high_deadlocks(rs):
+    r = rs.run(**dict(CLC, clc_readers_delta=1))
+    assert r["status_name"] == "deadlock" and "clc_empty" in r["detail"], r
+
+
+def _first_failing_tile_count(rs, limit, **kw):
+    for tiles in range(1, limit + 1):
+        r = rs.run(**dict(kw, tiles=tiles))
+        if r["status_name"] != "ok":
+            return tiles, r
+    return None, None
+
+
+@pytest.mark.parametrize("pairs", [1, 2])
+def test_clc_reader_count_too_low_shows_only_after_many_tiles(rs, pairs):
+    # One reader forgotten: each response's surplus arrival completes the
+    # slot's next phase one reader earlier, until the requester overwrites a
+    # response that epilogue warps have not read, or the parities fall out
+    # of step and it deadlocks.  With more slots this takes more tiles per
+    # cluster: with four slots more than a GPU run of 8192^3 gives a cluster
+    # (1024 tiles over 76 clusters), so only a long run or this model shows it.
+    kw = dict(CLC, pairs=pairs, epilogue_time=6.0, clc_readers_delta=-1)
+    n1, r1 = _first_failing_tile_count(rs, 400, clc_slots=1, **kw)
+    n4, r4 = _first_failing_tile_count(rs, 400, clc_slots=4, **kw)
+    assert n1 is not None and r1["status_name"] == "overwrite", r1
+    assert "have not read it" in r1["detail"]
+    assert n4 is not None and r4["status_name"] in ("overwrite", "deadlock"), r4
+    assert n4 > 3 * n1 and n4 > 1024 // 76, (n1, n4)
+
+
+def test_clc_missing_rearm_deadlocks_at_the_second_use(rs):
+    assert rs.run(**dict(CLC, clc_no_rearm=1, tiles=4))["status_name"] == "ok"
+    r = rs.run(**dict(CLC, clc_no_rearm=1, tiles=5))
+    assert r["status_name"] == "deadlock" and "-16 bytes pending" in r["detail"], r
+
+
+@pytest.mark.parametrize("slots", [1, 4])
+def test_clc_rearm_after_release_is_benign(rs, slots):
+    # the next response may land before the re-arm: its bytes count against
+    # the phase first, and the phase completes with the re-arm's arrival
+    r = rs.run(**dict(CLC, clc_slots=slots, clc_rearm_after_release=1, issue_latency=50.0))
+    assert r["status_name"] == "ok" and r["tiles_stored"] == 9, r
+    assert r["response_wait"] > 0
+
+
+def test_clc_request_at_tile_start_hides_the_latency(rs):
+    ref = rs.run(**dict(CLC, clc_latency=0.0))
+    early = rs.run(**dict(CLC, clc_latency=3.0))
+    late = rs.run(**dict(CLC, clc_latency=3.0, clc_request_late=1))
+    assert ref["status_name"] == early["status_name"] == late["status_name"] == "ok"
+    assert early["makespan"] == pytest.approx(ref["makespan"])
+    assert early["response_wait"] == 0
+    # requested at the end of each tile, every response (the last included)
+    # is waited for in full
+    assert late["response_wait"] == pytest.approx(9 * 3.0)
+    assert late["makespan"] > ref["makespan"]
+    # a latency longer than a tile is exposed even when requested early
+    slow = rs.run(**dict(CLC, clc_latency=12.0))
+    assert slow["response_wait"] > 0 and slow["makespan"] > ref["makespan"]
+
+
+def test_clc_one_slot_stalls_the_requester(rs):
+    # with one slot a request waits for the epilogue warps to read the
+    # previous response; two slots already remove the cost here
+    kw = dict(CLC, epilogue_time=6.0, clc_latency=2.0)
+    one, two, four = (rs.run(clc_slots=n, **kw) for n in (1, 2, 4))
+    assert one["status_name"] == two["status_name"] == four["status_name"] == "ok"
+    assert one["request_wait"] > two["request_wait"] > 0 and four["request_wait"] == 0
+    assert one["makespan"] > two["makespan"] == pytest.approx(four["makespan"])
+
+
+def test_clc_bad_arguments(rs):
+    for kw in (dict(clc_slots=17), dict(clc_slots=-1), dict(clc_latency=-1.0),
+               dict(clc_readers_delta=-11), dict(pairs=3)):
+        assert rs.run(protocol="clc", **kw)["status_name"] == "bad argument", kw

@@ -8,8 +8,10 @@ uses:
   a budget announced several times, a missed phase flip, phases reset per
   persistent tile, an early refill, an epilogue that does not wait, and for
   the CTA-pair kernel a leader that frees only its own pair's stages or an
-  empty barrier that counts one arrival where two leaders commit): the model
-  reports the deadlock or the first read of incomplete data;
+  empty barrier that counts one arrival where two leaders commit, and for the
+  response ring of the dynamic tile schedule a wrong reader count or a
+  missing re-arm): the model reports the deadlock or the first read of
+  incomplete data;
 * the timing model of "GEMM II -- pipelining with TMA" (the interactive
   pipeline Gantt: serial vs prefetch, PIPE_DEPTH, K tiles, load : MMA cost),
   as makespan, tensor-core idle fraction, back-to-back MMAs and loads in
@@ -28,7 +30,7 @@ SRC = os.path.join(HERE, "sim", "ringsim.cpp")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "ringsim.h")
 LIB_PATH = os.path.join(HERE, "libringsim.so")
 
-LOCKSTEP, WARP_SPEC, PAIR = 0, 1, 2
+LOCKSTEP, WARP_SPEC, PAIR, CLC = 0, 1, 2, 3
 (OK, DEADLOCK, EARLY_READ, OVERWRITE, EXTRA_ARRIVAL, BAD_ARG) = range(6)
 STATUS_NAMES = {OK: "ok", DEADLOCK: "deadlock", EARLY_READ: "early read", OVERWRITE: "overwrite",
                 EXTRA_ARRIVAL: "extra arrival", BAD_ARG: "bad argument"}
@@ -44,7 +46,10 @@ class RingsimConfig(ctypes.Structure):
                 ("skip_phase_flip", ctypes.c_int), ("reset_phase_per_tile", ctypes.c_int),
                 ("refill_before_mma", ctypes.c_int), ("epilogue_no_wait", ctypes.c_int),
                 ("pairs", ctypes.c_int), ("commit_own_pair_only", ctypes.c_int),
-                ("empty_count_one", ctypes.c_int)]
+                ("empty_count_one", ctypes.c_int), ("clc_slots", ctypes.c_int),
+                ("clc_latency", ctypes.c_double), ("clc_readers_delta", ctypes.c_int),
+                ("clc_no_rearm", ctypes.c_int), ("clc_rearm_after_release", ctypes.c_int),
+                ("clc_request_late", ctypes.c_int)]
 
 
 class RingsimResult(ctypes.Structure):
@@ -52,7 +57,9 @@ class RingsimResult(ctypes.Structure):
                 ("mma_busy", ctypes.c_double), ("idle_fraction", ctypes.c_double),
                 ("mma_back_to_back", ctypes.c_int), ("max_loads_in_flight", ctypes.c_int),
                 ("stages_consumed", ctypes.c_int), ("tiles_stored", ctypes.c_int),
-                ("roles_unique", ctypes.c_int), ("detail", ctypes.c_char * 256)]
+                ("roles_unique", ctypes.c_int), ("detail", ctypes.c_char * 256),
+                ("response_wait", ctypes.c_double), ("request_wait", ctypes.c_double),
+                ("responses_read", ctypes.c_int)]
 
 
 def _cxx():
@@ -96,12 +103,14 @@ DEFAULTS = dict(protocol=WARP_SPEC, depth=4, k_tiles=8, tiles=1, accumulators=2,
                 stage_bytes=(128 * 64 + 128 * 64) * 2, chunks=2, bytes_delta=0,
                 announce_times=1, skip_phase_flip=0, reset_phase_per_tile=0,
                 refill_before_mma=0, epilogue_no_wait=0, pairs=1, commit_own_pair_only=0,
-                empty_count_one=0)
+                empty_count_one=0, clc_slots=4, clc_latency=0.5, clc_readers_delta=0,
+                clc_no_rearm=0, clc_rearm_after_release=0, clc_request_late=0)
 
 
 def run(**kw):
     """Run one configuration (keyword arguments as in ringsim_config; the
-    protocol may be given as "lockstep", "warp_spec" or "pair"); returns a dict."""
+    protocol may be given as "lockstep", "warp_spec", "pair" or "clc"); returns
+    a dict."""
     args = dict(DEFAULTS)
     unknown = set(kw) - set(args)
     if unknown:
@@ -109,7 +118,7 @@ def run(**kw):
     args.update(kw)
     if isinstance(args["protocol"], str):
         args["protocol"] = {"lockstep": LOCKSTEP, "warp_spec": WARP_SPEC,
-                            "pair": PAIR}[args["protocol"]]
+                            "pair": PAIR, "clc": CLC}[args["protocol"]]
     cfg = RingsimConfig(**args)
     res = RingsimResult()
     lib().ringsim_run(ctypes.byref(cfg), ctypes.byref(res))

@@ -94,7 +94,7 @@ struct Accum {
     bool drained = true;
 };
 
-enum EventKind { EV_BYTES, EV_MMA_DONE, EV_COMMIT, EV_EPI_DONE, EV_WAKE };
+enum EventKind { EV_BYTES, EV_MMA_DONE, EV_COMMIT, EV_EPI_DONE, EV_WAKE, EV_CLC_RESPONSE, EV_CLC_REARM };
 
 struct Event {
     double t;
@@ -952,6 +952,366 @@ struct PairSim {
 
 }  // namespace
 
+namespace {
+
+// The response ring of the dynamic tile schedule (RINGSIM_CLC).  Each CTA c
+// has clc_full[c][j] and a response slot j; the rank-0 CTA has clc_empty[j].
+// Roles: a producer per CTA (the rank-0 one also requests), an MMA issuer
+// per pair (in its leader), four epilogue warps per CTA.  Every role walks
+// the same tile sequence: its own tile, then the tile each response names,
+// until a response names none.
+struct ClcSim {
+    ringsim_config c{};
+    ringsim_result* r = nullptr;
+    int NP = 1, C = 2, S = 4, D = 1, A = 2, K = 1;
+    double T = 0.0;  // MMA time of one tile
+    double now = 0.0;
+    long long seq = 0;
+    std::priority_queue<Event, std::vector<Event>, std::greater<Event>> events;
+    struct RespSlot {
+        int use = -1, value = -1, readers_left = 0;
+    };
+    std::vector<RespSlot> slots;        // [cta * S + j]
+    std::vector<Barrier> full;          // [cta * S + j]
+    std::vector<Barrier> empty;         // [j], in the rank-0 CTA
+    // per role: position in the tile sequence and the current tile's index
+    struct Clc {
+        int pc = 0;
+        int i = 0;          // tiles started
+        int tile = 0;       // current tile (-1: done)
+        int use = 0;        // responses read
+        double ready_at = 0.0;
+        double wait_since = -1.0;
+        bool done = false;
+    };
+    std::vector<Clc> roles;
+    std::vector<std::vector<double>> prod_start;  // [cta][i]
+    std::vector<std::vector<double>> mma_start;   // [pair][i]
+    std::vector<int> mma_started, mma_ended;      // [pair]
+    std::vector<int> epi_done;                    // [cta * 4 + w]
+    int requests = 0;
+    bool fault = false;
+
+    static constexpr long long RESP_BYTES = 16;
+
+    void fail(int status, const char* what)
+    {
+        if (fault) return;
+        fault = true;
+        r->status = status;
+        std::snprintf(r->detail, sizeof(r->detail), "t=%.3f: %s", now, what);
+    }
+    void push(Event e)
+    {
+        e.seq = seq++;
+        events.push(e);
+    }
+    void wake(Clc& s, double t)
+    {
+        s.ready_at = t;
+        Event e{};
+        e.t = t;
+        e.kind = EV_WAKE;
+        push(e);
+    }
+    int readers_in(int cta) const { return 5 + ((cta & 1) == 0 ? 1 : 0); }
+    int cta_of_role(int i) const
+    {
+        if (i < C) return i;
+        if (i < C + NP) return 2 * (i - C);
+        return (i - C - NP) / 4;
+    }
+
+    void apply(const Event& e)
+    {
+        if (e.kind == EV_CLC_RESPONSE) {
+            // the multicast response lands in every CTA's slot
+            for (int d = 0; d < C; ++d) {
+                RespSlot& sl = slots[d * S + e.slot];
+                if (sl.use >= 0 && sl.readers_left > 0) {
+                    char m[200];
+                    std::snprintf(m, sizeof(m),
+                                  "response %d lands in CTA %d slot %d while %d reader(s) of response %d "
+                                  "have not read it",
+                                  e.k, d, e.slot, sl.readers_left, sl.use);
+                    fail(RINGSIM_OVERWRITE, m);
+                    return;
+                }
+                sl.use = e.k;
+                sl.value = e.tile;
+                sl.readers_left = readers_in(d);
+                full[d * S + e.slot].complete_tx(RESP_BYTES);
+            }
+        } else if (e.kind == EV_CLC_REARM) {
+            e.bar->arrive_expect_tx(ROLE_PRODUCER, RESP_BYTES);
+        }
+    }
+
+    // Request the tile after the current one (rank-0 producer).  False while
+    // the slot is still held by readers of its previous response.
+    bool request(Clc& s)
+    {
+        const int j = requests % S;
+        const unsigned free_parity = (static_cast<unsigned>(requests / S) & 1u) ^ 1u;
+        if (!empty[j].passed(ROLE_PRODUCER, free_parity)) {
+            if (s.wait_since < 0) s.wait_since = now;
+            return false;
+        }
+        if (s.wait_since >= 0) {
+            r->request_wait += now - s.wait_since;
+            s.wait_since = -1.0;
+        }
+        Event e{};
+        e.t = now + c.clc_latency;
+        e.kind = EV_CLC_RESPONSE;
+        e.slot = j;
+        e.k = requests;                                     // response index
+        e.tile = requests + 1 < c.tiles ? requests + 1 : -1;  // the cancelled cluster's tile
+        push(e);
+        ++requests;
+        return true;
+    }
+
+    // Read this role's next response in CTA `cta`; `arm`: the CTA's producer.
+    // False while the response has not landed.
+    bool read(Clc& s, int cta, bool arm, bool timed)
+    {
+        const int j = s.use % S;
+        Barrier& b = full[cta * S + j];
+        if (!b.passed(arm ? ROLE_PRODUCER : ROLE_EPILOGUE, static_cast<unsigned>(s.use / S) & 1u)) {
+            if (timed && s.wait_since < 0) s.wait_since = now;
+            return false;
+        }
+        if (timed && s.wait_since >= 0) {
+            r->response_wait += now - s.wait_since;
+            s.wait_since = -1.0;
+        }
+        RespSlot& sl = slots[cta * S + j];
+        if (sl.use != s.use) {
+            char m[200];
+            std::snprintf(m, sizeof(m), "a reader in CTA %d takes slot %d for response %d but it holds response %d",
+                          cta, j, s.use, sl.use);
+            fail(RINGSIM_EARLY_READ, m);
+            return true;
+        }
+        const int value = sl.value;
+        --sl.readers_left;
+        ++r->responses_read;
+        if (arm && !c.clc_no_rearm && !c.clc_rearm_after_release)
+            b.arrive_expect_tx(ROLE_PRODUCER, RESP_BYTES);
+        empty[j].arrive(ROLE_EPILOGUE);
+        if (arm && !c.clc_no_rearm && c.clc_rearm_after_release) {
+            Event e{};
+            e.t = now + c.issue_latency;
+            e.kind = EV_CLC_REARM;
+            e.bar = &b;
+            push(e);
+        }
+        ++s.use;
+        s.tile = value;
+        ++s.i;
+        return true;
+    }
+
+    bool step_producer(Clc& s, int cta)
+    {
+        const bool requester = cta == 0;
+        const int p = cta >> 1;
+        switch (s.pc) {
+        case 0:  // loop head: a tile to load, or done
+            if (s.tile < 0) {
+                s.done = true;
+                return true;
+            }
+            prod_start[cta].push_back(now);
+            s.pc = requester && !c.clc_request_late ? 1 : 2;
+            return true;
+        case 1:  // request at the start of the tile
+            if (!request(s)) return false;
+            s.pc = 2;
+            return true;
+        case 2: {  // issue the tile's loads: the last D wait for the MMAs to free stages
+            if (mma_started[p] <= s.i) return false;
+            const int ahead = K > D ? K - D : 0;
+            wake(s, std::max(now, mma_start[p][s.i] + ahead * c.mma_time));
+            s.pc = 3;
+            return true;
+        }
+        case 3:
+            if (now < s.ready_at) return false;
+            s.pc = requester && c.clc_request_late ? 4 : 5;
+            return true;
+        case 4:  // late request: at the end of the tile
+            if (!request(s)) return false;
+            s.pc = 5;
+            return true;
+        case 5:
+            if (!read(s, cta, true, requester)) return false;
+            s.pc = 0;
+            return true;
+        }
+        return false;
+    }
+
+    bool step_mma(Clc& s, int p)
+    {
+        switch (s.pc) {
+        case 0: {
+            if (s.tile < 0) {
+                s.done = true;
+                return true;
+            }
+            // the loads of this tile started in every CTA that feeds the pair
+            const int lo = NP == 2 ? 0 : 2 * p, hi = NP == 2 ? C : 2 * p + 2;
+            double first = 0.0;
+            for (int d = lo; d < hi; ++d) {
+                if (static_cast<int>(prod_start[d].size()) <= s.i) return false;
+                first = std::max(first, prod_start[d][s.i]);
+            }
+            // an accumulator is free: tile i - A drained by all the pair's epilogue warps
+            for (int d = 2 * p; d < 2 * p + 2; ++d)
+                for (int w = 0; w < 4; ++w)
+                    if (epi_done[d * 4 + w] < s.i - A + 1) return false;
+            wake(s, std::max(now, first + c.load_time));
+            s.pc = 1;
+            return true;
+        }
+        case 1:
+            if (now < s.ready_at) return false;
+            mma_start[p].push_back(now);
+            mma_started[p] = s.i + 1;
+            r->mma_busy += T;
+            r->stages_consumed += K;
+            wake(s, now + T);
+            s.pc = 2;
+            return true;
+        case 2:
+            if (now < s.ready_at) return false;
+            mma_ended[p] = s.i + 1;
+            s.pc = 3;
+            return true;
+        case 3:
+            if (!read(s, 2 * p, false, false)) return false;
+            s.pc = 0;
+            return true;
+        }
+        return false;
+    }
+
+    bool step_epilogue(Clc& s, int cta, int w)
+    {
+        const int p = cta >> 1;
+        switch (s.pc) {
+        case 0:
+            if (s.tile < 0) {
+                s.done = true;
+                return true;
+            }
+            if (mma_ended[p] <= s.i) return false;
+            wake(s, now + c.epilogue_time);
+            s.pc = 1;
+            return true;
+        case 1:
+            if (now < s.ready_at) return false;
+            epi_done[cta * 4 + w] = s.i + 1;
+            s.pc = 2;
+            return true;
+        case 2:
+            if (!read(s, cta, false, false)) return false;
+            s.pc = 0;
+            return true;
+        }
+        return false;
+    }
+
+    int run()
+    {
+        NP = c.pairs > 0 ? c.pairs : 1;
+        C = 2 * NP;
+        S = c.clc_slots > 0 ? c.clc_slots : 4;
+        D = c.depth;
+        A = c.accumulators;
+        K = c.k_tiles;
+        T = K * c.mma_time;
+        slots.resize(C * S);
+        full.resize(C * S);
+        empty.resize(S);
+        for (Barrier& b : full) b.arrive_expect_tx(ROLE_PRODUCER, RESP_BYTES);  // armed for first use
+        for (Barrier& b : empty) b.expected = b.pending = 11 * NP + c.clc_readers_delta;
+        roles.resize(C + NP + 4 * C);
+        prod_start.resize(C);
+        mma_start.resize(NP);
+        mma_started.assign(NP, 0);
+        mma_ended.assign(NP, 0);
+        epi_done.assign(4 * C, 0);
+        r->roles_unique = 1;
+        auto step = [&](int i) {
+            Clc& s = roles[i];
+            if (s.done || fault) return false;
+            if (i < C) return step_producer(s, i);
+            if (i < C + NP) return step_mma(s, i - C);
+            const int e = i - C - NP;
+            return step_epilogue(s, e / 4, e % 4);
+        };
+        long long budget_steps = 200LL * (c.tiles + 16) * static_cast<long long>(roles.size()) + 1000000;
+        const int nroles = static_cast<int>(roles.size());
+        while (!fault) {
+            bool progressed = true;
+            while (progressed && !fault && budget_steps >= 0) {
+                progressed = false;
+                for (int i = 0; i < nroles; ++i)
+                    while (step(i)) {
+                        progressed = true;
+                        if (--budget_steps < 0) break;
+                    }
+            }
+            if (fault) break;
+            if (budget_steps < 0) {
+                fail(RINGSIM_DEADLOCK, "step limit reached");
+                break;
+            }
+            bool all_done = true;
+            for (const Clc& s : roles) all_done = all_done && s.done;
+            if (events.empty()) {
+                if (!all_done) {
+                    std::string stuck = "deadlock:";
+                    for (int i = 0; i < nroles; ++i) {
+                        const Clc& s = roles[i];
+                        if (s.done) continue;
+                        const char* who = i < C ? "producer" : (i < C + NP ? "MMA issuer" : "epilogue warp");
+                        const int cta = cta_of_role(i);
+                        const int j = s.use % S;
+                        const Barrier& b = full[cta * S + j];
+                        char m[200];
+                        std::snprintf(m, sizeof(m),
+                                      " %s of CTA %d (tile %d, step %d, response %d; clc_full[%d] %u done, "
+                                      "%d arrivals, %lld bytes pending; clc_empty[%d] %u done, %d arrivals);",
+                                      who, cta, s.i, s.pc, s.use, j, b.completed, b.pending, b.tx,
+                                      requests % S, empty[requests % S].completed,
+                                      empty[requests % S].pending);
+                        stuck += m;
+                    }
+                    fail(RINGSIM_DEADLOCK, stuck.c_str());
+                }
+                break;
+            }
+            const Event e = events.top();
+            events.pop();
+            now = std::max(now, e.t);
+            apply(e);
+        }
+        r->makespan = now;
+        r->idle_fraction = now > 0 ? 1.0 - r->mma_busy / (now * NP) : 0.0;
+        r->mma_back_to_back = 0;
+        int stored = c.tiles;
+        for (int v : epi_done) stored = std::min(stored, v);
+        r->tiles_stored = stored;
+        return r->status;
+    }
+};
+
+}  // namespace
+
 extern "C" {
 
 RINGSIM_API int ringsim_run(const ringsim_config* cfg, ringsim_result* out)
@@ -965,15 +1325,21 @@ RINGSIM_API int ringsim_run(const ringsim_config* cfg, ringsim_result* out)
     };
     if (!cfg) return bad("config is NULL");
     const ringsim_config& c = *cfg;
-    if (c.protocol != RINGSIM_LOCKSTEP && c.protocol != RINGSIM_WARP_SPEC && c.protocol != RINGSIM_PAIR)
-        return bad("protocol must be RINGSIM_LOCKSTEP, RINGSIM_WARP_SPEC or RINGSIM_PAIR");
+    if (c.protocol < RINGSIM_LOCKSTEP || c.protocol > RINGSIM_CLC)
+        return bad("protocol must be RINGSIM_LOCKSTEP, RINGSIM_WARP_SPEC, RINGSIM_PAIR or RINGSIM_CLC");
     if (c.depth < 1 || c.depth > 64) return bad("depth must be 1..64");
     if (c.k_tiles < 1 || c.k_tiles > 65535) return bad("k_tiles must be 1..65535");
     if (c.tiles < 1 || c.tiles > 100000) return bad("tiles must be 1..100000");
     if (c.protocol != RINGSIM_LOCKSTEP && (c.accumulators < 1 || c.accumulators > 2))
         return bad("accumulators must be 1 or 2");
-    if (c.protocol == RINGSIM_PAIR && (c.pairs < 0 || c.pairs > 2))
+    if ((c.protocol == RINGSIM_PAIR || c.protocol == RINGSIM_CLC) && (c.pairs < 0 || c.pairs > 2))
         return bad("pairs must be 1 or 2");
+    if (c.protocol == RINGSIM_CLC) {
+        if (c.clc_slots < 0 || c.clc_slots > 16) return bad("clc_slots must be 0 (4) or 1..16");
+        if (c.clc_latency < 0) return bad("clc_latency must be non-negative");
+        if (11 * (c.pairs > 0 ? c.pairs : 1) + c.clc_readers_delta < 1)
+            return bad("clc_empty must expect at least one arrival");
+    }
     if (c.protocol == RINGSIM_PAIR && c.stage_bytes % 4 != 0)
         return bad("stage_bytes must be a multiple of 4 for CTA pairs");
     if (c.stage_bytes < 2 || c.load_time < 0 || c.mma_time < 0 || c.epilogue_time < 0 ||
@@ -982,6 +1348,12 @@ RINGSIM_API int ringsim_run(const ringsim_config* cfg, ringsim_result* out)
     if ((c.protocol == RINGSIM_PAIR ? 2 : 1) * c.stage_bytes + c.bytes_delta <= 0)
         return bad("the announced byte budget must be positive");
 
+    if (c.protocol == RINGSIM_CLC) {
+        ClcSim cs;
+        cs.c = c;
+        cs.r = out;
+        return cs.run();
+    }
     if (c.protocol == RINGSIM_PAIR) {
         PairSim ps;
         ps.c = c;
