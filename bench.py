@@ -14,6 +14,10 @@ launch stream around the K back-to-back launches; max over ranks.  The
 operands (A + B = 256 MiB at 8192^3) and the output (128 MiB) are larger than
 the 126 MiB L2, so no flush is inserted.
 
+The environment variables GEMM_VARIANT and GEMM_PIPE_DEPTH, when set, give
+the defaults of --variant and --depth (the library itself reads no
+environment).
+
 ``--impl reference`` times the CPU oracle (the only other implementation of
 this computation) on a bounded sample of the same workload on the host cores.
 """
@@ -273,8 +277,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="gemm_8192x8192x8192_f16out")
-    ap.add_argument("--variant", default="auto")
-    ap.add_argument("--depth", type=int, default=0)
+    ap.add_argument("--variant", default=os.environ.get("GEMM_VARIANT", "auto"))
+    ap.add_argument("--depth", type=int, default=int(os.environ.get("GEMM_PIPE_DEPTH", "0")))
     ap.add_argument("--block-n", type=int, default=0)
     ap.add_argument("--block-k", type=int, default=0, choices=[0, 64, 128])
     ap.add_argument("--graph", action="store_true",
