@@ -366,3 +366,15 @@ def test_clc_bad_arguments(rs):
     for kw in (dict(clc_slots=17), dict(clc_slots=-1), dict(clc_latency=-1.0),
                dict(clc_readers_delta=-11), dict(pairs=3)):
         assert rs.run(protocol="clc", **kw)["status_name"] == "bad argument", kw
+
+
+def test_command_line_tables(rs):
+    import sys
+    env = dict(os.environ, PYTHONPATH=ROOT)
+    out = subprocess.run([sys.executable, "-m", "tma_pipelined_tensor_fp16_gb300.ringsim"],
+                         capture_output=True, text=True, check=True, cwd=ROOT, env=env).stdout
+    assert "makespan 17.60" in out and "makespan 9.80" in out
+    out = subprocess.run([sys.executable, "-m", "tma_pipelined_tensor_fp16_gb300.ringsim", "--clc"],
+                         capture_output=True, text=True, check=True, cwd=ROOT, env=env).stdout
+    assert out.count(" ok ") == 9
+    assert "4 slot(s): first fails at 41 tiles (deadlock)" in out

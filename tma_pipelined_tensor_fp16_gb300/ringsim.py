@@ -18,6 +18,7 @@ uses:
   flight.
 
     python -m tma_pipelined_tensor_fp16_gb300.ringsim [--depth 2] [--k-tiles 8] [--load-mma 1.2]
+    python -m tma_pipelined_tensor_fp16_gb300.ringsim --clc [--pairs 2]
 """
 import argparse
 import ctypes
@@ -151,12 +152,62 @@ def gantt(mode="prefetch", depth=2, k_tiles=8, load_mma=1.2):
             "loads_in_flight_max": r["max_loads_in_flight"] // 2}
 
 
+def clc_table(slots=(1, 2, 4), latencies=(0.5, 4.0, 12.0), pairs=1, tiles=17, k_tiles=8,
+              epilogue_time=6.0):
+    """The dynamic schedule's response ring: for each slot count and response
+    latency (in MMA times per K block; a tile is k_tiles of them), the
+    makespan of `tiles` tiles and the time the requester waited for a free
+    slot and for responses, with requests at the start of each tile."""
+    rows = []
+    for n in slots:
+        for lat in latencies:
+            r = run(protocol=CLC, pairs=pairs, clc_slots=n, clc_latency=lat, tiles=tiles,
+                    k_tiles=k_tiles, depth=4, load_time=1.2, mma_time=1.0,
+                    epilogue_time=epilogue_time)
+            rows.append({"slots": n, "latency": lat, "status": r["status_name"],
+                         "makespan": r["makespan"], "request_wait": r["request_wait"],
+                         "response_wait": r["response_wait"]})
+    return rows
+
+
+def clc_miscount_onset(slots=(1, 2, 4, 8), pairs=1, limit=400):
+    """Tiles per cluster after which a response ring whose empty barriers
+    count one reader too few first fails (overwrite or deadlock)."""
+    out = []
+    for n in slots:
+        onset = None
+        for tiles in range(1, limit + 1):
+            r = run(protocol=CLC, pairs=pairs, clc_slots=n, tiles=tiles, k_tiles=8, depth=4,
+                    load_time=1.2, mma_time=1.0, epilogue_time=6.0, clc_readers_delta=-1)
+            if r["status_name"] != "ok":
+                onset = (tiles, r["status_name"])
+                break
+        out.append({"slots": n, "onset": onset})
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--depth", type=int, default=2)
     ap.add_argument("--k-tiles", type=int, default=8)
     ap.add_argument("--load-mma", type=float, default=1.2)
+    ap.add_argument("--clc", action="store_true",
+                    help="the dynamic schedule's response ring instead of the pipeline Gantt")
+    ap.add_argument("--pairs", type=int, default=1, choices=[1, 2])
     a = ap.parse_args()
+    if a.clc:
+        print("response ring, %d pair(s), 17 tiles of %d K blocks (times in MMA times per K block)"
+              % (a.pairs, a.k_tiles))
+        for row in clc_table(pairs=a.pairs, k_tiles=a.k_tiles):
+            print("slots %d  latency %5.1f  %-8s makespan %7.1f  request wait %6.1f  "
+                  "response wait %6.1f" % (row["slots"], row["latency"], row["status"],
+                                            row["makespan"], row["request_wait"],
+                                            row["response_wait"]))
+        for row in clc_miscount_onset(pairs=a.pairs):
+            print("one reader too few, %d slot(s): %s" % (
+                row["slots"], "first fails at %d tiles (%s)" % row["onset"] if row["onset"]
+                else "no failure within 400 tiles"))
+        return
     for mode in ("serial", "prefetch"):
         g = gantt(mode, a.depth, a.k_tiles, a.load_mma)
         print("%-8s PIPE_DEPTH=%d K tiles=%d load:MMA=%.2f  makespan %.2f  tensor idle %.1f%%  "
