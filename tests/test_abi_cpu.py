@@ -453,3 +453,13 @@ def test_half_height_a_slots_for_at_most_64_rows(b):
     assert c.a_rows == 128
     st, c = b.gemm_select_config(64, 1024, 1024, 1, b.make_options(variant="pipelined"))
     assert c.a_rows == 128  # lock-step kernels keep full-height slots
+
+
+def test_missing_library_fails_loudly(b, monkeypatch, tmp_path):
+    # no fallback path: without the built library every entry point raises
+    monkeypatch.setattr(b, "_lib", None)
+    monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "libtmagemm.so"))
+    with pytest.raises(RuntimeError, match="is missing: build it first"):
+        b.Plan(256, 256, 256, out="f32")
+    with pytest.raises(RuntimeError, match="is missing"):
+        b.gemm_select_config(256, 256, 256, 0)
