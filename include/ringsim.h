@@ -100,7 +100,8 @@ typedef struct {
     int protocol;          /* RINGSIM_LOCKSTEP, RINGSIM_WARP_SPEC, RINGSIM_PAIR or RINGSIM_CLC */
     int depth;             /* PIPE_DEPTH, 1..64 */
     int k_tiles;           /* K blocks per output tile, >= 1 */
-    int tiles;             /* output tiles processed in sequence by one CTA, >= 1 */
+    int tiles;             /* output tiles processed in sequence by one CTA (pair: by each
+                              pair; CLC: by the cluster, its own and one per response), >= 1 */
     int accumulators;      /* warp-specialised, pair, CLC: TMEM accumulator buffers, 1 or 2 */
     double load_time;      /* time from a copy's issue to its bytes landing */
     double mma_time;       /* tensor-pipe time of one stage's MMAs */
@@ -109,7 +110,8 @@ typedef struct {
     long long stage_bytes; /* bytes of one stage of one CTA (two copies of half each: A and B) */
     int chunks;            /* each copy's bytes land in this many equal parts (>= 1) */
     /* fault injection (0 = off) */
-    long long bytes_delta;     /* the announced byte budget is stage_bytes + bytes_delta */
+    long long bytes_delta;     /* the announced byte budget is stage_bytes + bytes_delta
+                                  (pair: the leader's 2 * stage_bytes + bytes_delta) */
     int announce_times;        /* the budget is announced this many times (1 = correct; 0 = 1) */
     int skip_phase_flip;       /* the issuing side never flips its ring phase */
     int reset_phase_per_tile;  /* ring position and phases restart at 0 at every tile */
@@ -130,11 +132,13 @@ typedef struct {
     int status;                /* RINGSIM_* */
     double makespan;           /* end of the last activity */
     double mma_busy;           /* total tensor-pipe busy time */
-    double idle_fraction;      /* 1 - mma_busy / makespan */
-    int mma_back_to_back;      /* 1 if every MMA after the first started as the previous ended */
+    double idle_fraction;      /* 1 - mma_busy / (makespan * pairs); pairs = 1 unless pair/CLC */
+    int mma_back_to_back;      /* 1 if every MMA after the first started as the previous ended
+                                  (per pair; CLC: not tracked, 0) */
     int max_loads_in_flight;   /* most copies issued and not yet landed at once */
     int stages_consumed;       /* stages whose MMAs were issued */
-    int tiles_stored;          /* accumulators drained by the epilogue */
+    int tiles_stored;          /* accumulators drained by the epilogue (pair: summed over
+                                  pairs; CLC: tiles drained by every epilogue warp) */
     int roles_unique;          /* 1 if every barrier had one arriving and one waiting role
                                   (RINGSIM_CLC: always 1; its responses have many readers) */
     char detail[256];          /* the hazard or deadlock, in words */
