@@ -463,3 +463,48 @@ def test_missing_library_fails_loudly(b, monkeypatch, tmp_path):
         b.Plan(256, 256, 256, out="f32")
     with pytest.raises(RuntimeError, match="is missing"):
         b.gemm_select_config(256, 256, 256, 0)
+
+
+def _random_shapes(n, seed):
+    rng = np.random.default_rng(seed)
+    edges = [1, 2, 63, 64, 65, 127, 128, 129, 255, 256, 257, 511, 513]
+    for _ in range(n):
+        M = int(rng.choice(edges)) if rng.random() < 0.3 else int(rng.integers(1, 20000))
+        dt = int(rng.integers(0, 2))
+        step = 8 if dt == 1 else 4  # N * sizeof(C element) a multiple of 16 bytes
+        N = max(step, int(rng.integers(1, 20000)) // step * step)
+        K = max(8, int(rng.integers(1, 20000)) // 8 * 8)
+        yield M, N, K, dt
+
+
+def test_plan_invariants_over_random_shapes(b):
+    # Every valid shape gets a plan from every variant, and each plan is
+    # self-consistent: tile counts cover M and N, shared memory and TMEM fit,
+    # two accumulators for the persistent kernels, and the byte budget is
+    # the bytes the stage's copies deliver (both CTAs' with a pair).
+    import math
+    for M, N, K, dt in _random_shapes(1500, 2024):
+        for v in range(0, 10):
+            st, c = b.gemm_select_config(M, N, K, dt, b.make_options(variant=v))
+            where = (M, N, K, dt, v)
+            assert st == 0, (where, b.last_error())
+            var, bm, bn = c.variant, c.block_m, c.block_n
+            pair = var in (7, 8, 9)
+            assert var == v or v == 0, where
+            assert bm == (256 if pair else 128), where
+            assert c.tiles_m == math.ceil(M / bm) and c.tiles_n == math.ceil(N / bn), where
+            assert c.num_tiles == c.tiles_m * c.tiles_n, where
+            assert c.k_blocks == math.ceil(K / 64), where
+            assert 1 <= c.pipe_depth <= 8 and 0 < c.smem_bytes <= 232448, where
+            t = c.tmem_cols
+            assert t == 0 or (32 <= t <= 512 and t & (t - 1) == 0), where
+            if var in (5, 7, 8, 9):
+                assert t >= 2 * bn, where
+            if var in (4, 5, 7, 8, 9):
+                per_cta = (c.a_rows * 64 + (bn // 2 if pair else bn) * 64) * 2 * (c.block_k // 64)
+                assert c.tx_bytes == (2 * per_cta if pair else per_cta), where
+            assert c.a_rows == 128 or (c.a_rows == 64 and M <= 64 and not pair), where
+            if var == 9:
+                assert c.grid == 4 * c.tiles_m * math.ceil(c.tiles_n / 2), where
+            if var in (5, 7):
+                assert c.grid <= 152, where
