@@ -394,6 +394,25 @@ def test_swizzle_map_matches_page_rule_and_bank_analysis(b):
 def test_work_units_cover_every_k_block_once(b, M, N, K, opts):
     st, c = b.gemm_select_config(M, N, K, 1, b.make_options(**opts))
     assert st == 0, b.last_error()
+    _assert_units_cover(b, c)
+
+
+def test_work_units_cover_every_k_block_once_random_shapes(b):
+    rng = np.random.default_rng(2025)
+    for _ in range(150):
+        M, N = int(rng.integers(1, 3000)), int(rng.integers(1, 3000)) // 8 * 8 + 8
+        K = int(rng.integers(1, 3000)) // 8 * 8 + 8
+        for opts in ({"variant": "persistent", "stream_k": "on"},
+                     {"variant": "persistent_2cta", "stream_k": "on"},
+                     {"variant": "dynamic_2cta", "stream_k": "on"},
+                     {"variant": "dynamic_2cta"},
+                     {"variant": "persistent", "grid": int(rng.integers(1, 152))}):
+            st, c = b.gemm_select_config(M, N, K, 1, b.make_options(**opts))
+            assert st == 0, (M, N, K, opts, b.last_error())
+            _assert_units_cover(b, c)
+
+
+def _assert_units_cover(b, c):
     pair = c.variant in (b.GEMM_VAR_PERSISTENT_2CTA, b.GEMM_VAR_DYNAMIC_2CTA)
     workers = c.grid // 2 if pair else c.grid
     cover = np.zeros((c.num_tiles, c.k_blocks), dtype=np.int64)
