@@ -410,6 +410,14 @@ def test_work_units_cover_every_k_block_once_random_shapes(b):
             st, c = b.gemm_select_config(M, N, K, 1, b.make_options(**opts))
             assert st == 0, (M, N, K, opts, b.last_error())
             _assert_units_cover(b, c)
+        # two pairs per cluster: one cluster per unit of two side-by-side
+        # tiles, each taking its own unit whole
+        st, c = b.gemm_select_config(M, N, K, 1, b.make_options(variant="dynamic_2x2"))
+        assert st == 0, (M, N, K, b.last_error())
+        units = c.tiles_m * ((c.tiles_n + 1) // 2)
+        assert c.grid == 4 * units
+        for w in range(units):
+            assert b.gemm_worker_units(c, w) == [(w, 0, c.k_blocks, 0, 1)], (M, N, K, w)
 
 
 def _assert_units_cover(b, c):
