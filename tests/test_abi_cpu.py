@@ -344,6 +344,23 @@ def test_raster_covers_every_tile_once_in_group_order(b, M, N, group):
     assert st == b.GEMM_ERR_INVALID_ARG
 
 
+def test_raster_is_the_grouped_order_of_the_persistent_step(b):
+    # "GEMM II" Step 6 (l2_group_size): tiles run down a group of G tile rows
+    # before moving one tile column right; the last group may be shorter
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        M, N = int(rng.integers(1, 6000)), int(rng.integers(1, 6000)) // 8 * 8 + 8
+        G = int(rng.integers(1, 17))
+        st, c = b.gemm_select_config(M, N, 64, 1, b.make_options(group_m=G, block_n=256,
+                                                                  variant="persistent"))
+        assert st == 0
+        for t in range(c.num_tiles):
+            first_row = G * (t // (G * c.tiles_n))
+            rows = min(c.tiles_m - first_row, G)
+            r = t % (G * c.tiles_n)
+            assert b.gemm_schedule_tile(c, t) == (0, first_row + r % rows, r // rows), (M, N, G, t)
+
+
 def test_persistent_ctas_partition_the_tiles(b):
     st, c = b.gemm_select_config(4000, 3000, 5000, 0)
     assert st == 0
