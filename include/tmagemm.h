@@ -295,12 +295,16 @@ TMAGEMM_API int gemm_select_config(int64_t M, int64_t N, int64_t K, int dtype_ou
  * l2_group_size).  Returns GEMM_ERR_INVALID_ARG if tile is out of range. */
 TMAGEMM_API int gemm_schedule_tile(const gemm_config* cfg, int64_t tile, int* m_tile, int* n_tile);
 
-/* Work unit `index` (0, 1, ...) of persistent worker `worker` (a CTA, or a
- * CTA pair for the pair variant) under `cfg`, in the order the kernels process
- * them: whole tiles first, then the worker's share of the stream-K part.
- * Writes the tile (raster index), its K-block range [kb0, kb1) and the
- * worker's rank among the tile's contributors; returns 1, or 0 when the
- * worker has no unit `index`, or GEMM_ERR_INVALID_ARG. */
+/* Work unit `index` (0, 1, ...) of persistent worker `worker` (a CTA, a CTA
+ * pair for the pair variants, or a cluster of two pairs for dynamic_2x2)
+ * under `cfg`, in the order the kernels process them: whole tiles first,
+ * then the worker's share of the stream-K part.  Under the dynamic schedule
+ * only the worker's own unit (index 0) is fixed before the run -- the rest
+ * are taken by cancellation while the kernel runs -- and for dynamic_2x2 the
+ * unit is a pair of side-by-side tiles, reported by its unit index.  Writes
+ * the tile (raster index), its K-block range [kb0, kb1) and the worker's rank
+ * among the tile's contributors; returns 1, or 0 when the worker has no unit
+ * `index`, or GEMM_ERR_INVALID_ARG. */
 TMAGEMM_API int gemm_schedule_unit(const gemm_config* cfg, int worker, int index, int* tile,
                                    int* kb0, int* kb1, int* contrib, int* ncontrib);
 
