@@ -38,8 +38,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = ["csrc/ptx.cuh", "csrc/gemm_common.h", "csrc/device_common.cuh",
                   "csrc/kernel_ws.cu", "csrc/kernel_ws2.cuh", "csrc/kernel_ws2.cu",
                   "csrc/kernel_ws2_dyn.cu", "csrc/kernels_ladder.cu", "csrc/api.cu",
-                  "csrc/launch.h", "csrc/kernel_ws2_k2.cu", "csrc/kernel_ws2_dyn_k2.cu",
-                  "csrc/kernel_ws2_x2.cu", "csrc/kernel_ws2_x2_k2.cu"]
+                  "csrc/launch.h", "csrc/kernel_ws2_k2.cu", "csrc/kernel_ws2_dyn_k2.cu"]
 
 
 def kernel_source_hash():

@@ -40,26 +40,22 @@
  *                      tmem_full[a]) and an epilogue (wait tmem_full[a], read,
  *                      arrive tmem_empty[a]) with `accumulators` TMEM buffers;
  *                      ring position and phases run on across tiles.
- *   RINGSIM_PAIR       the CTA-pair kernel with `pairs` pairs per cluster: a
- *                      producer in every CTA, the MMA issuer and its barriers
- *                      in each pair's leader.  Both CTAs' copies of a stage
- *                      signal the leader's full[s] (armed once with the pair's
- *                      bytes); the leader's commit frees empty[s] in every CTA
- *                      whose stage it read from or whose producer writes into
- *                      it.  With two pairs, the CTAs of equal rank share A: each
- *                      loads one half into both, so empty[s] counts an arrival
- *                      from each leader.
+ *   RINGSIM_PAIR       the CTA-pair kernel (a cluster of two CTAs): a
+ *                      producer in each CTA, the MMA issuer and its barriers
+ *                      in the leader.  Both CTAs' copies of a stage signal the
+ *                      leader's full[s] (armed once with the pair's bytes);
+ *                      the leader's commit frees empty[s] in both CTAs.
  *   RINGSIM_CLC        the response ring of the dynamic tile schedule
  *                      (cluster launch control, which "GEMM II" Step 6 names
  *                      as the successor of its precomputed tile assignment).
- *                      One cluster of `pairs` CTA pairs takes `tiles` tiles:
+ *                      One cluster (a CTA pair) takes `tiles` tiles:
  *                      its own, then one per cancellation response.  The
  *                      rank-0 producer requests at the start of each tile
  *                      (wait clc_empty[j], try_cancel multicast into every
  *                      CTA's slot j, landing `clc_latency` later and
  *                      completing 16 bytes on that CTA's clc_full[j]).  Every
  *                      reader -- each CTA's producer and four epilogue warps,
- *                      each leader's MMA issuer: 11 per pair -- reads the
+ *                      the leader's MMA issuer: 11 in all -- reads the
  *                      next response after its tile (wait clc_full[j],
  *                      decode; the producer re-arms its CTA's clc_full[j]
  *                      with 16 bytes for the slot's next use) and arrives on
@@ -117,12 +113,9 @@ typedef struct {
     int reset_phase_per_tile;  /* ring position and phases restart at 0 at every tile */
     int refill_before_mma;     /* lock-step: refill a slot before waiting for its MMA */
     int epilogue_no_wait;      /* warp-specialised: the epilogue skips its accumulator wait */
-    int pairs;                 /* RINGSIM_PAIR, RINGSIM_CLC: CTA pairs per cluster, 1 or 2 (0 = 1) */
-    int commit_own_pair_only;  /* RINGSIM_PAIR fault: a leader frees only its own pair's stages */
-    int empty_count_one;       /* RINGSIM_PAIR fault: empty[s] expects one arrival with two pairs */
     int clc_slots;             /* RINGSIM_CLC: response slots, 1..16 (0 = 4) */
     double clc_latency;        /* RINGSIM_CLC: time from a request to its response landing */
-    int clc_readers_delta;     /* RINGSIM_CLC fault: clc_empty expects 11 * pairs + this arrivals */
+    int clc_readers_delta;     /* RINGSIM_CLC fault: clc_empty expects 11 + this arrivals */
     int clc_no_rearm;          /* RINGSIM_CLC fault: the producer never re-arms clc_full */
     int clc_rearm_after_release; /* RINGSIM_CLC: the producer re-arms after its release, issue_latency later */
     int clc_request_late;      /* RINGSIM_CLC: the next request is issued at the end of a tile */
@@ -132,13 +125,13 @@ typedef struct {
     int status;                /* RINGSIM_* */
     double makespan;           /* end of the last activity */
     double mma_busy;           /* total tensor-pipe busy time */
-    double idle_fraction;      /* 1 - mma_busy / (makespan * pairs); pairs = 1 unless pair/CLC */
+    double idle_fraction;      /* 1 - mma_busy / makespan */
     int mma_back_to_back;      /* 1 if every MMA after the first started as the previous ended
                                   (per pair; CLC: not tracked, 0) */
     int max_loads_in_flight;   /* most copies issued and not yet landed at once */
     int stages_consumed;       /* stages whose MMAs were issued */
-    int tiles_stored;          /* accumulators drained by the epilogue (pair: summed over
-                                  pairs; CLC: tiles drained by every epilogue warp) */
+    int tiles_stored;          /* accumulators drained by the epilogue (CLC: tiles drained
+                                  by every epilogue warp) */
     int roles_unique;          /* 1 if every barrier had one arriving and one waiting role
                                   (RINGSIM_CLC: always 1; its responses have many readers) */
     char detail[256];          /* the hazard or deadlock, in words */

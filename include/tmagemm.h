@@ -58,11 +58,7 @@ typedef enum {
                                        GEMM_VAR_DYNAMIC_2CTA, or
                                        GEMM_VAR_PERSISTENT_2CTA when the options
                                        set grid or stream_k = 2 -- else
-                                       GEMM_VAR_PERSISTENT.  When K % 64 != 0
-                                       (rows off 128-byte lines) and no width,
-                                       depth, stage or stream-K option is set,
-                                       GEMM_VAR_DYNAMIC_2X2 if a makespan model
-                                       predicts it at least 5 % faster */
+                                       GEMM_VAR_PERSISTENT */
     GEMM_VAR_SYNC_TILED = 1,        /* Step 3: thread copies, one MMA at a time */
     GEMM_VAR_TMA_SERIAL = 2,        /* Step 4: TMA load + expect_tx, serial loop */
     GEMM_VAR_PIPELINED = 3,         /* Step 5: PIPE_DEPTH ring, lock-step prefetch */
@@ -91,21 +87,6 @@ typedef enum {
                                        (see stream_k); gemm_schedule_unit
                                        reports only each cluster's own unit,
                                        the rest being assigned at run time */
-    GEMM_VAR_DYNAMIC_2X2 = 9        /* GEMM_VAR_DYNAMIC_2CTA with two CTA pairs
-                                       per cluster (4 CTAs) on two side-by-side
-                                       tiles of the same 256 rows: the CTAs of
-                                       equal rank in the two pairs need the same
-                                       128 rows of A, and each loads one 64-row
-                                       half and multicasts it to both, so A
-                                       leaves L2 once per cluster.  block_n 192,
-                                       224 or 256; with an odd number of tile
-                                       columns the last cluster's second tile
-                                       lies past N and is not stored.  grid must
-                                       be 0; no stream-K.  gemm_schedule_unit
-                                       reports each cluster's own unit u: tile
-                                       row and unit column from the grouped
-                                       raster over tiles_m x ceil(tiles_n / 2),
-                                       tiles 2 x column and 2 x column + 1 */
 } gemm_variant;
 
 /* Plan options; a zero field means "choose automatically". */
@@ -133,8 +114,7 @@ typedef struct {
                            than SM count / 2) are each split into S = 2..4 equal
                            K ranges, S = (SM count / 2) / those tiles, each
                            range at least 4 stages, run as separate units;
-                           gemm_config.sk_max_contrib is S.  Not with
-                           GEMM_VAR_DYNAMIC_2X2. */
+                           gemm_config.sk_max_contrib is S. */
     int l2_policy;      /* L2 eviction priority of the operand loads (warp-specialised
                            variants): 0 = default, 1 = A evict_last and B
                            evict_first, 2 = A evict_first and B evict_last,
@@ -295,13 +275,12 @@ TMAGEMM_API int gemm_select_config(int64_t M, int64_t N, int64_t K, int dtype_ou
  * l2_group_size).  Returns GEMM_ERR_INVALID_ARG if tile is out of range. */
 TMAGEMM_API int gemm_schedule_tile(const gemm_config* cfg, int64_t tile, int* m_tile, int* n_tile);
 
-/* Work unit `index` (0, 1, ...) of persistent worker `worker` (a CTA, a CTA
- * pair for the pair variants, or a cluster of two pairs for dynamic_2x2)
- * under `cfg`, in the order the kernels process them: whole tiles first,
- * then the worker's share of the stream-K part.  Under the dynamic schedule
- * only the worker's own unit (index 0) is fixed before the run -- the rest
- * are taken by cancellation while the kernel runs -- and for dynamic_2x2 the
- * unit is a pair of side-by-side tiles, reported by its unit index.  Writes
+/* Work unit `index` (0, 1, ...) of persistent worker `worker` (a CTA, or a
+ * CTA pair for the pair variants) under `cfg`, in the order the kernels
+ * process them: whole tiles first, then the worker's share of the stream-K
+ * part.  Under the dynamic schedule only the worker's own unit (index 0) is
+ * fixed before the run -- the rest are taken by cancellation while the
+ * kernel runs.  Writes
  * the tile (raster index), its K-block range [kb0, kb1) and the worker's rank
  * among the tile's contributors; returns 1, or 0 when the worker has no unit
  * `index`, or GEMM_ERR_INVALID_ARG. */

@@ -109,28 +109,14 @@ def test_headline_configuration(b):
 @pytest.mark.parametrize("M,N,K,dt,variant,bn", [(256, 256, 256, 0, 5, 64),
                                                  (4096, 4096, 4096, 1, 8, 224),
                                                  (8192, 8192, 8192, 1, 8, 256),
-                                                 (4000, 3000, 5000, 0, 9, 256),
+                                                 (4000, 3000, 5000, 0, 8, 224),
                                                  (4000, 3000, 4992, 0, 8, 224),
-                                                 (8192, 8192, 8200, 1, 9, 256),
+                                                 (8192, 8192, 8200, 1, 8, 256),
                                                  (64, 16384, 16384, 1, 5, 128),
                                                  (128, 65536, 64, 1, 5, 256)])
 def test_auto_variant_choice(b, M, N, K, dt, variant, bn):
     st, c = b.gemm_select_config(M, N, K, dt)
     assert st == 0 and c.variant == variant and c.block_n == bn
-
-
-def test_two_pairs_for_misaligned_rows_only_when_shorter(b):
-    # rows off 128-byte lines (K % 64 != 0): two pairs per cluster when the
-    # makespan model (waves over 36 four-CTA clusters x tile cost x 0.87)
-    # beats one pair per cluster (waves over 76) by 5 %
-    st, c = b.gemm_select_config(4000, 3000, 5000, 0)
-    assert (c.variant, c.block_n, c.block_k, c.grid) == (b.GEMM_VAR_DYNAMIC_2X2, 256, 64,
-                                                         4 * 16 * 6)
-    # aligned rows, explicit options or stream-K keep one pair per cluster
-    for K, opts in [(4992, {}), (5000, {"block_n": 256}), (5000, {"pipe_depth": 4}),
-                    (5000, {"stream_k": "off"}), (5000, {"stream_k": "on"})]:
-        st, c = b.gemm_select_config(4000, 3000, K, 0, b.make_options(**opts))
-        assert st == 0 and c.variant != b.GEMM_VAR_DYNAMIC_2X2, (K, opts)
 
 
 def test_pair_variant_constraints(b):
@@ -183,36 +169,6 @@ def test_dynamic_pair_configuration(b):
                                  b.make_options(variant="dynamic_2cta", stream_k="off"))
     assert st == 0
     for w in range(c.grid // 2):
-        assert b.gemm_worker_units(c, w) == [(w, 0, c.k_blocks, 0, 1)]
-
-
-def test_two_pair_cluster_configuration(b):
-    # Two CTA pairs per cluster on side-by-side tiles, one cluster (4 CTAs)
-    # per unit of two tile columns; an odd column count leaves the last
-    # unit's second tile past N.
-    st, c = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(variant="dynamic_2x2"))
-    assert st == 0, b.last_error()
-    assert c.variant == b.GEMM_VAR_DYNAMIC_2X2
-    assert (c.block_m, c.block_n, c.block_k, c.pipe_depth, c.threads) == (256, 256, 128, 3, 192)
-    assert (c.tiles_m, c.tiles_n, c.num_tiles) == (32, 32, 1024)
-    assert c.grid == 4 * 32 * 16
-    st, c = b.gemm_select_config(600, 776, 328, 0, b.make_options(variant="dynamic_2x2"))
-    assert st == 0 and c.block_n == 192 and c.tiles_n == 5
-    assert c.grid == 4 * c.tiles_m * 3
-    st, c = b.gemm_select_config(4000, 3000, 5000, 0,
-                                 b.make_options(variant="dynamic_2x2", block_n=224))
-    assert st == 0 and (c.tiles_m, c.tiles_n, c.grid) == (16, 14, 4 * 16 * 7)
-    for bad in (dict(block_n=128), dict(block_n=160), dict(grid=144)):
-        st, _ = b.gemm_select_config(8192, 8192, 8192, 1,
-                                     b.make_options(variant="dynamic_2x2", **bad))
-        assert st == b.GEMM_ERR_INVALID_ARG, bad
-    st, _ = b.gemm_select_config(8192, 8192, 8192, 1,
-                                 b.make_options(variant="dynamic_2x2", stream_k="on"))
-    assert st == b.GEMM_ERR_UNSUPPORTED
-    # each cluster's own unit; the rest is decided while the kernel runs
-    st, c = b.gemm_select_config(1000, 1000, 520, 1, b.make_options(variant="dynamic_2x2"))
-    assert st == 0 and c.grid == 4 * c.tiles_m * ((c.tiles_n + 1) // 2)
-    for w in range(c.grid // 4):
         assert b.gemm_worker_units(c, w) == [(w, 0, c.k_blocks, 0, 1)]
 
 
@@ -427,14 +383,6 @@ def test_work_units_cover_every_k_block_once_random_shapes(b):
             st, c = b.gemm_select_config(M, N, K, 1, b.make_options(**opts))
             assert st == 0, (M, N, K, opts, b.last_error())
             _assert_units_cover(b, c)
-        # two pairs per cluster: one cluster per unit of two side-by-side
-        # tiles, each taking its own unit whole
-        st, c = b.gemm_select_config(M, N, K, 1, b.make_options(variant="dynamic_2x2"))
-        assert st == 0, (M, N, K, b.last_error())
-        units = c.tiles_m * ((c.tiles_n + 1) // 2)
-        assert c.grid == 4 * units
-        for w in range(units):
-            assert b.gemm_worker_units(c, w) == [(w, 0, c.k_blocks, 0, 1)], (M, N, K, w)
 
 
 def _assert_units_cover(b, c):
@@ -528,12 +476,12 @@ def test_plan_invariants_over_random_shapes(b):
     # the bytes the stage's copies deliver (both CTAs' with a pair).
     import math
     for M, N, K, dt in _random_shapes(1500, 2024):
-        for v in range(0, 10):
+        for v in range(0, 9):
             st, c = b.gemm_select_config(M, N, K, dt, b.make_options(variant=v))
             where = (M, N, K, dt, v)
             assert st == 0, (where, b.last_error())
             var, bm, bn = c.variant, c.block_m, c.block_n
-            pair = var in (7, 8, 9)
+            pair = var in (7, 8)
             assert var == v or v == 0, where
             assert bm == (256 if pair else 128), where
             assert c.tiles_m == math.ceil(M / bm) and c.tiles_n == math.ceil(N / bn), where
@@ -542,13 +490,11 @@ def test_plan_invariants_over_random_shapes(b):
             assert 1 <= c.pipe_depth <= 8 and 0 < c.smem_bytes <= 232448, where
             t = c.tmem_cols
             assert t == 0 or (32 <= t <= 512 and t & (t - 1) == 0), where
-            if var in (5, 7, 8, 9):
+            if var in (5, 7, 8):
                 assert t >= 2 * bn, where
-            if var in (4, 5, 7, 8, 9):
+            if var in (4, 5, 7, 8):
                 per_cta = (c.a_rows * 64 + (bn // 2 if pair else bn) * 64) * 2 * (c.block_k // 64)
                 assert c.tx_bytes == (2 * per_cta if pair else per_cta), where
             assert c.a_rows == 128 or (c.a_rows == 64 and M <= 64 and not pair), where
-            if var == 9:
-                assert c.grid == 4 * c.tiles_m * math.ceil(c.tiles_n / 2), where
             if var in (5, 7):
                 assert c.grid <= 152, where

@@ -33,7 +33,7 @@ def _built():
     __graft_entry__.build()
 
 
-@pytest.mark.parametrize("variant", ["dynamic_2cta", "persistent", "dynamic_2x2"])
+@pytest.mark.parametrize("variant", ["dynamic_2cta", "persistent", "persistent_2cta"])
 def test_operand_written_by_the_previous_kernel(variant):
     import torch
 
@@ -61,8 +61,8 @@ def test_operand_written_by_the_previous_kernel(variant):
 
 @pytest.mark.parametrize("first,second", [("dynamic_2cta", "persistent"),
                                           ("persistent", "dynamic_2cta"),
-                                          ("dynamic_2x2", "dynamic_2cta"),
-                                          ("dynamic_2cta", "dynamic_2x2")])
+                                          ("persistent_2cta", "dynamic_2cta"),
+                                          ("dynamic_2cta", "persistent_2cta")])
 def test_chained_gemms(first, second):
     import torch
 

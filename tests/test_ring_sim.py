@@ -14,13 +14,10 @@
   fail when a stage completes an odd number of phases per tile, a refill
   before the MMA is done overwrites, an epilogue that does not wait reads an
   incomplete accumulator.
-* The CTA-pair protocol (one or two pairs per cluster) runs clean over the
-  same sweep; with two pairs sharing A, a leader that frees only its own
-  pair's stages deadlocks (empty[s] waits for the other leader), and an
-  empty[s] that counts one arrival lets a producer overwrite a stage the
-  other pair is still reading.
+* The CTA-pair protocol runs clean over the same sweep, and a byte budget
+  armed for one CTA instead of the pair releases the stage early.
 * The response ring of the dynamic tile schedule (cluster launch control)
-  runs clean for one to eight slots, one or two pairs, any response latency
+  runs clean for one to eight slots, any response latency
   and epilogue time; a reader count too high deadlocks; one reader too few
   overwrites a response still unread, or deadlocks, only after a number of
   tiles per cluster that grows with the slot count (beyond what one cluster
@@ -212,50 +209,23 @@ def test_bad_arguments(rs):
         rs.run(no_such_option=1)
 
 
-@pytest.mark.parametrize("pairs", [1, 2])
 @pytest.mark.parametrize("D", [1, 2, 3, 4, 6])
-def test_pair_protocol_runs_clean(rs, pairs, D):
+def test_pair_protocol_runs_clean(rs, D):
     for K in sorted({1, max(1, D - 1), D, D + 1, 2 * D + 1}):
         for tiles in (1, 3):
             for acc in (1, 2):
-                r = rs.run(protocol="pair", pairs=pairs, depth=D, k_tiles=K, tiles=tiles,
+                r = rs.run(protocol="pair", depth=D, k_tiles=K, tiles=tiles,
                            accumulators=acc, chunks=3, epilogue_time=0.7, load_time=1.3,
                            mma_time=1.0, issue_latency=0.1)
-                where = (pairs, D, K, tiles, acc, r["detail"])
+                where = (D, K, tiles, acc, r["detail"])
                 assert r["status_name"] == "ok", where
-                assert r["stages_consumed"] == pairs * tiles * K, where
-                assert r["tiles_stored"] == pairs * tiles, where
+                assert r["stages_consumed"] == tiles * K, where
+                assert r["tiles_stored"] == tiles, where
                 assert r["roles_unique"] == 1, where
 
 
-def test_pairs_in_step_cost_nothing_over_one_pair(rs):
-    # when both pairs run in step, waiting for the other leader's commit
-    # before a refill adds no time
-    kw = dict(protocol="pair", depth=4, k_tiles=16, tiles=3, load_time=2.5, epilogue_time=2.0)
-    one, two = rs.run(pairs=1, **kw), rs.run(pairs=2, **kw)
-    assert one["status_name"] == two["status_name"] == "ok"
-    assert two["makespan"] == pytest.approx(one["makespan"])
-    assert two["mma_busy"] == pytest.approx(2 * one["mma_busy"])
-    assert two["idle_fraction"] == pytest.approx(one["idle_fraction"])
-
-
-def test_two_pairs_need_both_leaders_commits(rs):
+def test_pair_byte_budget_faults(rs):
     kw = dict(protocol="pair", depth=4, k_tiles=8, tiles=2)
-    assert rs.run(pairs=2, **kw)["status_name"] == "ok"
-    own = rs.run(pairs=2, commit_own_pair_only=1, **kw)
-    assert own["status_name"] == "deadlock", own
-    one = rs.run(pairs=2, empty_count_one=1, **kw)
-    assert one["status_name"] == "overwrite", one
-    both = rs.run(pairs=2, commit_own_pair_only=1, empty_count_one=1, **kw)
-    assert both["status_name"] == "overwrite", both
-    # with one pair there is no other leader: both faults are no-ops
-    for fault in (dict(commit_own_pair_only=1), dict(empty_count_one=1)):
-        assert rs.run(pairs=1, **fault, **kw)["status_name"] == "ok", fault
-
-
-@pytest.mark.parametrize("pairs", [1, 2])
-def test_pair_byte_budget_faults(rs, pairs):
-    kw = dict(protocol="pair", pairs=pairs, depth=4, k_tiles=8, tiles=2)
     big = rs.run(bytes_delta=16, **kw)
     assert big["status_name"] == "deadlock" and "16 bytes pending" in big["detail"], big
     # the leader arms its full[s] with one CTA's bytes instead of the pair's
@@ -266,29 +236,28 @@ def test_pair_byte_budget_faults(rs, pairs):
 
 
 def test_pair_bad_arguments(rs):
-    for kw in (dict(pairs=3), dict(pairs=-1), dict(stage_bytes=6), dict(accumulators=0)):
+    for kw in (dict(stage_bytes=6), dict(accumulators=0)):
         assert rs.run(protocol="pair", **kw)["status_name"] == "bad argument", kw
 
 
 CLC = dict(protocol="clc", depth=4, k_tiles=8, load_time=1.2, mma_time=1.0, tiles=9)
 
 
-@pytest.mark.parametrize("pairs", [1, 2])
 @pytest.mark.parametrize("slots", [1, 2, 4, 8])
-def test_clc_ring_runs_clean(rs, pairs, slots):
+def test_clc_ring_runs_clean(rs, slots):
     for tiles in (1, 2, 5, 17):
         for latency in (0.0, 0.5, 3.0, 20.0):
             for epi in (0.0, 2.0, 12.0):
                 for acc in (1, 2):
-                    r = rs.run(**dict(CLC, pairs=pairs, clc_slots=slots, tiles=tiles,
+                    r = rs.run(**dict(CLC, clc_slots=slots, tiles=tiles,
                                       clc_latency=latency, epilogue_time=epi, accumulators=acc))
-                    where = (pairs, slots, tiles, latency, epi, acc, r["detail"])
+                    where = (slots, tiles, latency, epi, acc, r["detail"])
                     assert r["status_name"] == "ok", where
                     assert r["tiles_stored"] == tiles, where
                     # every reader (11 per pair) reads every response, the last
                     # one included (it cancels nothing and ends the loop)
-                    assert r["responses_read"] == 11 * pairs * tiles, where
-                    assert r["stages_consumed"] == pairs * tiles * 8, where
+                    assert r["responses_read"] == 11 * tiles, where
+                    assert r["stages_consumed"] == tiles * 8, where
 
 
 def test_clc_reader_count_too_high_deadlocks(rs):
@@ -304,15 +273,14 @@ def _first_failing_tile_count(rs, limit, **kw):
     return None, None
 
 
-@pytest.mark.parametrize("pairs", [1, 2])
-def test_clc_reader_count_too_low_shows_only_after_many_tiles(rs, pairs):
+def test_clc_reader_count_too_low_shows_only_after_many_tiles(rs):
     # One reader forgotten: each response's surplus arrival completes the
     # slot's next phase one reader earlier, until the requester overwrites a
     # response that epilogue warps have not read, or the parities fall out
     # of step and it deadlocks.  With more slots this takes more tiles per
     # cluster: with four slots more than a GPU run of 8192^3 gives a cluster
     # (1024 tiles over 76 clusters), so only a long run or this model shows it.
-    kw = dict(CLC, pairs=pairs, epilogue_time=6.0, clc_readers_delta=-1)
+    kw = dict(CLC, epilogue_time=6.0, clc_readers_delta=-1)
     n1, r1 = _first_failing_tile_count(rs, 400, clc_slots=1, **kw)
     n4, r4 = _first_failing_tile_count(rs, 400, clc_slots=4, **kw)
     assert n1 is not None and r1["status_name"] == "overwrite", r1
@@ -364,7 +332,7 @@ def test_clc_one_slot_stalls_the_requester(rs):
 
 def test_clc_bad_arguments(rs):
     for kw in (dict(clc_slots=17), dict(clc_slots=-1), dict(clc_latency=-1.0),
-               dict(clc_readers_delta=-11), dict(pairs=3)):
+               dict(clc_readers_delta=-11)):
         assert rs.run(protocol="clc", **kw)["status_name"] == "bad argument", kw
 
 

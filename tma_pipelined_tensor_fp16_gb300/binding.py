@@ -15,7 +15,7 @@ GEMM_OUT_F32, GEMM_OUT_F16 = 0, 1
  GEMM_ERR_NO_DEVICE) = range(6)
 (GEMM_VAR_AUTO, GEMM_VAR_SYNC_TILED, GEMM_VAR_TMA_SERIAL, GEMM_VAR_PIPELINED,
  GEMM_VAR_WS_PIPELINED, GEMM_VAR_PERSISTENT, GEMM_VAR_PERSISTENT_LOCKSTEP,
- GEMM_VAR_PERSISTENT_2CTA, GEMM_VAR_DYNAMIC_2CTA, GEMM_VAR_DYNAMIC_2X2) = range(10)
+ GEMM_VAR_PERSISTENT_2CTA, GEMM_VAR_DYNAMIC_2CTA) = range(9)
 
 VARIANTS = {
     "auto": GEMM_VAR_AUTO,
@@ -27,7 +27,6 @@ VARIANTS = {
     "persistent_lockstep": GEMM_VAR_PERSISTENT_LOCKSTEP,
     "persistent_2cta": GEMM_VAR_PERSISTENT_2CTA,
     "dynamic_2cta": GEMM_VAR_DYNAMIC_2CTA,
-    "dynamic_2x2": GEMM_VAR_DYNAMIC_2X2,
 }
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 

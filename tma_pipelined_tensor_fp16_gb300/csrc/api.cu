@@ -83,7 +83,6 @@ const char* variant_name(int v)
     case VAR_PERSISTENT_LOCKSTEP: return "persistent_lockstep";
     case VAR_PERSISTENT_2CTA: return "persistent_2cta";
     case VAR_DYNAMIC_2CTA: return "dynamic_2cta";
-    case VAR_DYNAMIC_2X2: return "dynamic_2x2";
     default: return "?";
     }
 }
@@ -91,56 +90,31 @@ const char* variant_name(int v)
 bool is_ws(int v)
 {
     return v == VAR_WS_PIPELINED || v == VAR_PERSISTENT || v == VAR_PERSISTENT_2CTA ||
-           v == VAR_DYNAMIC_2CTA || v == VAR_DYNAMIC_2X2;
+           v == VAR_DYNAMIC_2CTA;
 }
 // One resident CTA per SM that takes tile after tile (statically or by
 // cancelling clusters that have not started).
 bool is_persistent(int v)
 {
     return v == VAR_PERSISTENT || v == VAR_PERSISTENT_LOCKSTEP || v == VAR_PERSISTENT_2CTA ||
-           v == VAR_DYNAMIC_2CTA || v == VAR_DYNAMIC_2X2;
+           v == VAR_DYNAMIC_2CTA;
 }
 // 256-row tiles computed by CTA pairs (cta_group::2).
 bool is_pair(int v)
 {
-    return v == VAR_PERSISTENT_2CTA || v == VAR_DYNAMIC_2CTA || v == VAR_DYNAMIC_2X2;
+    return v == VAR_PERSISTENT_2CTA || v == VAR_DYNAMIC_2CTA;
 }
 // One cluster per work unit, clusters cancelling those not started yet.
-bool is_dynamic(int v) { return v == VAR_DYNAMIC_2CTA || v == VAR_DYNAMIC_2X2; }
-// Pair tiles in the cluster's work unit: two side-by-side tiles sharing A.
-int unit_pairs(int v) { return v == VAR_DYNAMIC_2X2 ? 2 : 1; }
+bool is_dynamic(int v) { return v == VAR_DYNAMIC_2CTA; }
 bool has_ring(int v) { return v != VAR_SYNC_TILED && v != VAR_TMA_SERIAL; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
-// The kernel's view of the tile grid: its work units are pair tiles, or (two
-// pairs per cluster) side-by-side pairs of them, so Params::tiles_n counts
-// unit columns and Params::num_tiles units.
-struct UnitGrid {
-    int tiles_n, units;
-};
-UnitGrid unit_grid(const gemm_config& c)
-{
-    const int np = unit_pairs(c.variant);
-    UnitGrid g;
-    g.tiles_n = static_cast<int>(ceil_div(c.tiles_n, np));
-    g.units = c.tiles_m * g.tiles_n;
-    return g;
-}
 
 // Work units one full set of resident clusters takes at a time: the dynamic
 // schedule flips a unit's K direction every snake_span units.
 int snake_span_of(const gemm_config& c, int sms)
 {
-    const int np = unit_pairs(c.variant);
-    return std::max(1, std::min(sms / (2 * np), unit_grid(c).units));
-}
-
-// Rows of A per TMA box: two pairs per cluster load half of each 128-row
-// block each and multicast it to both pairs.
-uint32_t a_box_rows(const gemm_config& c)
-{
-    return static_cast<uint32_t>(c.variant == VAR_DYNAMIC_2X2 ? BLK_M / 2 : c.a_rows);
+    return std::max(1, std::min(sms / 2, c.num_tiles));
 }
 
 // Fraction of launched tile slots that do work when `tiles` tiles run in
@@ -175,10 +149,9 @@ int choose_block_n(int variant, int64_t M, int64_t N, int sms)
 // Pair tile widths the CTA-pair kernel is built for: multiples of 32 (fp32
 // output stores 32-column sub-tiles; fp16 output 64-column sub-tiles plus a
 // directly stored 32-column remainder for widths 160 and 224).
-bool pair_width_ok(int bn, int dtype, int variant)
+bool pair_width_ok(int bn)
 {
-    (void)dtype;  // fp16 widths of 160 / 224 store their last 32 columns directly
-    if (variant == VAR_DYNAMIC_2X2) return bn == 192 || bn == 224 || bn == 256;
+    // fp16 widths of 160 / 224 store their last 32 columns directly
     return bn == 128 || bn == 160 || bn == 192 || bn == 224 || bn == 256;
 }
 
@@ -189,26 +162,21 @@ bool pair_width_ok(int bn, int dtype, int variant)
 // wave and overhang losses divided out (narrower tiles issue more barrier
 // round trips and load more operand bytes per FLOP).  Stages of two K blocks
 // (ksub = 2) halve the round trips, and narrow tiles lose less.
-int choose_pair_bn(int64_t M, int64_t N, int sms, int dtype, int ksub, int variant)
+int choose_pair_bn(int64_t M, int64_t N, int sms, int ksub)
 {
     const int widths[5] = {256, 224, 192, 160, 128};
     const double eff_k64[5] = {1.0, 0.92, 0.79, 0.73, 0.54};
     const double eff_k128[5] = {1.0, 0.94, 0.89, 0.81, 0.70};
     const double* tile_eff = ksub == 2 ? eff_k128 : eff_k64;
-    // A work unit of the two-pair variant is two side-by-side tiles; with an
-    // odd number of tile columns the last unit's second tile lies past N.
-    const int np = unit_pairs(variant);
-    const int64_t slots = sms / (2 * np);
+    const int64_t slots = sms / 2;
     const int64_t tm = ceil_div(M, 2 * BLK_M);
     int best = 256;
     double best_score = -1.0;
     for (int i = 0; i < 5; ++i) {
         const int bn = widths[i];
-        if (!pair_width_ok(bn, dtype, variant)) continue;
         const int64_t tn = ceil_div(N, bn);
-        const int64_t un = ceil_div(tn, np);
-        const double cols = static_cast<double>(N) / static_cast<double>(un * np * bn);
-        const double score = wave_efficiency(tm * un, static_cast<int>(slots)) * cols * tile_eff[i];
+        const double cols = static_cast<double>(N) / static_cast<double>(tn * bn);
+        const double score = wave_efficiency(tm * tn, static_cast<int>(slots)) * cols * tile_eff[i];
         if (score > best_score + 1e-9) {
             best_score = score;
             best = bn;
@@ -233,57 +201,6 @@ int auto_variant(int64_t M, int64_t N, int sms, const gemm_options& opts)
     return VAR_PERSISTENT;
 }
 
-// Resident clusters of four CTAs at the pair kernels' shared-memory size:
-// cudaOccupancyMaxActiveClusters gives 36 on GB300's 152 SMs (144 SMs; the
-// GPCs' TPC counts leave 8 SMs over), against SM count / 2 = 76 clusters of
-// two.
-int four_cta_clusters(int sms) { return sms >= 16 ? (sms / 2 - 4) / 2 : 1; }
-
-// Relative time of one tile of a CTA pair, 256 rows x `bn` columns, against a
-// 256 x 256 tile (the per-width tables of choose_pair_bn).
-double pair_tile_cost(int bn, int ksub)
-{
-    const int widths[5] = {256, 224, 192, 160, 128};
-    const double eff_k64[5] = {1.0, 0.92, 0.79, 0.73, 0.54};
-    const double eff_k128[5] = {1.0, 0.94, 0.89, 0.81, 0.70};
-    for (int i = 0; i < 5; ++i)
-        if (widths[i] == bn) return (bn / 256.0) / (ksub == 2 ? eff_k128[i] : eff_k64[i]);
-    return 1.0;
-}
-
-// Automatic plans for rows of A and B that do not start on 128-byte lines
-// (K % 64 != 0): every box row then straddles two lines, the main loop waits
-// on operand loads, and two pairs per cluster sharing A (dynamic_2x2) run a
-// pair tile in 0.87 of the time (measured, 4000 x 3000 x 5000: a wave of
-// 224-wide tiles 26.4 us against 30.4).  Fewer clusters fit, so the choice
-// compares makespans: waves x tile cost, over the built widths of each
-// variant, and takes dynamic_2x2 when it is at least 5 % shorter.  Returns
-// the chosen width for dynamic_2x2, or 0 to keep one pair per cluster.
-int misaligned_two_pair_width(int64_t M, int64_t N, int sms, int dtype)
-{
-    const int64_t tm = ceil_div(M, 2 * BLK_M);
-    const int64_t cl2 = sms / 2, cl4 = four_cta_clusters(sms);
-    double pair_t = 1e300, quad_t = 1e300;
-    int quad_bn = 0;
-    const int widths[5] = {256, 224, 192, 160, 128};
-    for (int bn : widths) {
-        const int64_t tn = ceil_div(N, bn);
-        if (pair_width_ok(bn, dtype, VAR_DYNAMIC_2CTA)) {
-            const double t = static_cast<double>(ceil_div(tm * tn, cl2)) * pair_tile_cost(bn, 1);
-            if (t < pair_t) pair_t = t;
-        }
-        if (pair_width_ok(bn, dtype, VAR_DYNAMIC_2X2)) {
-            const double t =
-                static_cast<double>(ceil_div(tm * ceil_div(tn, 2), cl4)) * pair_tile_cost(bn, 1) * 0.87;
-            if (t < quad_t) {
-                quad_t = t;
-                quad_bn = bn;
-            }
-        }
-    }
-    return quad_t < 0.95 * pair_t ? quad_bn : 0;
-}
-
 int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_options* o,
                        int sms, int smem_optin, gemm_config* c)
 {
@@ -303,7 +220,7 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     if ((N * elt) % 16 != 0)
         return fail(GEMM_ERR_UNSUPPORTED,
                     "N * sizeof(output) must be a multiple of 16 bytes (TMA row stride of C)");
-    if (opts.variant < 0 || opts.variant > VAR_DYNAMIC_2X2)
+    if (opts.variant < 0 || opts.variant > VAR_DYNAMIC_2CTA)
         return fail(GEMM_ERR_INVALID_ARG, "unknown variant");
     if (opts.pipe_depth < 0 || opts.pipe_depth > MAX_STAGES)
         return fail(GEMM_ERR_INVALID_ARG, "pipe_depth must be 0 (auto) or 1..8");
@@ -323,23 +240,12 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
         return fail(GEMM_ERR_INVALID_ARG, "k_order must be 0 (auto), 1 (ascending) or 2 (snake)");
     if (sms < 1 || smem_optin < 1) return fail(GEMM_ERR_INVALID_ARG, "bad device limits");
 
-    int variant = opts.variant == VAR_AUTO ? auto_variant(M, N, sms, opts) : opts.variant;
-    if (opts.variant == VAR_AUTO && variant == VAR_DYNAMIC_2CTA && K % 64 != 0 &&
-        opts.block_n == 0 && opts.pipe_depth == 0 && opts.block_k != 128 && opts.stream_k == 0) {
-        const int qbn = misaligned_two_pair_width(M, N, sms, dtype);
-        if (qbn) {
-            variant = VAR_DYNAMIC_2X2;
-            opts.block_n = qbn;
-        }
-    }
+    const int variant = opts.variant == VAR_AUTO ? auto_variant(M, N, sms, opts) : opts.variant;
     if (opts.debug_stall && !is_ws(variant))
         return fail(GEMM_ERR_INVALID_ARG, "debug_stall needs a warp-specialised variant");
     if (is_dynamic(variant) && opts.grid != 0)
         return fail(GEMM_ERR_INVALID_ARG,
-                    "the dynamic variants launch one cluster per work unit: grid must be 0 (auto)");
-    if (variant == VAR_DYNAMIC_2X2 && opts.stream_k == 2)
-        return fail(GEMM_ERR_UNSUPPORTED,
-                    "dynamic_2x2 schedules whole tiles: stream-K needs another pair variant");
+                    "the dynamic variant launches one cluster per work unit: grid must be 0 (auto)");
     if (opts.block_k == 128 && !is_pair(variant))
         return fail(GEMM_ERR_INVALID_ARG, "block_k = 128 is built for the CTA-pair variants");
     // K blocks of 64 per stage (two 128-byte swizzle atoms at block_k = 128).
@@ -354,13 +260,11 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     const bool auto_k128 =
         opts.block_k == 0 && is_pair(variant) && opts.pipe_depth == 0 && K % 64 == 0;
     const int ksub = (opts.block_k == 128 || auto_k128) ? 2 : 1;
-    if (is_pair(variant) && opts.block_n != 0 && !pair_width_ok(opts.block_n, dtype, variant))
+    if (is_pair(variant) && opts.block_n != 0 && !pair_width_ok(opts.block_n))
         return fail(GEMM_ERR_INVALID_ARG,
-                    variant == VAR_DYNAMIC_2X2
-                        ? "dynamic_2x2 tile width (block_n) must be 192, 224 or 256"
-                        : "CTA-pair tile width (block_n) must be 128, 160, 192, 224 or 256");
+                    "CTA-pair tile width (block_n) must be 128, 160, 192, 224 or 256");
     const int bn = opts.block_n   ? opts.block_n
-                   : is_pair(variant) ? choose_pair_bn(M, N, sms, dtype, ksub, variant)
+                   : is_pair(variant) ? choose_pair_bn(M, N, sms, ksub)
                                       : choose_block_n(variant, M, N, sms);
     // Shared memory per CTA holds B tiles of `bn_cta` rows: a CTA of a pair
     // keeps half of the pair tile's B rows.
@@ -444,12 +348,9 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     };
     const bool sk_capable = variant == VAR_PERSISTENT || variant == VAR_PERSISTENT_2CTA;
     if (is_dynamic(variant)) {
-        // one cluster per work unit (pair tile, or two side-by-side pair
-        // tiles); running clusters cancel the rest
-        const int np = unit_pairs(variant);
-        const int64_t units = tm * ceil_div(tn, np);
-        if (2 * np * units > LIM) return fail(GEMM_ERR_UNSUPPORTED, "too many output tiles");
-        c->grid = static_cast<int>(2 * np * units);
+        // one cluster per pair tile; running clusters cancel the rest
+        if (2 * tiles > LIM) return fail(GEMM_ERR_UNSUPPORTED, "too many output tiles");
+        c->grid = static_cast<int>(2 * tiles);
     } else if (is_pair(variant)) {
         // clusters of two CTAs, one pair tile per cluster at a time
         int64_t pairs = (opts.grid ? opts.grid : sms) / 2;
@@ -767,7 +668,7 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
     const gemm_config& c = plan->cfg;
     if (A != plan->mapA_ptr || B != plan->mapB_ptr || C != plan->mapC_ptr) {
         int r = encode_2d(&plan->tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, plan->K, plan->M,
-                          plan->K * 2, BLK_K, a_box_rows(c), "A");
+                          plan->K * 2, BLK_K, static_cast<uint32_t>(c.a_rows), "A");
         if (r == GEMM_OK)
             r = encode_2d(&plan->tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, plan->K, plan->N,
                           plan->K * 2, BLK_K, is_pair(c.variant) ? c.block_n / 2 : c.block_n,
@@ -808,11 +709,8 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
     p.N = static_cast<int>(plan->N);
     p.K = static_cast<int>(plan->K);
     p.tiles_m = c.tiles_m;
-    {
-        const UnitGrid ug = unit_grid(c);
-        p.tiles_n = ug.tiles_n;
-        p.num_tiles = ug.units;
-    }
+    p.tiles_n = c.tiles_n;
+    p.num_tiles = c.num_tiles;
     p.k_blocks = c.k_blocks;
     p.group_m = c.group_m;
     p.pipe_depth = c.pipe_depth;
@@ -829,7 +727,7 @@ int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_
     p.snake_span = plan->snake_span;
     p.ksub = c.block_k / BLK_K;
     p.a_rows = c.a_rows;
-    p.dp_tiles = unit_pairs(c.variant) == 1 ? c.dp_tiles : p.num_tiles;
+    p.dp_tiles = c.dp_tiles;
     p.sk_tiles = c.sk_tiles;
     p.sk_kb_per_worker = c.sk_kb_per_worker;
     p.sk_max_contrib = c.sk_max_contrib;
@@ -1093,15 +991,13 @@ int gemm_schedule_unit(const gemm_config* cfg, int worker, int index, int* tile,
 {
     if (!cfg || !tile || !kb0 || !kb1 || !contrib || !ncontrib || index < 0)
         return fail(GEMM_ERR_INVALID_ARG, "NULL argument or negative index");
-    // workers: clusters (of NP CTA pairs) or CTAs; two pairs per cluster take
-    // units of two side-by-side tiles
-    const int np = unit_pairs(cfg->variant);
-    const int workers = is_pair(cfg->variant) ? cfg->grid / (2 * np) : cfg->grid;
+    // workers: clusters (CTA pairs) or CTAs
+    const int workers = is_pair(cfg->variant) ? cfg->grid / 2 : cfg->grid;
     if (worker < 0 || worker >= workers) return fail(GEMM_ERR_INVALID_ARG, "worker out of range");
     // the kernels count K in pipeline stages of `ks` K blocks; report blocks
     const int ks = cfg->block_k > BLK_K ? cfg->block_k / BLK_K : 1;
     const int stages = (cfg->k_blocks + ks - 1) / ks;
-    const int dp = np == 1 ? cfg->dp_tiles : unit_grid(*cfg).units;
+    const int dp = cfg->dp_tiles;
     if (is_dynamic(cfg->variant)) {
         // the cluster's own unit; the rest is decided while the kernel runs
         if (index > 0) {
@@ -1243,8 +1139,8 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     if (r != GEMM_OK) return r;
 
     CUtensorMap tmA, tmB, tmC;
-    r = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, K * 2, BLK_K, a_box_rows(c),
-                  "A");
+    r = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, K * 2, BLK_K,
+                  static_cast<uint32_t>(c.a_rows), "A");
     if (r == GEMM_OK)
         r = encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, K * 2, BLK_K,
                       static_cast<uint32_t>(is_pair(c.variant) ? c.block_n / 2 : c.block_n), "B");
@@ -1276,9 +1172,8 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
     p.tiles_m = c.tiles_m;
-    const UnitGrid ug = unit_grid(c);
-    p.tiles_n = ug.tiles_n;
-    p.num_tiles = ug.units;
+    p.tiles_n = c.tiles_n;
+    p.num_tiles = c.num_tiles;
     p.k_blocks = c.k_blocks;
     p.group_m = c.group_m;
     p.pipe_depth = c.pipe_depth;
@@ -1293,7 +1188,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     }
     p.budget_ns = 2000ull * 1000000ull;
     p.debug_stall = 0;
-    p.dp_tiles = ug.units;
+    p.dp_tiles = c.num_tiles;
     p.sk_tiles = 0;
     p.sk_kb_per_worker = 0;
     p.sk_max_contrib = 0;

@@ -11,11 +11,6 @@ cudaError_t launch_pair(const LaunchSpec& s, cudaStream_t stream)
 {
     if ((s.grid & 1) || (s.p.ksub != 1 && s.p.ksub != 2)) return cudaErrorInvalidValue;
     const bool k2 = s.p.ksub == 2;
-    if (s.variant == VAR_DYNAMIC_2X2) {
-        if (s.grid & 3) return cudaErrorInvalidValue;
-        return k2 ? launch_pair_width<true, 2, 2>(s, stream)
-                  : launch_pair_width<true, 1, 2>(s, stream);
-    }
     if (s.variant == VAR_DYNAMIC_2CTA)
         return k2 ? launch_pair_width<true, 2>(s, stream) : launch_pair_width<true, 1>(s, stream);
     if (s.variant == VAR_PERSISTENT_2CTA)

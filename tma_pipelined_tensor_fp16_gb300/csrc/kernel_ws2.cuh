@@ -1,12 +1,10 @@
 // kernel_ws2.cuh -- the persistent, warp-specialised GEMM on CTA pairs: a
 // cluster of two CTAs on the two SMs of a TPC computes one 256 x PAIR_BN
 // output tile with tcgen05.mma.cta_group::2 issued by the pair's leader.
-// Template flags: DYN (tile schedule, below), KS (K blocks of 64 per
-// pipeline stage: 1, or 2 for stages of K = 128) and NP (CTA pairs per
-// cluster, below).  Each (DYN, KS, NP) combination is instantiated by a
-// translation unit of its own: kernel_ws2.cu, kernel_ws2_k2.cu,
-// kernel_ws2_dyn.cu, kernel_ws2_dyn_k2.cu, kernel_ws2_x2.cu,
-// kernel_ws2_x2_k2.cu.
+// Template flags: DYN (tile schedule, below) and KS (K blocks of 64 per
+// pipeline stage: 1, or 2 for stages of K = 128).  Each (DYN, KS) combination
+// is instantiated by a translation unit of its own: kernel_ws2.cu,
+// kernel_ws2_k2.cu, kernel_ws2_dyn.cu, kernel_ws2_dyn_k2.cu.
 //
 // Why pairs: with one CTA per tile the 128 x 256 tile leaves room for only
 // four 48 KB stages beside the output staging.  In a pair each CTA keeps its
@@ -45,19 +43,7 @@
 //            pipelining with TMA" (Step 6, the persistent scheduler) names
 //            cluster launch control as the upgrade of its precomputed tile
 //            assignment: hardware work-stealing for uneven tile costs.
-//
-// Two pairs per cluster (NP = 2, dynamic schedule only): a cluster of four
-// CTAs takes a unit of two side-by-side pair tiles of the same 256 rows.  The
-// CTAs of equal rank in the two pairs (0 and 2, 1 and 3) need the same 128
-// rows of A; each loads one 64-row half and multicasts it into both (the
-// bytes landing in a pair are signalled on that pair's leader's full[s]),
-// so A leaves L2 once per cluster instead of twice.  Because a producer
-// writes into the other pair's stage too, a stage is free only when both
-// leaders have committed it: each leader's MMA commit reaches the empty[s]
-// barriers of all four CTAs, which count two arrivals.  The leader of rank 0
-// issues the cancellation requests; every reader of the four CTAs releases
-// the response slot.  On GB300 only 36 clusters of four fit at once (144 of
-// the 152 SMs), against 76 of two.
+
 #pragma once
 
 #include "device_common.cuh"
@@ -98,10 +84,9 @@ constexpr int CLC_READERS_PER_PAIR = 11;
 // One reader's take of response `use` (slot use % CLC_SLOTS): wait for it,
 // decode it, re-arm this CTA's full barrier of the slot for the slot's next
 // use when `arm` (one reader per CTA, its producer), and release the slot to
-// the cluster's rank-0 CTA.  Returns the work unit of the cancelled cluster (NP CTA pairs
-// per cluster), or -1 when nothing was cancelled (every cluster has started)
-// or the run aborted.
-template <int NP>
+// the cluster's rank-0 CTA.  Returns the work unit (pair tile) of the
+// cancelled cluster, or -1 when nothing was cancelled (every cluster has
+// started) or the run aborted.
 __device__ __forceinline__ int clc_read(uint32_t bars, int use, Watchdog& wd, bool arm)
 {
     const int slot = use % CLC_SLOTS;
@@ -116,13 +101,13 @@ __device__ __forceinline__ int clc_read(uint32_t bars, int use, Watchdog& wd, bo
     // wait for the MMA issuer's queued tensor-core work at every tile start
     // (measured 1.1 us per tile of drained MMA pipe at 8192^3).
     mbar_arrive_cluster_relaxed(map_shared_rank(bar_addr(bars, BAR_CLC_EMPTY + slot), 0));
-    return cancelled ? static_cast<int>(cta_x / (2u * NP)) : -1;
+    return cancelled ? static_cast<int>(cta_x / 2u) : -1;
 }
 
 // The tile sequence of one cluster as each of its roles walks it: the static
 // WorkIter sequence, or (DYN) the cluster's own tile followed by the tile of
 // every cluster that its cancellation requests took over.
-template <bool DYN, int NP>
+template <bool DYN>
 struct PairTiles {
     WorkIter it;  // static schedule
     int own;      // dynamic: this cluster's own unit
@@ -138,7 +123,7 @@ struct PairTiles {
             return it.next(u);
         } else {
             int t = own;
-            if (use >= 0) t = clc_read<NP>(bars, use, wd, arm);
+            if (use >= 0) t = clc_read(bars, use, wd, arm);
             ++use;
             return take(u, t);
         }
@@ -154,7 +139,7 @@ struct PairTiles {
         } else {
             int t = own;
             if (use >= 0) {
-                t = lane == 0 ? clc_read<NP>(bars, use, wd, arm) : -1;
+                t = lane == 0 ? clc_read(bars, use, wd, arm) : -1;
                 t = __shfl_sync(0xffffffffu, t, 0);
             }
             ++use;
@@ -184,10 +169,9 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t x)
 }
 
 // PAIR_BN: output columns per pair tile (a multiple of 32 up to 256; each CTA
-// holds PAIR_BN / 2 rows of B per stage).  NP: CTA pairs per cluster, 1 or 2
-// (two pairs on side-by-side tiles of the same 256 rows, sharing A).
-template <int PAIR_BN, bool F16OUT, bool DYN, int KS, int NP = 1>
-__global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
+// holds PAIR_BN / 2 rows of B per stage).
+template <int PAIR_BN, bool F16OUT, bool DYN, int KS>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
     k_ws2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
           const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB2,
           const Params p)
@@ -202,7 +186,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
     // the epilogue stores in whole sub-tiles.
     constexpr int NARROW_BN = PAIR_BN / 2;
     constexpr bool NARROW_OK =
-        NP == 1 && DYN && (F16OUT ? (NARROW_BN % 64 == 0 || NARROW_BN % 64 == 32)
+        DYN && (F16OUT ? (NARROW_BN % 64 == 0 || NARROW_BN % 64 == 32)
                                   : NARROW_BN % 32 == 0);
     constexpr int ACC = 2;
     // two accumulators of PAIR_BN columns, rounded up to a legal allocation
@@ -217,7 +201,6 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
     // which lands the same bytes and keeps the zero fill past a ragged K edge
     // (a 3-D view of a row-major matrix would read the next row there).
     static_assert(KS == 1 || KS == 2, "K blocks of 64 per stage");
-    static_assert(NP == 1 || (NP == 2 && DYN), "two pairs per cluster: dynamic schedule only");
     const SmemLayout L = smem_layout(D * KS, HALF_BN, NUM_STAGING);
     const uint32_t sA = sm.base + L.a;
     const uint32_t sB = sm.base + L.b;
@@ -228,18 +211,15 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
     const int warp = tid >> 5;
     const uint32_t lane = lane_id();
     const uint32_t rank = cluster_ctarank();
-    const uint32_t pr = rank & 1u;             // rank in the pair: 0 = leader
-    const uint32_t pp = rank >> 1;             // pair in the cluster
-    const uint32_t leader_rank = rank & ~1u;   // this pair's leader
+    const uint32_t pr = rank;                  // rank in the pair: 0 = leader
+    const uint32_t leader_rank = 0;
     const bool leader = pr == 0;
     Watchdog wd = make_watchdog(p);
-    // One work unit per cluster at a time: a pair tile (NP = 1), or two side-
-    // by-side pair tiles of one row of tiles (NP = 2; p.tiles_n counts such
-    // column pairs, and a second tile past N is computed but never stored).
-    const int cluster = static_cast<int>(blockIdx.x) / (2 * NP);
-    const int nclusters = static_cast<int>(gridDim.x) / (2 * NP);
+    // One work unit (a pair tile, or a K range of one) per cluster at a time.
+    const int cluster = static_cast<int>(blockIdx.x) / 2;
+    const int nclusters = static_cast<int>(gridDim.x) / 2;
     const int KB = (p.k_blocks + KS - 1) / KS;  // stages per tile
-    PairTiles<DYN, NP> tiles0;
+    PairTiles<DYN> tiles0;
     tiles0.it.init(cluster, nclusters, p.dp_tiles, p.sk_tiles, KB, p.sk_kb_per_worker);
     tiles0.own = cluster;
     tiles0.use = -1;
@@ -258,7 +238,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
         if (NARROW_OK && p.tail_halves > 0) prefetch_tensormap(&tmB2);
         for (int s = 0; s < D; ++s) {
             mbar_init(bar_addr(bars, BAR_FULL + s), 1);   // leader: its producer's expect_tx
-            mbar_init(bar_addr(bars, BAR_EMPTY + s), NP);  // each leader's multicast commit
+            mbar_init(bar_addr(bars, BAR_EMPTY + s), 1);   // the leader's multicast commit
         }
         for (int a = 0; a < ACC; ++a) {
             mbar_init(bar_addr(bars, BAR_TMEM_FULL + a), 1);   // the leader's multicast commit
@@ -267,7 +247,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
         if constexpr (DYN) {
             for (int j = 0; j < CLC_SLOTS; ++j) {
                 mbar_init(bar_addr(bars, BAR_CLC_FULL + j), 1);  // this CTA's producer arms it
-                mbar_init(bar_addr(bars, BAR_CLC_EMPTY + j), CLC_READERS_PER_PAIR * NP);  // rank 0's
+                mbar_init(bar_addr(bars, BAR_CLC_EMPTY + j), CLC_READERS_PER_PAIR);  // rank 0's
             }
         }
         mbar_init(bar_addr(bars, BAR_DRAIN), 1);
@@ -318,7 +298,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
         int end_stage = 0;       // ring position just after the last armed stage
         uint32_t end_phase = 0;
         int requests = 0;        // dynamic schedule: cancellation requests issued
-        PairTiles<DYN, NP> tiles = tiles0;
+        PairTiles<DYN> tiles = tiles0;
         WorkUnit u;
         int ui = 0;
         while (tiles.next_warp(u, bars, wd, lane, true)) {
@@ -346,7 +326,6 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
             unsigned long long empty_wait_ns = 0;
             int mt, nt;
             raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
-            nt = nt * NP + static_cast<int>(pp);
             const bool narrow = NARROW_OK && u.half != 0;
             const int m0 = mt * PAIR_BM + static_cast<int>(pr) * BLK_M;
             const int nb = narrow ? nt * PAIR_BN + (u.half - 1) * NARROW_BN +
@@ -371,22 +350,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
                     for (int s = 0; s < KS; ++s) {
                         const int slot = stage * KS + s;
                         const int kx = (kb * KS + s) * BLK_K;
-                        if constexpr (NP == 2) {
-                            // Both pairs need this CTA's 128 rows of A (the
-                            // CTAs of equal rank in the two pairs): each loads
-                            // the 64-row half of its pair index into both, so
-                            // each row of A leaves L2 once per cluster.
-                            const uint16_t mask = static_cast<uint16_t>((1u << pr) | (4u << pr));
-                            tma_load_2d_pair_multicast(
-                                sA + slot * A_TILE_BYTES + pp * (A_TILE_BYTES / 2), &tmA,
-                                fb_leader, kx, m0 + static_cast<int>(pp) * (BLK_M / 2), mask);
-                            if (p.l2_policy == 0)
-                                tma_load_2d_pair(sB + slot * b_tile_bytes(HALF_BN), mapB,
-                                                 fb_leader, kx, nb);
-                            else
-                                tma_load_2d_pair_hint(sB + slot * b_tile_bytes(HALF_BN), mapB,
-                                                      fb_leader, kx, nb, pol_b);
-                        } else if (p.l2_policy == 0) {
+                        if (p.l2_policy == 0) {
                             tma_load_2d_pair(sA + slot * A_TILE_BYTES, &tmA, fb_leader, kx, m0);
                             tma_load_2d_pair(sB + slot * b_tile_bytes(HALF_BN), mapB, fb_leader,
                                              kx, nb);
@@ -456,7 +420,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
             int acc = 0;
             uint32_t acc_phase = 0;
             int mui = 0;
-            PairTiles<DYN, NP> tiles = tiles0;
+            PairTiles<DYN> tiles = tiles0;
             WorkUnit u;
             while (tiles.next_warp(u, bars, wd, lane)) {
                 const int t = u.tile;
@@ -492,10 +456,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
                                                 (ki == 0 && s == 0 && kk == 0) ? 0u : 1u);
                         }
                         // frees stage `stage` in both CTAs once these MMAs have read it
-                        // (NP = 2: also in the other pair, whose producers
-                        // write their half of A into this pair's stage)
-                        mma_commit_pair_multicast(bar_addr(bars, BAR_EMPTY + stage),
-                                                  NP == 1 ? 0x3 : 0xF);
+                        mma_commit_pair_multicast(bar_addr(bars, BAR_EMPTY + stage), 0x3);
                     }
                     __syncwarp();
                     if (++stage == D) {
@@ -504,8 +465,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
                     }
                 }
                 if (lane == 0 && !wd.aborted)
-                    mma_commit_pair_multicast(bar_addr(bars, BAR_TMEM_FULL + acc),
-                                              static_cast<uint16_t>(0x3u << (2u * pp)));
+                    mma_commit_pair_multicast(bar_addr(bars, BAR_TMEM_FULL + acc), 0x3);
                 if (tr) {
                     trace_unit(p, mui, TRACE_U_MMA_LAST, globaltimer_ns());
                     trace_unit(p, mui, TRACE_U_FULL_WAIT, full_wait_ns);
@@ -530,7 +490,7 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t sub_count = 0;
-        PairTiles<DYN, NP> tiles = tiles0;
+        PairTiles<DYN> tiles = tiles0;
         WorkUnit u;
         volatile uint32_t* ticket_smem =
             reinterpret_cast<volatile uint32_t*>(sm.gen + L.bars + TICKET_SLOT_OFFSET);
@@ -539,7 +499,6 @@ __global__ void __cluster_dims__(2 * NP, 1, 1) __launch_bounds__(PAIR_THREADS, 1
             const int t = u.tile;
             int mt, nt;
             raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, mt, nt);
-            nt = nt * NP + static_cast<int>(pp);
             const int m0 = mt * PAIR_BM + static_cast<int>(pr) * BLK_M;
             wd.wait(bar_addr(bars, BAR_TMEM_FULL + acc), acc_phase, WAIT_TMEM_FULL, t, -1);
             tc_fence_after_sync();
@@ -605,48 +564,30 @@ cudaError_t launch_pair_kernel(KernelT kernel, const LaunchSpec& s, cudaStream_t
     return launch_programmatic(kernel, s, PAIR_THREADS, stream, s.tmB2 ? *s.tmB2 : *s.tmB);
 }
 
-// Launch k_ws2<block_n, f16out, DYN, KS, NP> for one of the built pair tile
-// widths (NP = 2: 192, 224 and 256 only).  Each (DYN, KS, NP) combination is
-// instantiated by a translation unit of its own (kernel_ws2.cu,
-// kernel_ws2_k2.cu, kernel_ws2_dyn.cu, kernel_ws2_dyn_k2.cu, kernel_ws2_x2.cu,
-// kernel_ws2_x2_k2.cu), so that they compile in parallel.
-template <bool DYN, int KS, int NP = 1>
+// Launch k_ws2<block_n, f16out, DYN, KS> for one of the built pair tile
+// widths.  Each (DYN, KS) combination is instantiated by a translation unit
+// of its own (kernel_ws2.cu, kernel_ws2_k2.cu, kernel_ws2_dyn.cu,
+// kernel_ws2_dyn_k2.cu), so that they compile in parallel.
+template <bool DYN, int KS>
 cudaError_t launch_pair_width(const LaunchSpec& s, cudaStream_t stream)
 {
-    if constexpr (NP == 1) {
-        if (s.f16out) {
-            switch (s.block_n) {
-            case 128: return launch_pair_kernel(k_ws2<128, true, DYN, KS>, s, stream);
-            case 160: return launch_pair_kernel(k_ws2<160, true, DYN, KS>, s, stream);
-            case 192: return launch_pair_kernel(k_ws2<192, true, DYN, KS>, s, stream);
-            case 224: return launch_pair_kernel(k_ws2<224, true, DYN, KS>, s, stream);
-            case 256: return launch_pair_kernel(k_ws2<256, true, DYN, KS>, s, stream);
-            default: return cudaErrorInvalidValue;
-            }
-        }
+    if (s.f16out) {
         switch (s.block_n) {
-        case 128: return launch_pair_kernel(k_ws2<128, false, DYN, KS>, s, stream);
-        case 160: return launch_pair_kernel(k_ws2<160, false, DYN, KS>, s, stream);
-        case 192: return launch_pair_kernel(k_ws2<192, false, DYN, KS>, s, stream);
-        case 224: return launch_pair_kernel(k_ws2<224, false, DYN, KS>, s, stream);
-        case 256: return launch_pair_kernel(k_ws2<256, false, DYN, KS>, s, stream);
+        case 128: return launch_pair_kernel(k_ws2<128, true, DYN, KS>, s, stream);
+        case 160: return launch_pair_kernel(k_ws2<160, true, DYN, KS>, s, stream);
+        case 192: return launch_pair_kernel(k_ws2<192, true, DYN, KS>, s, stream);
+        case 224: return launch_pair_kernel(k_ws2<224, true, DYN, KS>, s, stream);
+        case 256: return launch_pair_kernel(k_ws2<256, true, DYN, KS>, s, stream);
         default: return cudaErrorInvalidValue;
         }
-    } else {
-        if (s.f16out) {
-            switch (s.block_n) {
-            case 192: return launch_pair_kernel(k_ws2<192, true, DYN, KS, NP>, s, stream);
-            case 224: return launch_pair_kernel(k_ws2<224, true, DYN, KS, NP>, s, stream);
-            case 256: return launch_pair_kernel(k_ws2<256, true, DYN, KS, NP>, s, stream);
-            default: return cudaErrorInvalidValue;
-            }
-        }
-        switch (s.block_n) {
-        case 192: return launch_pair_kernel(k_ws2<192, false, DYN, KS, NP>, s, stream);
-        case 224: return launch_pair_kernel(k_ws2<224, false, DYN, KS, NP>, s, stream);
-        case 256: return launch_pair_kernel(k_ws2<256, false, DYN, KS, NP>, s, stream);
-        default: return cudaErrorInvalidValue;
-        }
+    }
+    switch (s.block_n) {
+    case 128: return launch_pair_kernel(k_ws2<128, false, DYN, KS>, s, stream);
+    case 160: return launch_pair_kernel(k_ws2<160, false, DYN, KS>, s, stream);
+    case 192: return launch_pair_kernel(k_ws2<192, false, DYN, KS>, s, stream);
+    case 224: return launch_pair_kernel(k_ws2<224, false, DYN, KS>, s, stream);
+    case 256: return launch_pair_kernel(k_ws2<256, false, DYN, KS>, s, stream);
+    default: return cudaErrorInvalidValue;
     }
 }
 
@@ -654,7 +595,5 @@ extern template cudaError_t launch_pair_width<false, 1>(const LaunchSpec&, cudaS
 extern template cudaError_t launch_pair_width<false, 2>(const LaunchSpec&, cudaStream_t);
 extern template cudaError_t launch_pair_width<true, 1>(const LaunchSpec&, cudaStream_t);
 extern template cudaError_t launch_pair_width<true, 2>(const LaunchSpec&, cudaStream_t);
-extern template cudaError_t launch_pair_width<true, 1, 2>(const LaunchSpec&, cudaStream_t);
-extern template cudaError_t launch_pair_width<true, 2, 2>(const LaunchSpec&, cudaStream_t);
 
 }  // namespace tg

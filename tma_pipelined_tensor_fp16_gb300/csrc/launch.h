@@ -18,8 +18,7 @@ enum : int {
     VAR_PERSISTENT = 5,
     VAR_PERSISTENT_LOCKSTEP = 6,
     VAR_PERSISTENT_2CTA = 7,
-    VAR_DYNAMIC_2CTA = 8,
-    VAR_DYNAMIC_2X2 = 9
+    VAR_DYNAMIC_2CTA = 8
 };
 
 struct LaunchSpec {
@@ -44,9 +43,8 @@ cudaError_t launch_ladder(const LaunchSpec& s, cudaStream_t stream);
 // Warp-specialised variants: VAR_WS_PIPELINED, VAR_PERSISTENT.
 cudaError_t launch_ws(const LaunchSpec& s, cudaStream_t stream);
 
-// Warp-specialised GEMM on CTA pairs: VAR_PERSISTENT_2CTA (static schedule),
-// VAR_DYNAMIC_2CTA (cluster launch control) and VAR_DYNAMIC_2X2 (cluster
-// launch control, two pairs per cluster sharing A), with stages of p.ksub K
+// Warp-specialised GEMM on CTA pairs: VAR_PERSISTENT_2CTA (static schedule)
+// and VAR_DYNAMIC_2CTA (cluster launch control), with stages of p.ksub K
 // blocks of 64.
 cudaError_t launch_pair(const LaunchSpec& s, cudaStream_t stream);
 

@@ -344,23 +344,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// The CTA-pair copy with cluster multicast: the box lands at local offset
-// `dst` in every CTA of `mask`, and the bytes landed in each destination are
-// signalled on the mbarrier at the offset of `cluster_bar` in that
-// destination's pair leader (`cluster_bar` is the executing CTA's pair
-// leader's barrier; every destination here has the executing CTA's rank
-// parity).
-__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const CUtensorMap* map,
-                                                           uint32_t cluster_bar, int32_t x,
-                                                           int32_t y, uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(cluster_bar), "h"(mask)
-        : "memory");
-}
-
 __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* map,
                                                       uint32_t cluster_bar, int32_t x, int32_t y,
                                                       uint64_t policy)

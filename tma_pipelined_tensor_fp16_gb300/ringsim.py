@@ -7,9 +7,7 @@ uses:
 * protocol checking, with faults injected on the host (a wrong byte budget,
   a budget announced several times, a missed phase flip, phases reset per
   persistent tile, an early refill, an epilogue that does not wait, and for
-  the CTA-pair kernel a leader that frees only its own pair's stages or an
-  empty barrier that counts one arrival where two leaders commit, and for the
-  response ring of the dynamic tile schedule a wrong reader count or a
+  the response ring of the dynamic tile schedule a wrong reader count or a
   missing re-arm): the model reports the deadlock or the first read of
   incomplete data;
 * the timing model of "GEMM II -- pipelining with TMA" (the interactive
@@ -18,7 +16,7 @@ uses:
   flight.
 
     python -m tma_pipelined_tensor_fp16_gb300.ringsim [--depth 2] [--k-tiles 8] [--load-mma 1.2]
-    python -m tma_pipelined_tensor_fp16_gb300.ringsim --clc [--pairs 2]
+    python -m tma_pipelined_tensor_fp16_gb300.ringsim --clc
 """
 import argparse
 import ctypes
@@ -46,8 +44,7 @@ class RingsimConfig(ctypes.Structure):
                 ("bytes_delta", ctypes.c_longlong), ("announce_times", ctypes.c_int),
                 ("skip_phase_flip", ctypes.c_int), ("reset_phase_per_tile", ctypes.c_int),
                 ("refill_before_mma", ctypes.c_int), ("epilogue_no_wait", ctypes.c_int),
-                ("pairs", ctypes.c_int), ("commit_own_pair_only", ctypes.c_int),
-                ("empty_count_one", ctypes.c_int), ("clc_slots", ctypes.c_int),
+                ("clc_slots", ctypes.c_int),
                 ("clc_latency", ctypes.c_double), ("clc_readers_delta", ctypes.c_int),
                 ("clc_no_rearm", ctypes.c_int), ("clc_rearm_after_release", ctypes.c_int),
                 ("clc_request_late", ctypes.c_int)]
@@ -103,8 +100,7 @@ DEFAULTS = dict(protocol=WARP_SPEC, depth=4, k_tiles=8, tiles=1, accumulators=2,
                 mma_time=1.0, epilogue_time=0.0, issue_latency=0.0,
                 stage_bytes=(128 * 64 + 128 * 64) * 2, chunks=2, bytes_delta=0,
                 announce_times=1, skip_phase_flip=0, reset_phase_per_tile=0,
-                refill_before_mma=0, epilogue_no_wait=0, pairs=1, commit_own_pair_only=0,
-                empty_count_one=0, clc_slots=4, clc_latency=0.5, clc_readers_delta=0,
+                refill_before_mma=0, epilogue_no_wait=0, clc_slots=4, clc_latency=0.5, clc_readers_delta=0,
                 clc_no_rearm=0, clc_rearm_after_release=0, clc_request_late=0)
 
 
@@ -152,7 +148,7 @@ def gantt(mode="prefetch", depth=2, k_tiles=8, load_mma=1.2):
             "loads_in_flight_max": r["max_loads_in_flight"] // 2}
 
 
-def clc_table(slots=(1, 2, 4), latencies=(0.5, 4.0, 12.0), pairs=1, tiles=17, k_tiles=8,
+def clc_table(slots=(1, 2, 4), latencies=(0.5, 4.0, 12.0), tiles=17, k_tiles=8,
               epilogue_time=6.0):
     """The dynamic schedule's response ring: for each slot count and response
     latency (in MMA times per K block; a tile is k_tiles of them), the
@@ -161,7 +157,7 @@ def clc_table(slots=(1, 2, 4), latencies=(0.5, 4.0, 12.0), pairs=1, tiles=17, k_
     rows = []
     for n in slots:
         for lat in latencies:
-            r = run(protocol=CLC, pairs=pairs, clc_slots=n, clc_latency=lat, tiles=tiles,
+            r = run(protocol=CLC, clc_slots=n, clc_latency=lat, tiles=tiles,
                     k_tiles=k_tiles, depth=4, load_time=1.2, mma_time=1.0,
                     epilogue_time=epilogue_time)
             rows.append({"slots": n, "latency": lat, "status": r["status_name"],
@@ -170,14 +166,14 @@ def clc_table(slots=(1, 2, 4), latencies=(0.5, 4.0, 12.0), pairs=1, tiles=17, k_
     return rows
 
 
-def clc_miscount_onset(slots=(1, 2, 4, 8), pairs=1, limit=400):
+def clc_miscount_onset(slots=(1, 2, 4, 8), limit=400):
     """Tiles per cluster after which a response ring whose empty barriers
     count one reader too few first fails (overwrite or deadlock)."""
     out = []
     for n in slots:
         onset = None
         for tiles in range(1, limit + 1):
-            r = run(protocol=CLC, pairs=pairs, clc_slots=n, tiles=tiles, k_tiles=8, depth=4,
+            r = run(protocol=CLC, clc_slots=n, tiles=tiles, k_tiles=8, depth=4,
                     load_time=1.2, mma_time=1.0, epilogue_time=6.0, clc_readers_delta=-1)
             if r["status_name"] != "ok":
                 onset = (tiles, r["status_name"])
@@ -193,17 +189,16 @@ def main():
     ap.add_argument("--load-mma", type=float, default=1.2)
     ap.add_argument("--clc", action="store_true",
                     help="the dynamic schedule's response ring instead of the pipeline Gantt")
-    ap.add_argument("--pairs", type=int, default=1, choices=[1, 2])
     a = ap.parse_args()
     if a.clc:
-        print("response ring, %d pair(s), 17 tiles of %d K blocks (times in MMA times per K block)"
-              % (a.pairs, a.k_tiles))
-        for row in clc_table(pairs=a.pairs, k_tiles=a.k_tiles):
+        print("response ring, 17 tiles of %d K blocks (times in MMA times per K block)"
+              % a.k_tiles)
+        for row in clc_table(k_tiles=a.k_tiles):
             print("slots %d  latency %5.1f  %-8s makespan %7.1f  request wait %6.1f  "
                   "response wait %6.1f" % (row["slots"], row["latency"], row["status"],
                                             row["makespan"], row["request_wait"],
                                             row["response_wait"]))
-        for row in clc_miscount_onset(pairs=a.pairs):
+        for row in clc_miscount_onset():
             print("one reader too few, %d slot(s): %s" % (
                 row["slots"], "first fails at %d tiles (%s)" % row["onset"] if row["onset"]
                 else "no failure within 400 tiles"))

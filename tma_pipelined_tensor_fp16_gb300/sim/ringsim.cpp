@@ -533,17 +533,17 @@ const char* role_name(int role)
 
 namespace {
 
-// The CTA-pair kernel (RINGSIM_PAIR): `pairs` pairs per cluster, CTAs 2p and
-// 2p + 1 forming pair p with its leader 2p.  Every CTA has a producer and
-// stage slots; each leader has the MMA issuer, full[s] and the accumulators;
-// every CTA has empty[s].  One epilogue role per pair stands for its eight
-// epilogue warps.  Role identities are counted by kind (producer, MMA issuer,
-// epilogue) for the unique-role check, since with two pairs both leaders'
-// commits free a stage by design.
+// The CTA-pair kernel (RINGSIM_PAIR): a cluster of two CTAs, 0 the leader
+// and 1 its peer.  Every CTA has a producer and stage slots; the leader has
+// the MMA issuer, full[s] and the accumulators; every CTA has empty[s].  One
+// epilogue role stands for the pair's eight epilogue warps.  Role identities
+// are counted by kind (producer, MMA issuer, epilogue) for the unique-role
+// check.
 struct PairSim {
     ringsim_config c{};
     ringsim_result* r = nullptr;
-    int NP = 1, C = 2, D = 1, A = 2;
+    static constexpr int NP = 1, C = 2;
+    int D = 1, A = 2;
     double now = 0.0;
     long long seq = 0;
     std::priority_queue<Event, std::vector<Event>, std::greater<Event>> events;
@@ -639,7 +639,7 @@ struct PairSim {
     bool step_producer(RoleState& s, int cta)
     {
         const int K = c.k_tiles;
-        const int pr = cta & 1, pp = cta >> 1;
+        const int pr = cta & 1;
         switch (s.pc) {
         case 0:
             if (s.tile == c.tiles) {
@@ -666,14 +666,7 @@ struct PairSim {
             }
             const long long half = c.stage_bytes / 2;  // A rows, and this CTA's half of B
             copy_into(cta, s.stage, s.tile, s.k, c.stage_bytes - half);  // B
-            if (NP == 1) {
-                copy_into(cta, s.stage, s.tile, s.k, half);  // A
-            } else {
-                // this CTA's 64-row half of A, into both CTAs of its rank
-                const long long quarter = half / 2 + (pp == 1 ? half % 2 : 0);
-                copy_into(pr, s.stage, s.tile, s.k, quarter);
-                copy_into(2 + pr, s.stage, s.tile, s.k, quarter);
-            }
+            copy_into(cta, s.stage, s.tile, s.k, half);                   // A
             if (++s.stage == D) {
                 s.stage = 0;
                 if (!c.skip_phase_flip) s.phase ^= 1u;
@@ -750,12 +743,8 @@ struct PairSim {
             done.tile = s.tile;
             done.acc = pair * A + s.acc;
             push(done);
-            // the commit frees the stage in both CTAs of the pair, and with
-            // two pairs in the other pair's CTAs too (their producers write
-            // their half of A into this pair's slots)
-            const int lo = (NP == 2 && !c.commit_own_pair_only) ? 0 : L;
-            const int hi = (NP == 2 && !c.commit_own_pair_only) ? C : L + 2;
-            for (int d = lo; d < hi; ++d) {
+            // the commit frees the stage in both CTAs of the pair
+            for (int d = L; d < L + 2; ++d) {
                 Event cm{};
                 cm.t = pipe_free[pair];
                 cm.kind = EV_COMMIT;
@@ -836,15 +825,12 @@ struct PairSim {
 
     int run()
     {
-        NP = c.pairs > 0 ? c.pairs : 1;
-        C = 2 * NP;
         D = c.depth;
         A = c.accumulators;
         slots.resize(C * D);
         full.resize(C * D);
         empty.resize(C * D);
-        const int empty_expected = (NP == 2 && !c.empty_count_one) ? 2 : 1;
-        for (Barrier& b : empty) b.expected = b.pending = empty_expected;
+        for (Barrier& b : empty) b.expected = b.pending = 1;
         tmem_full.resize(NP * A);
         tmem_empty.resize(NP * A);
         accs.resize(NP * A);
@@ -963,7 +949,8 @@ namespace {
 struct ClcSim {
     ringsim_config c{};
     ringsim_result* r = nullptr;
-    int NP = 1, C = 2, S = 4, D = 1, A = 2, K = 1;
+    static constexpr int NP = 1, C = 2;
+    int S = 4, D = 1, A = 2, K = 1;
     double T = 0.0;  // MMA time of one tile
     double now = 0.0;
     long long seq = 0;
@@ -1162,7 +1149,7 @@ struct ClcSim {
                 return true;
             }
             // the loads of this tile started in every CTA that feeds the pair
-            const int lo = NP == 2 ? 0 : 2 * p, hi = NP == 2 ? C : 2 * p + 2;
+            const int lo = 2 * p, hi = 2 * p + 2;
             double first = 0.0;
             for (int d = lo; d < hi; ++d) {
                 if (static_cast<int>(prod_start[d].size()) <= s.i) return false;
@@ -1226,8 +1213,6 @@ struct ClcSim {
 
     int run()
     {
-        NP = c.pairs > 0 ? c.pairs : 1;
-        C = 2 * NP;
         S = c.clc_slots > 0 ? c.clc_slots : 4;
         D = c.depth;
         A = c.accumulators;
@@ -1332,12 +1317,10 @@ RINGSIM_API int ringsim_run(const ringsim_config* cfg, ringsim_result* out)
     if (c.tiles < 1 || c.tiles > 100000) return bad("tiles must be 1..100000");
     if (c.protocol != RINGSIM_LOCKSTEP && (c.accumulators < 1 || c.accumulators > 2))
         return bad("accumulators must be 1 or 2");
-    if ((c.protocol == RINGSIM_PAIR || c.protocol == RINGSIM_CLC) && (c.pairs < 0 || c.pairs > 2))
-        return bad("pairs must be 1 or 2");
     if (c.protocol == RINGSIM_CLC) {
         if (c.clc_slots < 0 || c.clc_slots > 16) return bad("clc_slots must be 0 (4) or 1..16");
         if (c.clc_latency < 0) return bad("clc_latency must be non-negative");
-        if (11 * (c.pairs > 0 ? c.pairs : 1) + c.clc_readers_delta < 1)
+        if (11 + c.clc_readers_delta < 1)
             return bad("clc_empty must expect at least one arrival");
     }
     if (c.protocol == RINGSIM_PAIR && c.stage_bytes % 4 != 0)
