@@ -300,10 +300,11 @@ TMAGEMM_API int64_t gemm_sw128_offset(int64_t row, int64_t byte_in_row);
  * cannot pay the device synchronisation that cudaMalloc/cudaFree imply.  The
  * pages have no counterpart of this entry point.
  *
- * Runs the kernel an automatic plan (gemm_create_plan) would run for
- * C = A . B^T, with stream-K off -- the dynamic CTA-pair kernel for large
- * problems, the single-CTA persistent kernel for small or skinny ones -- with
- * the same operands, layouts, preconditions and arithmetic as gemm_run, on
+ * Runs the kernel the automatic plan of gemm_create_plan(M, N, K, dtype_out)
+ * runs for C = A . B^T -- the dynamic CTA-pair kernel for large problems, the
+ * single-CTA persistent kernel for small or skinny ones; automatic plans never
+ * use stream-K, the only option that needs a workspace -- with the same
+ * operands, layouts, preconditions and arithmetic as gemm_run, on
  * `cuda_stream`.  It allocates nothing: its only scratch memory, the kernel's
  * 32-byte watchdog status record, lives in a file-scope device array of 256
  * bytes (the stated maximum; a build whose record outgrew it would be rejected
@@ -311,15 +312,21 @@ TMAGEMM_API int64_t gemm_sw128_offset(int64_t row, int64_t byte_in_row);
  * the process exits.  It calls no cudaMalloc, cudaFree or allocating library
  * routine.
  *
- * The first call on each device looks up that array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture begins.  Every call on a device shares the one
- * array and clears it at the start (an asynchronous memset on `cuda_stream`),
- * so calls that overlap on the GPU race on the status record: serialise them.
+ * Set-up: the first call on each device looks up that array's device address
+ * (cudaGetSymbolAddress, with that device current), and so does the first
+ * call after the current context has changed (a cudaDeviceReset by the
+ * caller, or a context the caller made current): an address looked up in a
+ * destroyed context is never used.  Make such a first call before any stream
+ * capture begins.  Every call on a device shares the one array and clears it
+ * at the start (an asynchronous memset on `cuda_stream`), so calls that
+ * overlap on the GPU race on the status record: serialise them.
  *
- * device_status: NULL makes the call asynchronous (like gemm_run, with no
- * watchdog report).  Non-NULL makes it synchronise `cuda_stream` and store
- * GEMM_OK or GEMM_ERR_TIMEOUT there, which is also returned. */
+ * device_status: non-NULL makes the call synchronise `cuda_stream` and store
+ * GEMM_OK or GEMM_ERR_TIMEOUT there, which is also returned.  NULL makes the
+ * call asynchronous like gemm_run, and then a watchdog timeout is not
+ * reported at all: no call reads the shared record later, and the next call
+ * clears it.  Callers that must know whether C is complete pass
+ * device_status. */
 TMAGEMM_API int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, const void* A,
                                  const void* B, void* C, void* cuda_stream, int* device_status);
 

@@ -17,3 +17,18 @@ def pytest_configure(config):
 def oracle_mod():
     import oracle
     return oracle
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Print the largest error each full-size comparison saw."""
+    try:
+        import gpu_util
+    except ImportError:
+        return
+    if not gpu_util.ERROR_LOG:
+        return
+    tr = terminalreporter
+    tr.section("max |C_gpu - C_oracle| over every entry")
+    for what, n, err, ratio in gpu_util.ERROR_LOG:
+        tr.write_line("%-72s %10d entries  max |err| %.3e  max err/allowed %.3f"
+                      % (what, n, err, ratio))

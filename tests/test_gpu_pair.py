@@ -13,7 +13,7 @@ import pytest
 import oracle
 from tma_pipelined_tensor_fp16_gb300 import inputs
 
-from gpu_util import assert_close, assert_exact, run
+from gpu_util import assert_close, assert_exact, full_reference, record_error, run
 
 pytestmark = pytest.mark.gpu
 V = "persistent_2cta"
@@ -84,24 +84,17 @@ def test_pair_integer_bit_exact(out):
     assert_exact(got, oracle.gemm(A, B), out, desc)
 
 
-def _sample(M, N, count, seed):
-    rng = np.random.default_rng(seed)
-    rows = np.concatenate([rng.integers(0, M, count), [0, M - 1, min(255, M - 1), min(256, M - 1)]])
-    cols = np.concatenate([rng.integers(0, N, count), [N - 1, 0, min(255, N - 1), N - 1]])
-    return rows.astype(np.int64), cols.astype(np.int64)
-
-
 @pytest.mark.parametrize("cfg", inputs.CONFIGS, ids=[c["name"] for c in inputs.CONFIGS])
-def test_pair_workloads_sampled(cfg):
+def test_pair_workloads_every_entry(cfg):
     M, N, K, out = cfg["M"], cfg["N"], cfg["K"], cfg["out"]
-    A, B = inputs.make_operands(M, N, K, cfg["dist"], cfg["seed"])
+    A, B, ref = full_reference(cfg)
     got, _, desc = run(A, B, out, variant=V)
     assert np.isfinite(got.astype(np.float32)).all(), desc
-    rows, cols = _sample(M, N, 3000, cfg["seed"])
-    assert_close(got[rows, cols], oracle.gemm_entries(A, B, rows, cols), K, out, desc)
-    Ai, Bi = inputs.make_operands(M, N, K, "int", 60 + cfg["seed"])
+    record_error("%s (%s)" % (cfg["name"], V), got, ref, K, out)
+    assert_close(got, ref, K, out, desc)
+    Ai, Bi, refi = full_reference(cfg, "int", 60 + cfg["seed"])
     goti, _, _ = run(Ai, Bi, out, variant=V)
-    assert_exact(goti[rows, cols], oracle.gemm_entries(Ai, Bi, rows, cols), out, desc)
+    assert_exact(goti, refi, out, desc)
 
 
 def test_pair_watchdog_timeout():

@@ -1,15 +1,22 @@
 """The allocation-free entry point gemm_run_noalloc, through the C ABI.
 
-It exists for callers that cannot call cudaMalloc (device memory owned by a
-framework allocator or a pre-reserved arena; loops that cannot pay the device
-synchronisation of an allocation).  Its output must match gemm_run's -- the
-existing entry point with a plan -- within the parity tolerance, on two calls
-in a row (the second call reuses the shared static scratch array the first
-one left behind).  The file is named to be collected last.
+It exists for callers that cannot call cudaMalloc: device memory owned by a
+framework's caching allocator or a pre-reserved arena, where a foreign
+allocation fails or is forbidden, and loops that cannot pay the device
+synchronisation an allocation implies.  Its scratch memory is one static
+device array that every call shares.
+
+Each case makes two calls in a row on one stream (the second finds the
+shared array as the first left it) and checks both outputs against the
+existing entry point (gemm_run with a plan) and against the CPU oracle,
+within the parity tolerance; the two entry points run the same kernel with
+the same plan, so their outputs are also compared bit for bit.  The file is
+named to be collected last.
 """
 import numpy as np
 import pytest
 
+import oracle
 from tma_pipelined_tensor_fp16_gb300 import inputs
 
 from gpu_util import assert_close
@@ -26,58 +33,76 @@ def _built():
     __graft_entry__.build()
 
 
-def _with_plan(A, B, out):
+def _dtype(out):
+    import torch
+    return torch.float16 if out == "f16" else torch.float32
+
+
+def _with_plan(dA, dB, M, N, K, out):
     import torch
 
     import tma_pipelined_tensor_fp16_gb300 as pkg
-    M, K = A.shape
-    N = B.shape[0]
-    dA = torch.from_numpy(A.view(np.float16)).cuda()
-    dB = torch.from_numpy(B.view(np.float16)).cuda()
-    C = torch.empty((M, N), dtype=torch.float16 if out == "f16" else torch.float32, device="cuda")
+    C = torch.full((M, N), float("nan"), dtype=_dtype(out), device="cuda")
     plan = pkg.Plan(M, N, K, out=out)
-    plan(dA, dB, C)
-    torch.cuda.synchronize()
-    assert plan.device_status() == 0
-    plan.close()
-    return C.cpu().numpy().astype(np.float64)
+    try:
+        plan(dA, dB, C)
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        desc = plan.describe()
+    finally:
+        plan.close()
+    return C.cpu().numpy(), desc
 
 
-def _no_alloc(A, B, out, synchronous):
+def _no_alloc_twice(dA, dB, M, N, K, out, synchronous):
+    """Two gemm_run_noalloc calls in a row on one stream, each into its own
+    NaN-filled C; returns both outputs."""
     import torch
 
     from tma_pipelined_tensor_fp16_gb300 import binding
-    M, K = A.shape
-    N = B.shape[0]
+    dt = binding.GEMM_OUT_F16 if out == "f16" else binding.GEMM_OUT_F32
+    s = torch.cuda.Stream()
+    outs = []
+    Cs = [torch.full((M, N), float("nan"), dtype=_dtype(out), device="cuda") for _ in range(2)]
+    torch.cuda.synchronize()
+    for C in Cs:
+        st, ds = binding.gemm_run_noalloc(M, N, K, dt, dA.data_ptr(), dB.data_ptr(),
+                                          C.data_ptr(), s.cuda_stream, want_status=synchronous)
+        assert st == binding.GEMM_OK, binding.last_error()
+        if synchronous:
+            assert ds == binding.GEMM_OK
+    s.synchronize()
+    for C in Cs:
+        outs.append(C.cpu().numpy())
+    return outs
+
+
+# (shape, output, operands, seed, synchronous): the single-CTA persistent
+# kernel (small shapes, and 64-wide tiles over a long K), and the dynamic
+# CTA-pair kernel with stages of K = 64 and of K = 128.
+CASES = [((300, 264, 328), "f32", "uniform", 21, False),
+         ((520, 392, 1000), "f16", "normal", 22, True),
+         ((2560, 1024, 1000), "f16", "normal", 23, True),
+         ((2560, 1040, 512), "f32", "uniform", 24, False),
+         ((1024, 1024, 4096), "f16", "uniform", 25, False)]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "%dx%dx%d_%s" % (c[0] + (c[1],)))
+def test_no_alloc_matches_gemm_run_and_oracle_on_two_calls_in_a_row(case):
+    import torch
+    (M, N, K), out, dist, seed, sync = case
+    A, B = inputs.make_operands(M, N, K, dist, seed)
     dA = torch.from_numpy(A.view(np.float16)).cuda()
     dB = torch.from_numpy(B.view(np.float16)).cuda()
-    C = torch.full((M, N), float("nan"),
-                   dtype=torch.float16 if out == "f16" else torch.float32, device="cuda")
-    torch.cuda.synchronize()
-    dt = binding.GEMM_OUT_F16 if out == "f16" else binding.GEMM_OUT_F32
-    s = torch.cuda.current_stream()
-    st, ds = binding.gemm_run_noalloc(M, N, K, dt, dA.data_ptr(), dB.data_ptr(), C.data_ptr(),
-                                      s.cuda_stream, want_status=synchronous)
-    assert st == binding.GEMM_OK, binding.last_error()
-    if synchronous:
-        assert ds == binding.GEMM_OK
-    torch.cuda.synchronize()
-    return C.cpu().numpy().astype(np.float64)
-
-
-def test_no_alloc_matches_gemm_run_on_two_calls_in_a_row():
-    # small shapes take the single-CTA kernel; the last two have enough pair
-    # tiles for the dynamic CTA-pair kernel (stages of K = 64 and of K = 128)
-    cases = [((300, 264, 328), "f32", "uniform", 21, False),
-             ((520, 392, 1000), "f16", "normal", 22, True),
-             ((2560, 1024, 1000), "f16", "normal", 23, True),
-             ((2560, 1040, 512), "f32", "uniform", 24, False)]
-    for (M, N, K), out, dist, seed, sync in cases:
-        A, B = inputs.make_operands(M, N, K, dist, seed)
-        want = _with_plan(A, B, out)
-        got = _no_alloc(A, B, out, sync)
-        assert np.isfinite(got).all()
-        assert_close(got, want, K, out, "gemm_run_noalloc vs gemm_run %dx%dx%d %s" % (M, N, K, out))
+    want, desc = _with_plan(dA, dB, M, N, K, out)
+    ref = oracle.gemm(A, B)
+    assert_close(want, ref, K, out, "gemm_run %s" % desc)
+    for i, got in enumerate(_no_alloc_twice(dA, dB, M, N, K, out, sync)):
+        what = "gemm_run_noalloc call %d, %dx%dx%d %s (%s)" % (i + 1, M, N, K, out, desc)
+        assert np.isfinite(got.astype(np.float32)).all(), what
+        assert_close(got, want.astype(np.float64), K, out, what + " vs gemm_run")
+        assert_close(got, ref, K, out, what + " vs the oracle")
+        assert np.array_equal(got.view(np.uint8), want.view(np.uint8)), what + " not bitwise"
 
 
 def test_no_alloc_rejects_bad_arguments():

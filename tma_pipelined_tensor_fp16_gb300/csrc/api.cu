@@ -1053,10 +1053,10 @@ int64_t gemm_sw128_offset(int64_t row, int64_t byte_in_row)
 // policy), and latency-critical serving loops that cannot afford the device
 // synchronisation cudaMalloc/cudaFree imply.  gemm_create_plan allocates the
 // plan's device status record, so those callers use gemm_run_noalloc instead.
-// It runs the kernel an automatic plan would, without stream-K (the only
-// option that needs a workspace); the kernel's only scratch memory, the status
-// record, lives in the file-scope array below, which every GPU that loads this
-// library holds until the process exits.
+// It runs the kernel an automatic plan would (automatic plans never use
+// stream-K, the only option that needs a workspace); the kernel's only
+// scratch memory, the status record, lives in the file-scope array below,
+// which every GPU that loads this library holds until the process exits.
 
 namespace {
 
@@ -1066,7 +1066,36 @@ static_assert(sizeof(DevStatus) <= NOALLOC_SCRATCH_BYTES, "status record must fi
 constexpr int NOALLOC_MAX_DEVICES = 64;
 std::mutex g_noalloc_mutex;
 void* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
+unsigned long long g_noalloc_ctx[NOALLOC_MAX_DEVICES] = {};  // context the address belongs to
 int g_noalloc_epoch[NOALLOC_MAX_DEVICES] = {};
+
+// Unique id of the calling thread's current CUDA context, or 0 when there is
+// none or the driver cannot say.  A context created after cudaDeviceReset
+// gets a new id, so an address looked up in the old one is never reused.
+unsigned long long current_context_id()
+{
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+    });
+    CUcontext ctx = nullptr;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    unsigned long long id = 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 }  // namespace
 
@@ -1078,18 +1107,23 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH
 namespace {
 
 // Device address of g_noalloc_scratch on device `dev` (which is current),
-// looked up once per device with cudaGetSymbolAddress.
+// looked up with cudaGetSymbolAddress once per device and again whenever the
+// current context is not the one the cached address was looked up in (a
+// cudaDeviceReset by the caller, or a context of the caller's own).
 int noalloc_scratch_ptr(int dev, void** out)
 {
     if (dev < 0 || dev >= NOALLOC_MAX_DEVICES)
         return fail(GEMM_ERR_UNSUPPORTED, "device index too large for gemm_run_noalloc");
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
+    const unsigned long long ctx = current_context_id();
+    if (!g_noalloc_ptr[dev] || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
         void* p = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p)
             return cuda_fail("cudaGetSymbolAddress(g_noalloc_scratch)", e);
         g_noalloc_ptr[dev] = p;
+        // the lookup has made the device's context current if none was
+        g_noalloc_ctx[dev] = current_context_id();
     }
     *out = g_noalloc_ptr[dev];
     return GEMM_OK;
@@ -1126,24 +1160,26 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     if (major != 10 || minor != 3)
         return fail(GEMM_ERR_NO_DEVICE, "this library is built for sm_103a (GB300) only");
 
-    gemm_options opts;
-    std::memset(&opts, 0, sizeof(opts));
-    opts.variant = VAR_AUTO;
-    opts.stream_k = 1;  // no workspace: every tile whole
     gemm_config c;
-    int r = select_config_impl(M, N, K, dtype_out, &opts, sms, smem_optin, &c);
+    int r = select_config_impl(M, N, K, dtype_out, nullptr, sms, smem_optin, &c);
     if (r != GEMM_OK) return r;
+    // automatic plans never split K: no workspace
+    if (c.sk_tiles != 0 || c.workspace_bytes != 0)
+        return fail(GEMM_ERR_UNSUPPORTED, "gemm_run_noalloc: the automatic plan needs a workspace");
 
     void* scratch = nullptr;
     r = noalloc_scratch_ptr(dev, &scratch);
     if (r != GEMM_OK) return r;
 
-    CUtensorMap tmA, tmB, tmC;
+    CUtensorMap tmA, tmB, tmC, tmB2;
     r = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, K * 2, BLK_K,
                   static_cast<uint32_t>(c.a_rows), "A");
     if (r == GEMM_OK)
         r = encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, K * 2, BLK_K,
                       static_cast<uint32_t>(is_pair(c.variant) ? c.block_n / 2 : c.block_n), "B");
+    if (r == GEMM_OK && c.tail_halves > 0)
+        r = encode_2d(&tmB2, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, K * 2, BLK_K,
+                      static_cast<uint32_t>(c.block_n / 4), "B (narrow)");
     if (r == GEMM_OK) {
         if (dtype_out == GEMM_OUT_F16)
             r = encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, N, M, N * 2, 64, 32, "C");
@@ -1167,6 +1203,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     s.tmA = &tmA;
     s.tmB = &tmB;
     s.tmC = &tmC;
+    s.tmB2 = c.tail_halves > 0 ? &tmB2 : nullptr;
     Params& p = s.p;
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
@@ -1188,7 +1225,8 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int dtype_out, 
     }
     p.budget_ns = 2000ull * 1000000ull;
     p.debug_stall = 0;
-    p.dp_tiles = c.num_tiles;
+    p.dp_tiles = c.dp_tiles;
+    p.tail_halves = c.tail_halves;
     p.sk_tiles = 0;
     p.sk_kb_per_worker = 0;
     p.sk_max_contrib = 0;
