@@ -172,7 +172,41 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm),
                 "sm_max_mhz": float(inside[0][2]),
                 "power_w_max": max(power) if power else None,
+                "power_w_median": statistics.median(power) if power else None,
                 "samples": len(inside), "window": window, "reasons": sorted(reasons)}
+
+
+NOMINAL_F16_TFLOPS = 2250.0  # GB300 dense fp16/bf16 tensor rate, nominal
+
+
+def clock_pass_record(clocks, launches, total_ms, flops, ms_per_step, peaks, memory_bound,
+                      nbytes):
+    """The informational clock pass: the bench's plan launched back to back
+    for about a second outside the timed region, with nvidia-smi sampling
+    every 20 ms.  Its throughput against the sustained peak, the SM clock and
+    power the samples saw while it ran, and the headline's step time
+    expressed in SM cycles at that clock."""
+    rec = {"launches": launches, "seconds": total_ms * 1e-3,
+           "ms_per_launch": total_ms / launches,
+           "sm_mhz_median": clocks.get("sm_mhz"), "sm_mhz_min": clocks.get("sm_min_mhz"),
+           "sm_max_mhz": clocks.get("sm_max_mhz"), "power_w_median": clocks.get("power_w_median"),
+           "power_w_max": clocks.get("power_w_max"), "samples": clocks.get("samples", 0),
+           "reasons": clocks.get("reasons", [])}
+    if memory_bound:
+        rec["value"] = nbytes * launches / (total_ms * 1e-3) / 1e9
+        rec["unit"] = "GB/s"
+        rec["frac_of_hbm_gbs"] = rec["value"] / float(peaks["hbm_gbs"])
+    else:
+        rec["value"] = flops * launches / (total_ms * 1e-3) / 1e12
+        rec["unit"] = "TFLOP/s"
+        sus = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+        rec["frac_of_sustained_peak"] = rec["value"] / sus
+        rec["frac_of_nominal"] = rec["value"] / NOMINAL_F16_TFLOPS
+    mhz = clocks.get("sm_mhz")
+    if mhz:
+        rec["cycles_per_launch"] = rec["ms_per_launch"] * 1e-3 * mhz * 1e6
+        rec["headline_cycles_per_step"] = ms_per_step * 1e-3 * mhz * 1e6
+    return rec
 
 
 # --------------------------------------------------------------- oracle timing
@@ -292,6 +326,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--clock-pass-seconds", type=float, default=1.5,
+                    help="length of the informational clock pass after the timed region "
+                         "(0 = none)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -420,6 +457,32 @@ def main():
     value = whole_job_rate(world, flops, args.steps, total_ms)
     avg_launch_s = statistics.mean(launch_ms) * 1e-3
 
+    # ------------------------------------------ clock pass (informational)
+    # Outside the timed region: the same plan back to back for about a
+    # second, long enough for nvidia-smi's 20 ms samples to show the SM clock
+    # and power under this load (the timed region itself is shorter than a
+    # few sampling periods at 8192^3).
+    clock_pass = None
+    if args.clock_pass_seconds > 0 and graph is None:
+        n_pass = max(8, int(args.clock_pass_seconds * 1e3 / max(ms_per_step, 1e-3)))
+        cs = ClockSampler(local_rank)
+        cs.start()
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        cs.mark_start()
+        with torch.cuda.stream(stream):
+            p0.record(stream)
+            for _ in range(n_pass):
+                plan.run(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), sh)
+            p1.record(stream)
+        torch.cuda.synchronize()
+        cs.mark_end()
+        pass_clocks = cs.stop()
+        if plan.device_status() != 0:
+            raise SystemExit("clock pass failed: " + pkg.gemm_last_error())
+        clock_pass = (pass_clocks, n_pass, p0.elapsed_time(p1))
+
     # --------------------------------------------------- end to end, host buffers
     e2e = None
     if not args.no_e2e:
@@ -487,6 +550,11 @@ def main():
                 "frac_of_burst_peak": achieved / float(peaks["bf16_tflops"])}
     roof["algorithmic_per_launch"] = flops if not memory_bound else nbytes
     roof["avg_launch_ms"] = avg_launch_s * 1e3
+    if not memory_bound:
+        roof["frac_of_nominal"] = achieved / NOMINAL_F16_TFLOPS
+    if clock_pass is not None:
+        clock_pass = clock_pass_record(clock_pass[0], clock_pass[1], clock_pass[2], flops,
+                                       ms_per_step, peaks, memory_bound, nbytes)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -515,6 +583,7 @@ def main():
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks,
+        "clock_pass": clock_pass,
     }
     if single_ms:
         line["single_launch_median"] = {

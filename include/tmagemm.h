@@ -177,11 +177,19 @@ typedef struct {
  * state, a 32-byte device status record and, when its configuration uses
  * stream-K, a device workspace of gemm_config.workspace_bytes; because of
  * that workspace, runs of one plan must not overlap on the GPU (use one plan
- * per concurrent stream). */
+ * per concurrent stream).
+ * Passage: "GEMM II -- pipelining with TMA", Steps 5 and 6 -- what is fixed
+ * before the launch (PIPE_DEPTH stages sized against shared memory, the tile
+ * shape, a grid of one CTA per SM) -- and "B200 Tma Pipeline Designer",
+ * Execution, steps 2 (the tensor-map descriptor of each operand) and 6 (the
+ * stage ring and its shared-memory total against residency). */
 TMAGEMM_API gemm_plan* gemm_create_plan(int64_t M, int64_t N, int64_t K, int dtype_out);
 
 /* Same with options (NULL = all automatic).  An explicit pipe_depth whose ring
- * does not fit in shared memory fails with GEMM_ERR_UNSUPPORTED. */
+ * does not fit in shared memory fails with GEMM_ERR_UNSUPPORTED.
+ * Passage: "GEMM II -- pipelining with TMA", Steps 3-6 (the variants of the
+ * ablation ladder) and Step 5 (PIPE_DEPTH); tilus matmul-hopper v2,
+ * Multi-Stage Software Pipelining (deeper rings force smaller tiles). */
 TMAGEMM_API gemm_plan* gemm_create_plan_ex(int64_t M, int64_t N, int64_t K, int dtype_out,
                                const gemm_options* opts);
 
@@ -211,7 +219,12 @@ TMAGEMM_API gemm_plan* gemm_create_plan_ex(int64_t M, int64_t N, int64_t K, int 
  * have fix-up tickets keyed by the run counter, which a replay would repeat
  * and so leave shared tiles unwritten: the static schedule refuses capture
  * with GEMM_ERR_UNSUPPORTED, and a captured launch of the dynamic schedule
- * runs every tile whole. */
+ * runs every tile whole.
+ * Passage: "GEMM II -- pipelining with TMA", Steps 4-6 (one elected thread
+ * issues the bulk-tensor loads and announces their bytes; the staged
+ * mainloop; the TMA-store epilogue), on tensor maps encoded for the pointer
+ * triple ("05 Async Data Movement - TMA", How One Thread Describes an Entire
+ * Tile). */
 TMAGEMM_API int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_stream);
 
 /* End-to-end variant of gemm_run for HOST buffers: copies A and B to device
@@ -223,28 +236,39 @@ TMAGEMM_API int gemm_run(gemm_plan* plan, const void* A, const void* B, void* C,
  * as soon as its rows of A have landed, and each band of C comes back on a
  * second copy stream while later bands compute; otherwise the copies and the
  * GEMM run one after the other on `cuda_stream`.  Returns GEMM_ERR_TIMEOUT if
- * a kernel's watchdog fired. */
+ * a kernel's watchdog fired.
+ * Passage: none -- the pages define no interface, so this call belongs to the library's own boundary; the GEMM it runs is gemm_run's. */
 TMAGEMM_API int gemm_run_host(gemm_plan* plan, const void* A, const void* B, void* C, void* cuda_stream);
 
 /* Read (and clear) the plan's device status record.  Call after
  * synchronising the stream(s) the plan ran on.  Returns GEMM_OK or
  * GEMM_ERR_TIMEOUT (a wait ran past wait_budget_ms; the kernel then skipped
  * its remaining work, freed TMEM and exited, so C is incomplete), or
- * GEMM_ERR_CUDA if the read itself failed. */
+ * GEMM_ERR_CUDA if the read itself failed.
+ * Passage: none -- the pages define no interface, so this call belongs to the library's own boundary.  The pages' barrier waits are unbounded ("05 Async
+ * Data Movement - TMA", How to Wait for a TMA Load); the bound on each wait
+ * and this record of where one ran out are the library's own. */
 TMAGEMM_API int gemm_get_device_status(gemm_plan* plan);
 
-/* Free the plan (NULL is allowed). */
+/* Free the plan and the device memory it owns (NULL is allowed).  The caller
+ * must have synchronised every stream the plan ran on.
+ * Passage: none -- the pages define no interface, so this call belongs to the library's own boundary. */
 TMAGEMM_API void gemm_destroy(gemm_plan* plan);
 
-/* Message / code of the last failing call on this host thread. */
+/* Message / code of the last failing call on this host thread (thread-local;
+ * the message is empty after a call that succeeded).
+ * Passage: none -- the pages define no interface, so this call belongs to the library's own boundary. */
 TMAGEMM_API const char* gemm_last_error(void);
 TMAGEMM_API int gemm_last_status(void);
 
 /* Human-readable one-line description of the plan (variant, tile, depth,
- * shared memory, grid).  The string is owned by the plan. */
+ * shared memory, grid).  The string is owned by the plan.
+ * Passage: none -- the pages define no interface, so this call belongs to the library's own boundary; the values it reports are the choices of "GEMM II
+ * -- pipelining with TMA", Steps 5 and 6 (PIPE_DEPTH, tile, grid). */
 TMAGEMM_API const char* gemm_plan_describe(const gemm_plan* plan);
 
-/* The plan's resolved configuration. */
+/* The plan's resolved configuration.
+ * Passage: none -- the pages define no interface, so this call belongs to the library's own boundary; see gemm_config for the pages' quantities it holds. */
 TMAGEMM_API int gemm_plan_config(const gemm_plan* plan, gemm_config* out);
 
 /* Record a device timeline of the following runs of `plan` into
@@ -266,7 +290,10 @@ TMAGEMM_API int gemm_set_trace(gemm_plan* plan, void* device_buffer, int units_p
 
 /* Resolve options into a configuration for a device with `sm_count` SMs and
  * `smem_optin` bytes of opt-in shared memory per block, exactly as
- * gemm_create_plan_ex does.  Returns a gemm_status. */
+ * gemm_create_plan_ex does.  Returns a gemm_status.
+ * Passage: as gemm_create_plan_ex; the stage-count limit is "B200 Tma
+ * Pipeline Designer", Execution, step 6 (total shared memory of the ring
+ * against residency). */
 TMAGEMM_API int gemm_select_config(int64_t M, int64_t N, int64_t K, int dtype_out, const gemm_options* opts,
                        int sm_count, int smem_optin, gemm_config* out);
 
@@ -283,7 +310,10 @@ TMAGEMM_API int gemm_schedule_tile(const gemm_config* cfg, int64_t tile, int* m_
  * kernel runs.  Writes
  * the tile (raster index), its K-block range [kb0, kb1) and the worker's rank
  * among the tile's contributors; returns 1, or 0 when the worker has no unit
- * `index`, or GEMM_ERR_INVALID_ARG. */
+ * `index`, or GEMM_ERR_INVALID_ARG.
+ * Passage: "GEMM II -- pipelining with TMA", Step 6 (each persistent CTA
+ * walks its own sequence of tiles); the split of K among workers (stream-K)
+ * has no passage. */
 TMAGEMM_API int gemm_schedule_unit(const gemm_config* cfg, int worker, int index, int* tile,
                                    int* kb0, int* kb1, int* contrib, int* ncontrib);
 

@@ -49,3 +49,25 @@ def test_no_sample_near_the_region():
     t = 1_800_000_000.0
     c = _sampler([_row(t - 5.0, 2070)], t, t + 0.002).stop()
     assert c["samples"] == 0 and c["sm_mhz"] is None
+
+
+def test_clock_pass_record():
+    # 2000 launches of 0.6 ms (1.2 s) of the 8192^3 GEMM at a median 1900 MHz
+    flops = 2.0 * 8192 ** 3
+    clocks = {"sm_mhz": 1900.0, "sm_min_mhz": 1800.0, "sm_max_mhz": 2070.0,
+              "power_w_median": 1200.0, "power_w_max": 1390.0, "samples": 60,
+              "reasons": ["sw_power_cap"]}
+    peaks = {"hbm_gbs": 6663.6, "bf16_tflops": 1941.1, "bf16_tflops_sustained": 1728.9}
+    r = bench.clock_pass_record(clocks, 2000, 1200.0, flops, 0.59, peaks, False, 0.0)
+    want = flops / 0.6e-3 / 1e12
+    assert abs(r["value"] - want) < 1e-6 and r["unit"] == "TFLOP/s"
+    assert abs(r["frac_of_sustained_peak"] - want / 1728.9) < 1e-12
+    assert abs(r["frac_of_nominal"] - want / 2250.0) < 1e-12
+    assert abs(r["cycles_per_launch"] - 0.6e-3 * 1.9e9) < 1e-3
+    assert abs(r["headline_cycles_per_step"] - 0.59e-3 * 1.9e9) < 1e-3
+    assert r["samples"] == 60 and r["reasons"] == ["sw_power_cap"]
+    # the skinny shape is judged against copy bandwidth
+    nbytes = 541.1e6
+    m = bench.clock_pass_record(clocks, 100, 10.0, 1.0, 0.1, peaks, True, nbytes)
+    assert m["unit"] == "GB/s" and abs(m["value"] - nbytes * 100 / 0.01 / 1e9) < 1e-6
+    assert "frac_of_nominal" not in m and abs(m["frac_of_hbm_gbs"] - m["value"] / 6663.6) < 1e-12

@@ -142,8 +142,7 @@ def test_same_plan_launched_repeatedly(opts):
     variant = opts["variant"]
     ref = outs[0]
     assert not np.isnan(ref.astype(np.float32)).any()
-    rows, cols = _sample(M, N, 2000, 66)
-    assert_close(ref[rows, cols], oracle.gemm_entries(A, B, rows, cols), K, "f16", variant)
+    assert_close(ref, oracle.gemm(A, B), K, "f16", variant)
     for i, o in enumerate(outs[1:], 1):
         assert np.array_equal(o.view(np.uint16), ref.view(np.uint16)), "launch %d differs" % i
 
@@ -159,5 +158,4 @@ def test_dynamic_many_tiles_per_cluster(bk):
     assert not np.isnan(got.astype(np.float32)).any(), desc
     ref, _, _ = run(A, B, "f16", variant="persistent_2cta", block_k=bk)
     assert np.array_equal(got.view(np.uint16), ref.view(np.uint16)), desc
-    rows, cols = _sample(M, N, 4000, 78)
-    assert_close(got[rows, cols], oracle.gemm_entries(A, B, rows, cols), K, "f16", desc)
+    assert_close(got, oracle.gemm(A, B), K, "f16", desc)

@@ -140,11 +140,11 @@ def test_pair_block_k_128(variant, out, K):
                          ids=[c["name"] for c in inputs.CONFIGS if c["M"] > 128])
 def test_pair_block_k_128_workloads(cfg):
     M, N, K, out = cfg["M"], cfg["N"], cfg["K"], cfg["out"]
-    A, B = inputs.make_operands(M, N, K, cfg["dist"], cfg["seed"])
+    A, B, ref = full_reference(cfg)
     # whole tiles on the dynamic schedule (no split tail): the same sums in the
     # same order as the static schedule, bit for bit
     got, _, desc = run(A, B, out, variant="dynamic_2cta", block_k=128, stream_k="off")
     stat, _, _ = run(A, B, out, variant="persistent_2cta", block_k=128)
     assert np.array_equal(got.view(np.uint8), stat.view(np.uint8)), desc
-    rows, cols = _sample(M, N, 2000, cfg["seed"] + 7)
-    assert_close(got[rows, cols], oracle.gemm_entries(A, B, rows, cols), K, out, desc)
+    record_error("%s (dynamic_2cta, block_k 128)" % cfg["name"], got, ref, K, out)
+    assert_close(got, ref, K, out, desc)
