@@ -177,15 +177,19 @@ class ClockSampler:
 
 
 NOMINAL_F16_TFLOPS = 2250.0  # GB300 dense fp16/bf16 tensor rate, nominal
+# Dense fp16 MMA rate of one SM per clock: 4096 multiply-adds.  At 152 SMs and
+# about 1.8 GHz this is the nominal 2.25 PFLOP/s; an ncu capture of the 8192^3
+# kernel (FLOP / duration / SMs / clock / tensor-pipe busy fraction) gives
+# 7,940 FLOP per busy SM cycle at the capture's clock.
+PIPE_FLOP_PER_SM_CYCLE = 8192
 
 
-def clock_pass_record(clocks, launches, total_ms, flops, ms_per_step, peaks, memory_bound,
-                      nbytes):
+def clock_pass_record(clocks, launches, total_ms, flops, peaks, memory_bound, nbytes, sms):
     """The informational clock pass: the bench's plan launched back to back
     for about a second outside the timed region, with nvidia-smi sampling
-    every 20 ms.  Its throughput against the sustained peak, the SM clock and
-    power the samples saw while it ran, and the headline's step time
-    expressed in SM cycles at that clock."""
+    every 20 ms.  Its throughput against the sustained peak and against the
+    tensor pipe's peak at the SM clock the samples saw, that clock, the power,
+    and the launch time in SM cycles at that clock."""
     rec = {"launches": launches, "seconds": total_ms * 1e-3,
            "ms_per_launch": total_ms / launches,
            "sm_mhz_median": clocks.get("sm_mhz"), "sm_mhz_min": clocks.get("sm_min_mhz"),
@@ -205,7 +209,10 @@ def clock_pass_record(clocks, launches, total_ms, flops, ms_per_step, peaks, mem
     mhz = clocks.get("sm_mhz")
     if mhz:
         rec["cycles_per_launch"] = rec["ms_per_launch"] * 1e-3 * mhz * 1e6
-        rec["headline_cycles_per_step"] = ms_per_step * 1e-3 * mhz * 1e6
+        if not memory_bound:
+            pipe = sms * PIPE_FLOP_PER_SM_CYCLE * mhz * 1e6 / 1e12
+            rec["pipe_peak_at_clock_tflops"] = pipe
+            rec["frac_of_pipe_peak_at_clock"] = rec["value"] / pipe
     return rec
 
 
@@ -553,8 +560,12 @@ def main():
     if not memory_bound:
         roof["frac_of_nominal"] = achieved / NOMINAL_F16_TFLOPS
     if clock_pass is not None:
-        clock_pass = clock_pass_record(clock_pass[0], clock_pass[1], clock_pass[2], flops,
-                                       ms_per_step, peaks, memory_bound, nbytes)
+        sms = torch.cuda.get_device_properties(local_rank).multi_processor_count
+        clock_pass = clock_pass_record(clock_pass[0], clock_pass[1], clock_pass[2], flops, peaks,
+                                       memory_bound, nbytes, sms)
+    if clocks.get("sm_mhz"):
+        # SM cycles of one step at the clock sampled around the timed region
+        roof["cycles_per_step_at_sampled_clock"] = ms_per_step * 1e-3 * clocks["sm_mhz"] * 1e6
 
     cpu = None
     if not args.no_cpu_baseline:

@@ -58,16 +58,19 @@ def test_clock_pass_record():
               "power_w_median": 1200.0, "power_w_max": 1390.0, "samples": 60,
               "reasons": ["sw_power_cap"]}
     peaks = {"hbm_gbs": 6663.6, "bf16_tflops": 1941.1, "bf16_tflops_sustained": 1728.9}
-    r = bench.clock_pass_record(clocks, 2000, 1200.0, flops, 0.59, peaks, False, 0.0)
+    r = bench.clock_pass_record(clocks, 2000, 1200.0, flops, peaks, False, 0.0, 152)
     want = flops / 0.6e-3 / 1e12
     assert abs(r["value"] - want) < 1e-6 and r["unit"] == "TFLOP/s"
     assert abs(r["frac_of_sustained_peak"] - want / 1728.9) < 1e-12
     assert abs(r["frac_of_nominal"] - want / 2250.0) < 1e-12
     assert abs(r["cycles_per_launch"] - 0.6e-3 * 1.9e9) < 1e-3
-    assert abs(r["headline_cycles_per_step"] - 0.59e-3 * 1.9e9) < 1e-3
+    pipe = 152 * 8192 * 1.9e9 / 1e12
+    assert abs(r["pipe_peak_at_clock_tflops"] - pipe) < 1e-9
+    assert abs(r["frac_of_pipe_peak_at_clock"] - want / pipe) < 1e-12
     assert r["samples"] == 60 and r["reasons"] == ["sw_power_cap"]
     # the skinny shape is judged against copy bandwidth
     nbytes = 541.1e6
-    m = bench.clock_pass_record(clocks, 100, 10.0, 1.0, 0.1, peaks, True, nbytes)
+    m = bench.clock_pass_record(clocks, 100, 10.0, 1.0, peaks, True, nbytes, 152)
     assert m["unit"] == "GB/s" and abs(m["value"] - nbytes * 100 / 0.01 / 1e9) < 1e-6
     assert "frac_of_nominal" not in m and abs(m["frac_of_hbm_gbs"] - m["value"] / 6663.6) < 1e-12
+    assert "frac_of_pipe_peak_at_clock" not in m

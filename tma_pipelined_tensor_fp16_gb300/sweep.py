@@ -2,7 +2,7 @@
 
     python -m tma_pipelined_tensor_fp16_gb300.sweep --config gemm_8192 \
         [--variants persistent,ws_pipelined] [--depths 2,3,4] [--block-n 64,128,256] \
-        [--iters 20] [--rounds 1] [--out results.jsonl]
+        [--iters 20] [--rounds 1] [--out results.jsonl] [--shape M,N,K]
 
 Prints one JSON line per configuration: the plan, the shared memory it needs
 (or why it does not fit), and the median / mean TFLOP/s and GB/s of its
@@ -41,6 +41,8 @@ def main(argv=None):
     ap.add_argument("--rounds", type=int, default=1,
                     help="interleaved rounds over all configurations")
     ap.add_argument("--out", default="")
+    ap.add_argument("--shape", default="",
+                    help="M,N,K overriding the workload's shape (same operand recipe and output)")
     a = ap.parse_args(argv)
 
     import numpy as np
@@ -48,7 +50,10 @@ def main(argv=None):
 
     from . import binding, build, inputs
     build.build()
-    cfg = next(c for c in inputs.CONFIGS if a.config in c["name"])
+    cfg = dict(next(c for c in inputs.CONFIGS if a.config in c["name"]))
+    if a.shape:
+        cfg["M"], cfg["N"], cfg["K"] = (int(x) for x in a.shape.split(","))
+        cfg["name"] = "%s@%dx%dx%d" % (cfg["name"], cfg["M"], cfg["N"], cfg["K"])
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
     A, B = inputs.make_operands(M, N, K, cfg["dist"], cfg["seed"])
     dA = torch.from_numpy(A.view(np.float16)).cuda()
