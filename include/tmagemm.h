@@ -126,16 +126,20 @@ typedef struct {
                            the same raster group) used last and that are still
                            in L2 */
     int block_k;        /* K extent of one pipeline stage: 64 = one 128-byte
-                           swizzle atom (64 fp16); 128 = two atoms per stage
-                           ("05 Async Data Movement - TMA", Using 3D TMA to Move
-                           Multiple Swizzle Atoms), loaded as two boxes and
-                           consumed by 8 MMAs behind one barrier round trip
-                           (CTA-pair variants only; pipe_depth then counts
-                           128-wide stages, and stream-K splits K in such
-                           stages).  A second block past K arrives zero-filled
-                           and is skipped.  0 = auto: 128 for the CTA-pair
-                           variants when K is a multiple of 64 (128-byte aligned
-                           operand rows) and pipe_depth is not set, else 64 */
+                           swizzle atom (64 fp16); 128 or 256 = two or four
+                           atoms per stage ("05 Async Data Movement - TMA",
+                           Using 3D TMA to Move Multiple Swizzle Atoms), loaded
+                           as that many boxes per operand and consumed by 8 or
+                           16 MMAs behind one barrier round trip.  128: the
+                           warp-specialised variants (CTA pairs and single
+                           CTAs); 256: the single-CTA warp-specialised variants
+                           (persistent, ws_pipelined).  pipe_depth then counts
+                           stages of this extent, and stream-K splits K in such
+                           stages.  A block of the last stage past K arrives
+                           zero-filled and is skipped.  0 = auto: 128 for the
+                           CTA-pair variants when K is a multiple of 64
+                           (128-byte aligned operand rows) and pipe_depth is
+                           not set, else 64 */
 } gemm_options;
 
 /* Resolved configuration of a plan (also returned by gemm_select_config). */

@@ -234,9 +234,12 @@ def test_block_k_128_stages(b):
     st, _ = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(
         variant="persistent_2cta", block_k=128, pipe_depth=4))
     assert st == b.GEMM_ERR_UNSUPPORTED and "does not fit" in b.last_error()
-    st, _ = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(variant="persistent",
-                                                                     block_k=128))
-    assert st == b.GEMM_ERR_INVALID_ARG
+    # the lock-step ladder has single-block stages only; K = 256 stages are
+    # built for the single-CTA warp-specialised kernel only
+    for v, bk in (("pipelined", 128), ("persistent_lockstep", 128), ("tma_serial", 128),
+                  ("persistent_2cta", 256), ("dynamic_2cta", 256), ("pipelined", 256)):
+        st, _ = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(variant=v, block_k=bk))
+        assert st == b.GEMM_ERR_INVALID_ARG, (v, bk)
     st, _ = b.gemm_select_config(8192, 8192, 8192, 1, b.make_options(block_k=96))
     assert st == b.GEMM_ERR_INVALID_ARG
     # stream-K (static pair schedule) splits K in 128-wide stages: the 36-tile
@@ -498,3 +501,38 @@ def test_plan_invariants_over_random_shapes(b):
             assert c.a_rows == 128 or (c.a_rows == 64 and M <= 64 and not pair), where
             if var in (5, 7):
                 assert c.grid <= 152, where
+
+
+def test_single_cta_multi_block_stages(b):
+    # The single-CTA warp-specialised kernel takes stages of 2 or 4 K blocks of
+    # 64: ksub sub-slots per stage, the byte budget ksub times one block's,
+    # and as many stages as fit.
+    for v in ("persistent", "ws_pipelined"):
+        for bk, ks in ((64, 1), (128, 2), (256, 4)):
+            st, c = b.gemm_select_config(1000, 1000, 1000, 1,
+                                         b.make_options(variant=v, block_k=bk, block_n=128))
+            assert st == 0, b.last_error()
+            per_block = (128 * 64 + 128 * 64) * 2
+            assert (c.block_k, c.tx_bytes, c.k_blocks) == (bk, ks * per_block, 16)
+            assert c.pipe_depth == {1: 6, 2: 3, 4: 1}[ks], (v, bk, c.pipe_depth)
+            assert c.smem_bytes <= 232448
+    # at most 64 rows: 64-row A slots, so twice as many stages of 4 blocks fit
+    st, c = b.gemm_select_config(64, 16384, 16384, 1, b.make_options(variant="persistent",
+                                                                     block_k=256))
+    assert st == 0 and (c.a_rows, c.block_k, c.pipe_depth) == (64, 256, 2)
+    assert c.tx_bytes == 4 * (64 * 64 + 128 * 64) * 2
+    # an explicit depth must fit in stages of the asked K extent
+    st, _ = b.gemm_select_config(64, 16384, 16384, 1, b.make_options(
+        variant="persistent", block_k=256, pipe_depth=3))
+    assert st == b.GEMM_ERR_UNSUPPORTED and "does not fit" in b.last_error()
+
+
+def test_single_cta_stream_k_in_multi_block_stages(b):
+    # the units of a stream-K split are stages of the plan's K extent; the
+    # automatic skinny plan keeps single-block stages
+    st, c = b.gemm_select_config(64, 16384, 16384, 1)
+    assert st == 0 and (c.variant, c.block_n, c.block_k, c.pipe_depth) == (5, 128, 64, 8)
+    st, c = b.gemm_select_config(64, 16384, 16384, 1, b.make_options(
+        variant="persistent", block_k=256, stream_k="on", grid=152))
+    assert st == 0 and c.block_k == 256 and c.sk_tiles > 0
+    _assert_units_cover(b, c)

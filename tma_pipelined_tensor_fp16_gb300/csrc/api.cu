@@ -234,8 +234,8 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
         return fail(GEMM_ERR_INVALID_ARG, "stream_k must be 0 (auto), 1 (off) or 2 (on)");
     if (opts.l2_policy < 0 || opts.l2_policy > 3)
         return fail(GEMM_ERR_INVALID_ARG, "l2_policy must be 0..3");
-    if (opts.block_k != 0 && opts.block_k != 64 && opts.block_k != 128)
-        return fail(GEMM_ERR_INVALID_ARG, "block_k must be 0 (auto), 64 or 128");
+    if (opts.block_k != 0 && opts.block_k != 64 && opts.block_k != 128 && opts.block_k != 256)
+        return fail(GEMM_ERR_INVALID_ARG, "block_k must be 0 (auto), 64, 128 or 256");
     if (opts.k_order < 0 || opts.k_order > 2)
         return fail(GEMM_ERR_INVALID_ARG, "k_order must be 0 (auto), 1 (ascending) or 2 (snake)");
     if (sms < 1 || smem_optin < 1) return fail(GEMM_ERR_INVALID_ARG, "bad device limits");
@@ -246,8 +246,16 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     if (is_dynamic(variant) && opts.grid != 0)
         return fail(GEMM_ERR_INVALID_ARG,
                     "the dynamic variant launches one cluster per work unit: grid must be 0 (auto)");
-    if (opts.block_k == 128 && !is_pair(variant))
-        return fail(GEMM_ERR_INVALID_ARG, "block_k = 128 is built for the CTA-pair variants");
+    // the single-CTA warp-specialised kernel
+    const bool single_ws = variant == VAR_PERSISTENT || variant == VAR_WS_PIPELINED;
+    if (opts.block_k == 128 && !is_pair(variant) && !single_ws)
+        return fail(GEMM_ERR_INVALID_ARG,
+                    "block_k = 128 is built for the warp-specialised variants");
+    if (opts.block_k == 256 && !single_ws)
+        return fail(GEMM_ERR_INVALID_ARG,
+                    "block_k = 256 is built for the single-CTA warp-specialised variants");
+    // A problem of at most 64 rows keeps 64-row A slots (more stages fit).
+    const int a_rows = (M <= 64 && single_ws) ? 64 : BLK_M;
     // K blocks of 64 per stage (two 128-byte swizzle atoms at block_k = 128).
     // Automatic for CTA pairs whose operand rows are 128-byte aligned (K a
     // multiple of 64), unless an explicit ring depth is asked for (a depth
@@ -259,7 +267,17 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     // straddles two lines and the wider stages lose: 1128-1143 vs 1162-1178.
     const bool auto_k128 =
         opts.block_k == 0 && is_pair(variant) && opts.pipe_depth == 0 && K % 64 == 0;
-    const int ksub = (opts.block_k == 128 || auto_k128) ? 2 : 1;
+    // Stages of 2 or 4 K blocks are also built for the single-CTA kernel but
+    // not chosen automatically.  A read-only stream of the skinny shape's B
+    // (16384 x 16384) in the GEMM's pattern measured 5.60 TB/s with 128-byte
+    // pieces per row and stage, 5.99 with 256-byte and 6.12 with 512-byte
+    // pieces (192 KB of ring each); but the GEMM's ring holds only 128 KB of
+    // B beside A's slots and the output staging, and each stage stays taken
+    // until its MMAs commit, so 64 x 16384 x 16384 measured 100.3 / 99.3 /
+    // 100.3 us with stages of 1 / 2 / 4 blocks.
+    const int ksub = opts.block_k == 256                   ? 4
+                     : (opts.block_k == 128 || auto_k128) ? 2
+                                                          : 1;
     if (is_pair(variant) && opts.block_n != 0 && !pair_width_ok(opts.block_n))
         return fail(GEMM_ERR_INVALID_ARG,
                     "CTA-pair tile width (block_n) must be 128, 160, 192, 224 or 256");
@@ -271,9 +289,6 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
     const int bn_cta = is_pair(variant) ? bn / 2 : bn;
     const int bm = is_pair(variant) ? 2 * BLK_M : BLK_M;
     const int staging = variant == VAR_SYNC_TILED ? 0 : NUM_STAGING;
-    // A problem of at most 64 rows keeps 64-row A slots (more stages fit).
-    const int a_rows = (M <= 64 && (variant == VAR_PERSISTENT || variant == VAR_WS_PIPELINED))
-                           ? 64 : BLK_M;
 
     int depth;
     if (!has_ring(variant)) {
@@ -373,7 +388,7 @@ int select_config_impl(int64_t M, int64_t N, int64_t K, int dtype, const gemm_op
         c->tmem_cols = alloc;
     }
     c->tx_bytes = static_cast<int>(is_pair(variant) ? 2 * stage_tx_bytes(bn_cta) * ksub
-                                                    : stage_tx_bytes(bn, a_rows));
+                                                    : stage_tx_bytes(bn, a_rows) * ksub);
     c->a_rows = a_rows;
 
     // Stream-K tail: whole waves stay data-parallel; the tiles of a partial

@@ -17,6 +17,13 @@
 //   warps 2..5         epilogue: wait tmem_full[acc], TMEM -> regs -> swizzled
 //                      staging -> TMA store, arrive tmem_empty[acc].
 //
+// A pipeline stage spans p.ksub (1, 2 or 4) K blocks of 64, each in a
+// sub-slot of its own (sub-slot stage * ksub + s): one barrier round trip per
+// ksub x 4 MMAs, and each row of an operand tile is read as ksub adjacent
+// 128-byte pieces ("05 Async Data Movement - TMA", Using 3D TMA to Move
+// Multiple Swizzle Atoms, loaded here as ksub 2-D boxes).  A block of the last
+// stage that lies past K arrives zero-filled and is not multiplied.
+//
 // PERSIST = false: one output tile per CTA, one accumulator (grid = tiles).
 // PERSIST = true : grid = SM count; each CTA walks the grouped raster
 // (t = blockIdx.x, + gridDim.x, ...), TMEM is allocated once for two
@@ -67,10 +74,11 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
     constexpr int ACC = PERSIST ? 2 : 1;
     constexpr uint32_t TMEM_COLS = ACC * BN;  // 64..512, a power of two
     const int D = p.pipe_depth;
+    const int KS = p.ksub == 2 || p.ksub == 4 ? p.ksub : 1;  // K blocks of 64 per stage
     const CtaSmem sm = cta_smem();
     const int a_rows = p.a_rows == 64 ? 64 : BLK_M;
     const uint32_t a_slot = a_slot_bytes(a_rows);
-    const SmemLayout L = smem_layout(D, BN, NUM_STAGING, a_rows);
+    const SmemLayout L = smem_layout(D * KS, BN, NUM_STAGING, a_rows);
     const uint32_t sA = sm.base + L.a;
     const uint32_t sB = sm.base + L.b;
     const uint32_t staging = sm.base + L.staging;
@@ -81,7 +89,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
     const uint32_t lane = lane_id();
     Watchdog wd = make_watchdog(p);
     const int workers = PERSIST ? static_cast<int>(gridDim.x) : p.num_tiles;
-    const int KB = p.k_blocks;
+    const int KB = (p.k_blocks + KS - 1) / KS;  // stages per tile
     WorkIter units0;
     units0.init(static_cast<int>(blockIdx.x), workers, PERSIST ? p.dp_tiles : p.num_tiles,
                 PERSIST ? p.sk_tiles : 0, KB, p.sk_kb_per_worker);
@@ -124,7 +132,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
     // the other lanes parked at a warp barrier, measured up to 9% slower).
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
-        const uint32_t tx = stage_tx_bytes(BN, a_rows);
+        // every box's full bytes, including those of a block past K
+        const uint32_t tx = stage_tx_bytes(BN, a_rows) * static_cast<uint32_t>(KS);
         const uint64_t pol_a = (p.l2_policy == 2) ? policy_evict_first() : policy_evict_last();
         const uint64_t pol_b = (p.l2_policy == 1) ? policy_evict_first() : policy_evict_last();
         const bool tr = p.trace && lane == 0;
@@ -158,13 +167,17 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
                 if (lane == 0 && ok) {
                     const uint32_t fb = bar_addr(bars, BAR_FULL + stage);
                     mbar_arrive_expect_tx(fb, tx);
-                    if (p.l2_policy == 0) {
-                        tma_load_2d(sA + stage * a_slot, &tmA, fb, kb * BLK_K, m0);
-                        tma_load_2d(sB + stage * b_tile_bytes(BN), &tmB, fb, kb * BLK_K, n0);
-                    } else {
-                        tma_load_2d_hint(sA + stage * a_slot, &tmA, fb, kb * BLK_K, m0, pol_a);
-                        tma_load_2d_hint(sB + stage * b_tile_bytes(BN), &tmB, fb, kb * BLK_K, n0,
-                                         pol_b);
+                    for (int s = 0; s < KS; ++s) {
+                        const int slot = stage * KS + s;
+                        const int kx = (kb * KS + s) * BLK_K;
+                        if (p.l2_policy == 0) {
+                            tma_load_2d(sA + slot * a_slot, &tmA, fb, kx, m0);
+                            tma_load_2d(sB + slot * b_tile_bytes(BN), &tmB, fb, kx, n0);
+                        } else {
+                            tma_load_2d_hint(sA + slot * a_slot, &tmA, fb, kx, m0, pol_a);
+                            tma_load_2d_hint(sB + slot * b_tile_bytes(BN), &tmB, fb, kx, n0,
+                                             pol_b);
+                        }
                     }
                     ++issued;
                 }
@@ -226,13 +239,18 @@ __global__ void __launch_bounds__(WS_THREADS, 1) k_ws(const __grid_constant__ CU
                 if (lane == 0 && ok) {
                     tc_fence_after_sync();
                     if (tr && ki == 0) trace_unit(p, mui, TRACE_U_MMA_FIRST, globaltimer_ns());
-                    const uint64_t adesc = sw128_kmajor_desc(sA + stage * a_slot);
-                    const uint64_t bdesc = sw128_kmajor_desc(sB + stage * b_tile_bytes(BN));
+                    for (int s = 0; s < KS; ++s) {
+                        // a block of the last stage may lie past K
+                        if (s > 0 && kb * KS + s >= p.k_blocks) break;
+                        const int slot = stage * KS + s;
+                        const uint64_t adesc = sw128_kmajor_desc(sA + slot * a_slot);
+                        const uint64_t bdesc = sw128_kmajor_desc(sB + slot * b_tile_bytes(BN));
 #pragma unroll
-                    for (int kk = 0; kk < BLK_K / MMA_K; ++kk)
-                        mma_f16_ss(d_tmem, adesc + static_cast<uint64_t>(kk * 2),
-                                   bdesc + static_cast<uint64_t>(kk * 2), idesc,
-                                   (ki == 0 && kk == 0) ? 0u : 1u);
+                        for (int kk = 0; kk < BLK_K / MMA_K; ++kk)
+                            mma_f16_ss(d_tmem, adesc + static_cast<uint64_t>(kk * 2),
+                                       bdesc + static_cast<uint64_t>(kk * 2), idesc,
+                                       (ki == 0 && s == 0 && kk == 0) ? 0u : 1u);
+                    }
                     // frees the stage once these MMAs have read it
                     mma_commit(bar_addr(bars, BAR_EMPTY + stage));
                 }
