@@ -119,9 +119,10 @@ struct Params {
     // odd.  With snake_span equal to the static schedule's cluster count,
     // every tile walks K in the same direction under both schedules.
     int snake_span;
-    // K blocks of 64 per pipeline stage in the CTA-pair kernel: 1, or 2 (a
-    // stage of K = 128 as two 128-byte swizzle atoms, one barrier round trip
-    // per 8 MMAs).  The single-CTA kernels use 1.
+    // K blocks of 64 per pipeline stage in the warp-specialised kernels: 1,
+    // 2 or (single-CTA kernel only) 4; a stage of K = 64 * ksub as that many
+    // 128-byte swizzle atoms, one barrier round trip per 4 * ksub MMAs.  The
+    // lock-step ladder kernels use 1.
     int ksub;
     // Dynamic pair schedule, narrow tail: the last `tail_halves` tiles are
     // each computed as two half-width tiles (see dynamic_unit); 0 = none.
