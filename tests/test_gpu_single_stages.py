@@ -93,6 +93,20 @@ def test_multi_block_many_tiles_per_cta(block_k, grid):
 
 
 @pytest.mark.parametrize("block_k", [128, 256])
+@pytest.mark.parametrize("out", ["f32", "f16"])
+def test_multi_block_stream_k_integer_bit_exact(block_k, out):
+    # partial sums of K-stage ranges added in a fixed order: exact on
+    # integer inputs, and the same bits on every run
+    M, N, K = 64, 8192, 2056
+    A, B = inputs.make_operands(M, N, K, "int", 93)
+    got, _, desc = run(A, B, out, variant="persistent", block_k=block_k, stream_k="on", grid=152)
+    assert "stream_k=0/" not in desc, desc
+    assert_exact(got, oracle.gemm(A, B), out, desc)
+    again, _, _ = run(A, B, out, variant="persistent", block_k=block_k, stream_k="on", grid=152)
+    assert np.array_equal(got.view(np.uint8), again.view(np.uint8)), "run-to-run difference"
+
+
+@pytest.mark.parametrize("block_k", [128, 256])
 def test_multi_block_stream_k(block_k):
     # stream-K over 152 CTAs splits the tiles of the partial last wave in
     # ranges of stages; partial sums meet in the workspace
