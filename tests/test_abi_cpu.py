@@ -66,6 +66,12 @@ def test_create_plan_without_device_reports_no_device(b):
     ((8, 6, 8, 0), 2),         # N*4 bytes not a multiple of 16
     ((8, 12, 8, 1), 2),        # N*2 bytes not a multiple of 16
     ((8, 12, 8, 0), 0),        # N*4 = 48 bytes: fine for fp32 output
+    # the largest sizes the ABI takes (each below 2^31), and one past them
+    ((2 ** 31 - 1, 8, 8, 0), 0), ((2 ** 31, 8, 8, 0), 1),
+    ((8, 2 ** 31 - 8, 8, 0), 0), ((8, 2 ** 31 + 8, 8, 0), 1),
+    ((8, 8, 2 ** 31 - 8, 0), 0), ((8, 8, 2 ** 31 + 8, 0), 1),
+    # legal sizes whose tile count does not fit the schedule's 31-bit indices
+    ((2 ** 31 - 8, 2 ** 31 - 8, 8, 1), 2),
 ])
 def test_argument_checks(b, args, status):
     st, _ = b.gemm_select_config(*args)
