@@ -26,8 +26,9 @@ def _built():
     __graft_entry__.build()
 
 
-@pytest.mark.parametrize("variant", ["persistent", "ws_pipelined"])
-def test_stalled_wait_times_out_and_context_survives(variant):
+@pytest.mark.parametrize("variant,block_k", [("persistent", 64), ("ws_pipelined", 64),
+                                             ("persistent", 256), ("ws_pipelined", 128)])
+def test_stalled_wait_times_out_and_context_survives(variant, block_k):
     import time
 
     import torch
@@ -39,7 +40,8 @@ def test_stalled_wait_times_out_and_context_survives(variant):
     dA = torch.from_numpy(A.view(np.float16)).cuda()
     dB = torch.from_numpy(B.view(np.float16)).cuda()
     C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
-    plan = pkg.Plan(M, N, K, out="f32", variant=variant, debug_stall=1, wait_budget_ms=100)
+    plan = pkg.Plan(M, N, K, out="f32", variant=variant, debug_stall=1, wait_budget_ms=100,
+                    block_k=block_k)
     t0 = time.time()
     plan(dA, dB, C)
     torch.cuda.synchronize()
@@ -51,5 +53,5 @@ def test_stalled_wait_times_out_and_context_survives(variant):
     assert plan.device_status() == binding.GEMM_OK
     plan.close()
     # the context is intact: a normal run right after is correct
-    got, _, desc = run(A, B, "f32", variant=variant)
+    got, _, desc = run(A, B, "f32", variant=variant, block_k=block_k)
     assert_close(got, oracle.gemm(A, B), K, "f32", "after timeout: " + desc)
